@@ -1,0 +1,320 @@
+"""Pins for the oracle: checks against facts that the method and mathematics
+fix, independent of the oracle's own code.
+
+Each ``pin_*`` takes a loaded oracle library (ctypes handle) and raises
+AssertionError when the oracle disagrees.  ``test_oracle_pins.py`` runs them
+on the real oracle and, to show that they bite, on copies of the oracle with
+planted mistakes.
+
+Sources of truth (review page "Transformers are RNNs: Fast Autoregressive
+Transformers with Linear Attention", section "proposed method" b1-b5, and
+section "main results" b2 for the elu-based map; review page "Stable, Fast
+and Accurate: Kernelized Attention with Relative Positional Encoding",
+section "proposed method" b6, for positive random features):
+  - brute force of the masked quadratic form in pure Python on tiny inputs;
+  - exact rational arithmetic where phi(x) = x + 1 (all inputs > 0);
+  - closed forms: equal keys give the running mean of V, constant V gives V;
+  - special cases that reduce to library routines: with D = 1 and keys <= 0
+    the elu+1 map gives causal softmax over the keys; with m = 1 the PRF map
+    gives causal softmax over w.k - |k|^2/2; elu(x) + 1 from torch;
+  - invariants: convex hull, last causal row = non-causal row, the recurrent
+    step iterated N times = the forward pass, head and key/value
+    permutations, linearity in V;
+  - the PRF kernel's expectation E_w[phi(q).phi(k)] = exp(q.k).
+"""
+from __future__ import annotations
+
+import math
+from fractions import Fraction
+
+import numpy as np
+import scipy.special
+import torch
+
+import oracle
+
+RTOL = 1e-12
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _close(a, b, rtol=RTOL, atol=0.0, what=""):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    assert a.shape == b.shape, (what, a.shape, b.shape)
+    assert np.all(np.isfinite(a)), f"{what}: non-finite values"
+    scale = max(np.max(np.abs(b)), 1e-300)
+    err = np.max(np.abs(a - b)) if a.size else 0.0
+    assert err <= rtol * scale + atol, f"{what}: max err {err:.3e} vs scale {scale:.3e}"
+
+
+# ---------------------------------------------------------------- brute force
+
+def _py_phi(x, feature, W):
+    if feature == "elu1":
+        return [xi + 1.0 if xi > 0 else math.exp(xi) for xi in x]
+    m = len(W)
+    sq = sum(xi * xi for xi in x)
+    return [math.exp(sum(w * xi for w, xi in zip(W[r], x)) - sq / 2) / math.sqrt(m)
+            for r in range(m)]
+
+
+def _py_attention(q, k, v, causal, feature, W):
+    """sum_j (phi(q_i).phi(k_j)) v_j / sum_j phi(q_i).phi(k_j), pure Python."""
+    N, Dv = len(q), len(v[0])
+    fk = [_py_phi(kj, feature, W) for kj in k]
+    out = []
+    for i in range(N):
+        fq = _py_phi(q[i], feature, W)
+        J = range(i + 1) if causal else range(N)
+        num = [0.0] * Dv
+        den = 0.0
+        for j in J:
+            w = sum(a * b for a, b in zip(fq, fk[j]))
+            den += w
+            for c in range(Dv):
+                num[c] += w * v[j][c]
+        out.append([x / den for x in num])
+    return out
+
+
+def pin_pure_python_brute_force(lib):
+    r = _rng(1)
+    for (N, D, Dv, feature, m) in [(7, 3, 2, "elu1", 0), (9, 2, 5, "elu1", 0),
+                                   (6, 3, 4, "prf", 5), (5, 1, 1, "elu1", 0)]:
+        q = r.normal(size=(1, 2, N, D))
+        k = r.normal(size=(1, 2, N, D))
+        v = r.normal(size=(1, 2, N, Dv))
+        W = r.normal(size=(m, D)) if feature == "prf" else None
+        Wl = W.tolist() if W is not None else None
+        for causal in (True, False):
+            got = oracle.forward(q, k, v, causal=causal, feature=feature, W=W, lib=lib)
+            for h in range(2):
+                ref = _py_attention(q[0, h].tolist(), k[0, h].tolist(), v[0, h].tolist(),
+                                    causal, feature, Wl)
+                _close(got[0, h], ref, what=f"brute force {feature} causal={causal} N={N}")
+
+
+def pin_exact_rational(lib):
+    """All q, k > 0: phi(x) = x + 1 exactly, so the causal output is rational."""
+    r = _rng(2)
+    N, D, Dv = 8, 3, 2
+    qi = r.integers(1, 17, size=(N, D))
+    ki = r.integers(1, 17, size=(N, D))
+    vi = r.integers(-16, 17, size=(N, Dv))
+    q = [[Fraction(int(x), 8) for x in row] for row in qi]
+    k = [[Fraction(int(x), 8) for x in row] for row in ki]
+    v = [[Fraction(int(x), 4) for x in row] for row in vi]
+    exact = []
+    for i in range(N):
+        num = [Fraction(0)] * Dv
+        den = Fraction(0)
+        for j in range(i + 1):
+            w = sum((a + 1) * (b + 1) for a, b in zip(q[i], k[j]))
+            den += w
+            num = [n + w * vj for n, vj in zip(num, v[j])]
+        exact.append([float(n / den) for n in num])
+    to = lambda M: np.array([[float(x) for x in row] for row in M])[None, None]
+    got = oracle.forward(to(q), to(k), to(v), causal=True, lib=lib)
+    _close(got[0, 0], exact, rtol=1e-14, what="exact rational")
+
+
+def pin_oracle_quadratic_vs_recurrence(lib):
+    r = _rng(3)
+    for (N, D, Dv, feature, m) in [(256, 1, 3, "elu1", 0), (200, 4, 4, "elu1", 0),
+                                   (256, 16, 8, "elu1", 0), (128, 4, 6, "prf", 16),
+                                   (96, 16, 16, "prf", 8)]:
+        q = r.normal(size=(1, 2, N, D))
+        k = r.normal(size=(1, 2, N, D))
+        v = r.normal(size=(1, 2, N, Dv))
+        W = r.normal(size=(m, D)) if feature == "prf" else None
+        for causal in (True, False):
+            a = oracle.forward(q, k, v, causal=causal, feature=feature, W=W, lib=lib)
+            b = oracle.quadratic(q, k, v, causal=causal, feature=feature, W=W, lib=lib)
+            _close(a, b, rtol=1e-11, what=f"quadratic vs recurrence {feature} {causal}")
+
+
+# ------------------------------------------------------------- closed forms
+
+def pin_equal_keys_running_mean(lib):
+    r = _rng(4)
+    N, D, Dv = 50, 6, 3
+    q = r.normal(size=(1, 1, N, D))
+    k = np.broadcast_to(r.normal(size=(D,)), (1, 1, N, D)).copy()
+    v = r.normal(size=(1, 1, N, Dv))
+    mean = np.cumsum(v[0, 0], axis=0) / np.arange(1, N + 1)[:, None]
+    for feature, W in (("elu1", None), ("prf", r.normal(size=(7, D)))):
+        got = oracle.forward(q, k, v, causal=True, feature=feature, W=W, lib=lib)
+        _close(got[0, 0], mean, rtol=1e-12, what=f"running mean {feature}")
+        got = oracle.forward(q, k, v, causal=False, feature=feature, W=W, lib=lib)
+        _close(got[0, 0], np.broadcast_to(v[0, 0].mean(0), (N, Dv)), rtol=1e-12,
+               what=f"mean {feature}")
+
+
+def pin_constant_values(lib):
+    r = _rng(5)
+    N, D, Dv = 40, 5, 4
+    q = r.normal(size=(2, 1, N, D))
+    k = r.normal(size=(2, 1, N, D))
+    c = r.normal(size=(Dv,))
+    v = np.broadcast_to(c, (2, 1, N, Dv)).copy()
+    for causal in (True, False):
+        got = oracle.forward(q, k, v, causal=causal, lib=lib)
+        _close(got, np.broadcast_to(c, got.shape), rtol=1e-13, what="constant v")
+
+
+def pin_elu_is_torch_elu_plus_one(lib):
+    x = np.linspace(-6, 6, 241)
+    x = np.concatenate([x, [0.0, -0.0, 1e-300, -1e-300, 30.0, -30.0]])
+    got = oracle.phi(x[:, None], "elu1", lib=lib)[:, 0]
+    ref = torch.nn.functional.elu(torch.tensor(x, dtype=torch.float64), alpha=1.0).numpy() + 1
+    _close(got, ref, rtol=1e-15, what="elu+1")
+
+
+def pin_elu_d1_negative_keys_is_softmax(lib):
+    """D = 1 and k <= 0: weights phi(q)exp(k_j), q cancels -> softmax over k."""
+    r = _rng(6)
+    N = 30
+    q = r.normal(size=(1, 1, N, 1))
+    k = -np.abs(r.normal(size=(1, 1, N, 1))) * 3
+    v = r.normal(size=(1, 1, N, 3))
+    got = oracle.forward(q, k, v, causal=True, lib=lib)[0, 0]
+    ref = np.stack([scipy.special.softmax(k[0, 0, :i + 1, 0]) @ v[0, 0, :i + 1]
+                    for i in range(N)])
+    _close(got, ref, rtol=1e-13, what="softmax special case")
+
+
+def pin_elu_d1_positive_keys_linear_weights(lib):
+    """D = 1 and k > 0: weights proportional to k_j + 1."""
+    r = _rng(7)
+    N = 30
+    q = r.normal(size=(1, 1, N, 1))
+    k = np.abs(r.normal(size=(1, 1, N, 1))) + 0.01
+    v = r.normal(size=(1, 1, N, 2))
+    w = k[0, 0, :, 0] + 1
+    ref = np.stack([np.average(v[0, 0, :i + 1], axis=0, weights=w[:i + 1]) for i in range(N)])
+    got = oracle.forward(q, k, v, causal=True, lib=lib)[0, 0]
+    _close(got, ref, rtol=1e-13, what="linear-weight special case")
+
+
+def pin_prf_m1_is_softmax(lib):
+    """m = 1: phi(q) cancels; weights exp(w.k_j - |k_j|^2/2) -> a softmax."""
+    r = _rng(8)
+    N, D = 25, 4
+    W = r.normal(size=(1, D))
+    q = r.normal(size=(1, 1, N, D))
+    k = r.normal(size=(1, 1, N, D))
+    v = r.normal(size=(1, 1, N, 3))
+    logits = k[0, 0] @ W[0] - 0.5 * np.sum(k[0, 0] ** 2, axis=1)
+    ref = np.stack([scipy.special.softmax(logits[:i + 1]) @ v[0, 0, :i + 1] for i in range(N)])
+    got = oracle.forward(q, k, v, causal=True, feature="prf", W=W, lib=lib)[0, 0]
+    _close(got, ref, rtol=1e-12, what="PRF m=1 softmax")
+    got = oracle.forward(q, k, v, causal=False, feature="prf", W=W, lib=lib)[0, 0]
+    _close(got, np.broadcast_to(ref[-1], got.shape), rtol=1e-12, what="PRF m=1 non-causal")
+
+
+def pin_prf_kernel_expectation(lib):
+    """E over w ~ N(0, I) of phi(q).phi(k) = exp(q.k) (standard PRF identity).
+
+    With m = 2**16 features the sample mean is within a few standard errors.
+    """
+    r = _rng(9)
+    D, m = 4, 1 << 16
+    W = r.normal(size=(m, D))
+    for _ in range(3):
+        q = r.normal(size=D) * 0.4
+        k = r.normal(size=D) * 0.4
+        fq = oracle.phi(q[None], "prf", W, lib=lib)[0]
+        fk = oracle.phi(k[None], "prf", W, lib=lib)[0]
+        est = float(fq @ fk)
+        # per-feature terms t_r = m * fq_r * fk_r have mean exp(q.k)
+        t = m * fq * fk
+        se = t.std() / math.sqrt(m)
+        target = math.exp(float(q @ k))
+        assert abs(est - target) < 5 * se + 1e-12, (est, target, se)
+        assert np.all(fq > 0) and np.all(fk > 0)
+
+
+# ------------------------------------------------------------- invariants
+
+def pin_convex_hull(lib):
+    r = _rng(10)
+    N, D, Dv = 64, 8, 5
+    q, k, v = (r.normal(size=(1, 2, N, x)) for x in (D, D, Dv))
+    got = oracle.forward(q, k, v, causal=True, lib=lib)
+    lo = np.minimum.accumulate(v, axis=2)
+    hi = np.maximum.accumulate(v, axis=2)
+    assert np.all(got >= lo - 1e-12) and np.all(got <= hi + 1e-12)
+
+
+def pin_last_row_equals_noncausal(lib):
+    r = _rng(11)
+    N, D, Dv = 33, 7, 3
+    q, k, v = (r.normal(size=(2, 1, N, x)) for x in (D, D, Dv))
+    for feature, W in (("elu1", None), ("prf", r.normal(size=(9, D)))):
+        c = oracle.forward(q, k, v, causal=True, feature=feature, W=W, lib=lib)
+        n = oracle.forward(q, k, v, causal=False, feature=feature, W=W, lib=lib)
+        _close(c[:, :, -1], n[:, :, -1], rtol=1e-13, what=f"last row {feature}")
+
+
+def pin_step_iterated_equals_forward(lib):
+    r = _rng(12)
+    B, H, N, D, Dv = 2, 2, 20, 5, 3
+    for feature, W in (("elu1", None), ("prf", r.normal(size=(6, D)))):
+        P = oracle.phi_dim(D, feature, 0 if W is None else W.shape[0])
+        q, k, v = (r.normal(size=(B, H, N, x)) for x in (D, D, Dv))
+        ref, Sref, zref = oracle.forward(q, k, v, causal=True, feature=feature, W=W,
+                                         return_state=True, lib=lib)
+        S = np.zeros((B, H, P, Dv))
+        z = np.zeros((B, H, P))
+        outs = []
+        for i in range(N):
+            o, S, z = oracle.step(S, z, q[:, :, i], k[:, :, i], v[:, :, i], feature, W, lib=lib)
+            outs.append(o)
+        _close(np.stack(outs, axis=2), ref, rtol=1e-12, what=f"step x N {feature}")
+        _close(S, Sref, rtol=1e-12, what="final S")
+        _close(z, zref, rtol=1e-12, what="final z")
+        # resume: forward over the first N1 positions, then steps
+        N1 = 7
+        _, S1, z1 = oracle.forward(q[:, :, :N1], k[:, :, :N1], v[:, :, :N1], causal=True,
+                                   feature=feature, W=W, return_state=True, lib=lib)
+        for i in range(N1, N):
+            o, S1, z1 = oracle.step(S1, z1, q[:, :, i], k[:, :, i], v[:, :, i], feature, W,
+                                    lib=lib)
+            _close(o, ref[:, :, i], rtol=1e-12, what="resume")
+
+
+def pin_head_permutation(lib):
+    r = _rng(13)
+    N, D, Dv = 16, 4, 4
+    q, k, v = (r.normal(size=(1, 5, N, x)) for x in (D, D, Dv))
+    perm = r.permutation(5)
+    a = oracle.forward(q, k, v, causal=True, lib=lib)
+    b = oracle.forward(q[:, perm], k[:, perm], v[:, perm], causal=True, lib=lib)
+    _close(b, a[:, perm], rtol=0.0, what="head permutation")
+
+
+def pin_noncausal_key_permutation(lib):
+    r = _rng(14)
+    N, D, Dv = 31, 6, 2
+    q, k, v = (r.normal(size=(1, 1, N, x)) for x in (D, D, Dv))
+    perm = r.permutation(N)
+    a = oracle.forward(q, k, v, causal=False, lib=lib)
+    b = oracle.forward(q, k[:, :, perm], v[:, :, perm], causal=False, lib=lib)
+    _close(a, b, rtol=1e-13, what="key permutation")
+
+
+def pin_linear_in_v(lib):
+    r = _rng(15)
+    N, D, Dv = 24, 3, 4
+    q, k, v1, v2 = (r.normal(size=(1, 1, N, x)) for x in (D, D, Dv, Dv))
+    for causal in (True, False):
+        a = oracle.forward(q, k, 2.0 * v1 - 3.0 * v2, causal=causal, lib=lib)
+        b = 2.0 * oracle.forward(q, k, v1, causal=causal, lib=lib) \
+            - 3.0 * oracle.forward(q, k, v2, causal=causal, lib=lib)
+        _close(a, b, rtol=1e-12, what="linearity")
+
+
+ALL_PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_")]

@@ -1,0 +1,77 @@
+"""The oracle against its pins, and the pins against planted mistakes.
+
+The mutation test copies ``oracle/oracle.c``, plants one plausible mistake
+(a dropped term, a wrong sign or index, a transposed operand), compiles the
+copy on the CPU and checks that at least one pin rejects it.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import oracle_pins
+
+ORACLE_SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+
+@pytest.mark.parametrize("pin", oracle_pins.ALL_PINS, ids=lambda p: p.__name__)
+def test_pin(pin, oracle_lib):
+    pin(oracle_lib)
+
+
+CAUSAL_BODY = (
+    "            update_state(S, z, fk, vi, P, Dv);\n"
+    "            oracle_phi(qi, D, kind, W, m, fq);\n"
+    "            readout(S, z, fq, out + (h * N + i) * Dv, P, Dv);\n"
+)
+CAUSAL_BODY_EXCLUSIVE = (
+    "            oracle_phi(qi, D, kind, W, m, fq);\n"
+    "            readout(S, z, fq, out + (h * N + i) * Dv, P, Dv);\n"
+    "            update_state(S, z, fk, vi, P, Dv);\n"
+)
+
+MUTATIONS = {
+    "elu_drops_plus_one": ("return x + 1.0;", "return x;"),
+    "elu_wrong_sign": ("return exp(x);", "return exp(-x);"),
+    "elu_wrong_branch": ("if (x > 0.0)", "if (x > 1.0)"),
+    "prf_wx_sign": ("f[r] = exp(wx - 0.5 * sq)", "f[r] = exp(-wx - 0.5 * sq)"),
+    "prf_drops_half": ("f[r] = exp(wx - 0.5 * sq)", "f[r] = exp(wx - sq)"),
+    "prf_drops_norm": ("f[r] = exp(wx - 0.5 * sq)", "f[r] = exp(wx)"),
+    "prf_scale_1_over_m": ("1.0 / sqrt((double)m)", "1.0 / (double)m"),
+    "prf_transposed_W": ("W[(long)r * D + d]", "W[(long)d * m + r]"),
+    "causal_exclusive": (CAUSAL_BODY, CAUSAL_BODY_EXCLUSIVE),
+    "state_transposed": ("S[(long)a * Dv + c] += fk[a] * v[c];",
+                         "S[(long)c * P + a] += fk[a] * v[c];"),
+    "den_drops_phi_q": ("den += fq[a] * z[a];", "den += z[a];"),
+    "num_wrong_index": ("num += fq[a] * S[(long)a * Dv + c];",
+                        "num += fq[c % P] * S[(long)a * Dv + c];"),
+    "noncausal_drops_last_key": ("for (long j = 0; j < N; j++) {\n            oracle_phi(k + (h * N + j)",
+                                 "for (long j = 0; j < N - 1; j++) {\n            oracle_phi(k + (h * N + j)"),
+    "step_wrong_v_offset": ("update_state(Sh, zh, f, v + h * Dv, P, Dv);",
+                            "update_state(Sh, zh, f, v + h * D, P, Dv);"),
+    "quadratic_strict_mask": ("long last = causal ? i : N - 1;",
+                              "long last = causal ? i - 1 : N - 1;"),
+    "z_not_accumulated": ("z[a] += fk[a];", "z[a] = fk[a];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_reject_planted_mistake(name, tmp_path):
+    old, new = MUTATIONS[name]
+    src = open(ORACLE_SRC).read()
+    assert src.count(old) >= 1, f"mutation anchor not found for {name}"
+    mutated = src.replace(old, new)
+    c_path = tmp_path / "oracle_mut.c"
+    so_path = tmp_path / "liboracle_mut.so"
+    c_path.write_text(mutated)
+    subprocess.check_call(["gcc", "-O1", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+                           str(c_path), "-o", str(so_path), "-lm"])
+    lib = oracle.load(str(so_path))
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(lib)
+        except (AssertionError, FloatingPointError, ValueError, ZeroDivisionError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin rejects the planted mistake {name}"
