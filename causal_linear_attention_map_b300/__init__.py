@@ -1,0 +1,223 @@
+"""Python binding of liblinattn.so, the B300 kernelized linear-attention library.
+
+Argument marshalling only: each function takes torch CUDA tensors, checks
+that they are contiguous CUDA tensors of one dtype, and passes their device
+pointers and sizes to the C entry point of the same name (``include/linattn.h``).
+Every step of the computation runs in the library's CUDA kernels.  There is
+no other implementation: if the library is not built, ``load()`` raises.
+
+    out            = la_forward(q, k, v, causal=True, feature_map=None)
+    out, S, z      = la_forward_ex(q, k, v, causal=True, feature_map=None)
+    out            = la_step(S, z, q, k, v)           # S, z updated in place
+
+Shapes: q, k [B, H, N, D]; v [B, H, N, Dv]; S [B, H, Dphi, Dv] fp32;
+z [B, H, Dphi] fp32; decode q, k [B, H, D], v [B, H, Dv].
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "liblinattn.so")
+
+LA_F32, LA_BF16 = 0, 1
+LA_PHI_ELU1, LA_PHI_PRF = 0, 1
+LA_OK = 0
+STATUS_NAMES = {0: "LA_OK", -1: "LA_ERR_NULL", -2: "LA_ERR_DIM", -3: "LA_ERR_DTYPE",
+                -4: "LA_ERR_FEATURE", -5: "LA_ERR_CUDA", -6: "LA_ERR_TIMEOUT",
+                -7: "LA_ERR_ALIGN"}
+EXPORTED = ("la_forward", "la_forward_ex", "la_step", "la_status_string", "la_check",
+            "la_shutdown", "la_version", "la_launch_count")
+
+_DT = {torch.float32: LA_F32, torch.bfloat16: LA_BF16}
+
+
+class la_feature_map(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("m", ctypes.c_int), ("W", ctypes.c_void_p)]
+
+
+class LinAttnError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+class FeatureMap:
+    """phi: ``FeatureMap()`` is elu(x)+1; ``FeatureMap("prf", W)`` uses the
+    m x D fp32 CUDA tensor W: phi_r(x) = exp(w_r.x - |x|^2/2)/sqrt(m)."""
+
+    def __init__(self, kind: str = "elu1", W: torch.Tensor | None = None):
+        if kind not in ("elu1", "prf"):
+            raise ValueError(kind)
+        self.kind = kind
+        self.W = W
+        if kind == "prf":
+            if W is None or W.dtype != torch.float32 or not W.is_cuda or not W.is_contiguous():
+                raise ValueError("PRF needs W as a contiguous fp32 CUDA tensor [m, D]")
+
+    @property
+    def m(self) -> int:
+        return self.W.shape[0] if self.kind == "prf" else 0
+
+    def phi_dim(self, D: int) -> int:
+        return self.m if self.kind == "prf" else D
+
+    def c_struct(self) -> la_feature_map:
+        if self.kind == "prf":
+            return la_feature_map(LA_PHI_PRF, self.W.shape[0], self.W.data_ptr())
+        return la_feature_map(LA_PHI_ELU1, 0, None)
+
+
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load liblinattn.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise ImportError(f"{p} is missing: build the CUDA library first "
+                          "(python -m causal_linear_attention_map_b300.build)")
+    lib = ctypes.CDLL(p)
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    fm = ctypes.POINTER(la_feature_map)
+    lib.la_forward.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, fm, i, vp]
+    lib.la_forward.restype = i
+    lib.la_forward_ex.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, fm, i, vp, vp, vp]
+    lib.la_forward_ex.restype = i
+    lib.la_step.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, fm, i, vp]
+    lib.la_step.restype = i
+    lib.la_status_string.argtypes = [i]
+    lib.la_status_string.restype = ctypes.c_char_p
+    lib.la_check.argtypes = [vp]
+    lib.la_check.restype = i
+    lib.la_shutdown.argtypes = []
+    lib.la_shutdown.restype = None
+    lib.la_version.argtypes = []
+    lib.la_version.restype = i
+    lib.la_launch_count.argtypes = []
+    lib.la_launch_count.restype = ctypes.c_ulonglong
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def la_status_string(status: int) -> str:
+    return load().la_status_string(status).decode()
+
+
+def _raise(st: int):
+    if st != LA_OK:
+        raise LinAttnError(st, la_status_string(st))
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check_tensors(*ts):
+    dt = ts[0].dtype
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("tensors must be CUDA tensors")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+        if t.dtype != dt:
+            raise ValueError("q, k, v, out must share one dtype")
+    if dt not in _DT:
+        raise ValueError(f"unsupported dtype {dt}")
+    return _DT[dt]
+
+
+def _fm(feature_map):
+    fm = feature_map or FeatureMap()
+    return fm, ctypes.byref(fm.c_struct())
+
+
+def la_forward_ex(q, k, v, causal=True, feature_map: FeatureMap | None = None, out=None,
+                  S_out=None, z_out=None, stream=None, return_state=True):
+    """la_forward_ex: returns (out, S, z); S/z are allocated when not given."""
+    B, H, N, D = q.shape
+    Dv = v.shape[-1]
+    if k.shape != q.shape or tuple(v.shape[:3]) != (B, H, N):
+        raise ValueError("shape mismatch between q, k, v")
+    if out is None:
+        out = torch.empty((B, H, N, Dv), dtype=q.dtype, device=q.device)
+    dt = _check_tensors(q, k, v, out)
+    fm, fmp = _fm(feature_map)
+    P = fm.phi_dim(D)
+    if return_state:
+        if S_out is None:
+            S_out = torch.empty((B, H, P, Dv), dtype=torch.float32, device=q.device)
+        if z_out is None:
+            z_out = torch.empty((B, H, P), dtype=torch.float32, device=q.device)
+    for t in (S_out, z_out):
+        if t is not None and (t.dtype != torch.float32 or not t.is_contiguous() or not t.is_cuda):
+            raise ValueError("S_out / z_out must be contiguous fp32 CUDA tensors")
+    st = load().la_forward_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                              B, H, N, D, Dv, int(bool(causal)), fmp, dt, _stream(stream),
+                              S_out.data_ptr() if S_out is not None else None,
+                              z_out.data_ptr() if z_out is not None else None)
+    _raise(st)
+    return out, S_out, z_out
+
+
+def la_forward(q, k, v, causal=True, feature_map: FeatureMap | None = None, out=None,
+               stream=None):
+    """la_forward: kernelized attention over whole sequences -> out [B,H,N,Dv]."""
+    B, H, N, D = q.shape
+    Dv = v.shape[-1]
+    if k.shape != q.shape or tuple(v.shape[:3]) != (B, H, N):
+        raise ValueError("shape mismatch between q, k, v")
+    if out is None:
+        out = torch.empty((B, H, N, Dv), dtype=q.dtype, device=q.device)
+    dt = _check_tensors(q, k, v, out)
+    _, fmp = _fm(feature_map)
+    st = load().la_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                           B, H, N, D, Dv, int(bool(causal)), fmp, dt, _stream(stream))
+    _raise(st)
+    return out
+
+
+def la_step(S, z, q, k, v, feature_map: FeatureMap | None = None, out=None, stream=None):
+    """la_step: one decode step; updates S [B,H,Dphi,Dv] and z [B,H,Dphi] in place."""
+    B, H, D = q.shape
+    Dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((B, H, Dv), dtype=q.dtype, device=q.device)
+    dt = _check_tensors(q, k, v, out)
+    for t in (S, z):
+        if t.dtype != torch.float32 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("S and z must be contiguous fp32 CUDA tensors")
+    _, fmp = _fm(feature_map)
+    st = load().la_step(S.data_ptr(), z.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                        out.data_ptr(), B, H, D, Dv, fmp, dt, _stream(stream))
+    _raise(st)
+    return out
+
+
+def la_check(stream=None) -> int:
+    """Synchronise the stream and return deferred device errors as a status."""
+    return load().la_check(_stream(stream))
+
+
+def la_shutdown() -> None:
+    load().la_shutdown()
+
+
+def la_version() -> int:
+    return load().la_version()
+
+
+def la_launch_count() -> int:
+    """Kernels launched by the library so far in this process."""
+    return load().la_launch_count()

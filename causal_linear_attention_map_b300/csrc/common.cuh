@@ -1,0 +1,35 @@
+// common.cuh -- small device helpers shared by the library's kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace la {
+
+// Input/output element types.
+template <typename T> __device__ __forceinline__ float to_f32(T x);
+template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x)
+{
+    return __bfloat162float(x);
+}
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x)
+{
+    return __float2bfloat16_rn(x);
+}
+
+// elu(x) + 1 with alpha = 1: x + 1 for x > 0, exp(x) otherwise
+// ("Transformers are RNNs", main results: the elu-based feature map).
+__device__ __forceinline__ float phi_elu1(float x) { return x > 0.f ? x + 1.f : expf(x); }
+
+// Same map with the fast exponential (MUFU ex2), for the bf16 paths whose
+// rounding is far coarser than its error.
+__device__ __forceinline__ float phi_elu1_fast(float x) { return x > 0.f ? x + 1.f : __expf(x); }
+
+__host__ __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+}  // namespace la

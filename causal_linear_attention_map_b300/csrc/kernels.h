@@ -1,0 +1,44 @@
+// kernels.h -- internal interface between the C ABI layer and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+namespace la {
+
+// Adds n to the library's launch counter (la_launch_count).
+void note_launches(int n);
+
+enum { DT_F32 = 0, DT_BF16 = 1 };
+enum { PHI_ELU1 = 0, PHI_PRF = 1 };
+
+// One validated forward problem.  Pointers are device pointers.
+struct Problem {
+    const void *q, *k, *v;
+    void *out;
+    long long BH;  // B * H heads
+    int N, D, Dv;
+    int P;         // feature dimension: D (elu+1) or m (PRF)
+    int kind;      // PHI_*
+    int m;
+    const float *W;
+    int dtype;     // DT_*
+};
+
+// CUDA-core (SIMT) chunked causal kernel, one CTA per head.  Any supported
+// size; the fp32 path and the fallback for shapes the tensor-core kernel
+// does not take.
+cudaError_t simt_causal(const Problem &p, float *S_out, float *z_out, cudaStream_t s);
+
+// Non-causal: KV = phi(K)^T V and ksum = sum phi(k) reduced over N into
+// fp32 scratch (KV [BH, P, Dv], ksum [BH, P]; zeroed here), then the readout.
+size_t noncausal_scratch_bytes(const Problem &p);
+cudaError_t noncausal(const Problem &p, void *scratch, float *S_out, float *z_out,
+                      cudaStream_t s);
+
+// One recurrent decode step for BH heads, in place on S [BH, P, Dv], z [BH, P].
+cudaError_t step(float *S, float *z, const void *q, const void *k, const void *v, void *out,
+                 long long BH, int D, int Dv, int P, int kind, int m, const float *W,
+                 int dtype, cudaStream_t s);
+
+}  // namespace la

@@ -1,0 +1,154 @@
+/*
+ * linattn.h -- C ABI of the B300 (sm_103a) kernelized linear-attention library.
+ *
+ * The method (review page "Transformers are RNNs: Fast Autoregressive
+ * Transformers with Linear Attention", section "proposed method", bullets
+ * 1-5): softmax attention is replaced by a kernel feature map phi, so that
+ *
+ *     out_i = phi(q_i)^T S_i / phi(q_i)^T z_i,
+ *     S_i   = sum_{j<=i} phi(k_j) v_j^T      (Dphi x Dv),
+ *     z_i   = sum_{j<=i} phi(k_j)            (Dphi),
+ *
+ * in the causal case (bullet 3: cumulative sums updated step by step); the
+ * non-causal form uses the sums over all N positions (bullet 2: phi(K)^T V is
+ * formed once and reused by every query).  The causal form is an RNN with
+ * the two memories (S, z) (bullet 5), which la_step advances one token at a
+ * time.  The sums include j = i.  No epsilon is added to the denominator.
+ *
+ * Feature maps:
+ *   LA_PHI_ELU1  phi(x) = elu(x) + 1 (alpha = 1), elementwise; Dphi = D.
+ *                ("main results", bullet 2: the elu-based feature map.)
+ *   LA_PHI_PRF   positive random features, phi_r(x) = exp(w_r.x - |x|^2/2)/sqrt(m),
+ *                r = 1..m, with W = [w_1..w_m] (m x D fp32) given by the
+ *                caller; Dphi = m.  (Review page "Stable, Fast and Accurate:
+ *                Kernelized Attention with Relative Positional Encoding",
+ *                "proposed method", bullet 6, names PRF among the maps.)
+ *
+ * Conventions for every entry point:
+ *  - Tensor pointers are DEVICE pointers owned by the caller, contiguous,
+ *    row-major, 16-byte aligned.  Heads are flattened as bh = b * H + h.
+ *      q, k   [B, H, N, D]        v, out [B, H, N, Dv]     (dtype)
+ *      S      [B, H, Dphi, Dv]    z      [B, H, Dphi]      (fp32)
+ *      W      [m, D]                                       (fp32)
+ *  - `dtype` is the type of q, k, v and out: LA_F32 or LA_BF16.  Arithmetic
+ *    is fp32 (accumulators, state, feature map) in both cases.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Work is enqueued asynchronously; nothing synchronises unless
+ *    stated.  The device used is the current CUDA device of the calling thread.
+ *  - Return value: LA_OK (0) or a negative la_status.  Argument errors are
+ *    detected on the host before anything is enqueued and leave all outputs
+ *    untouched.  LA_ERR_CUDA reports a failed launch or allocation
+ *    (cudaGetLastError is consumed).  Nothing is thrown and nothing aborts.
+ *  - Supported sizes: B, H, N >= 0 (a zero size is a no-op that returns
+ *    LA_OK; la_forward_ex then writes zero states); D and Dv in
+ *    {16, 32, 64, 128}; PRF m in {16, 32, 64, 128, 256} (else LA_ERR_FEATURE).
+ *  - Scratch: la_forward may take stream-ordered scratch memory from a
+ *    library-owned CUDA memory pool on the current device (per-segment
+ *    states of the causal scan, partial sums of the non-causal pass); it is
+ *    returned to the pool, in stream order, before the call returns.
+ *    la_shutdown() releases the pools.
+ */
+#ifndef LINATTN_H
+#define LINATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LA_VERSION 100
+
+typedef enum {
+    LA_F32 = 0,  /* float32 q, k, v, out */
+    LA_BF16 = 1  /* bfloat16 q, k, v, out */
+} la_dtype;
+
+typedef enum {
+    LA_PHI_ELU1 = 0, /* elu(x) + 1 */
+    LA_PHI_PRF = 1   /* positive random features exp(Wx - |x|^2/2)/sqrt(m) */
+} la_feature_kind;
+
+/* Feature-map descriptor.  Host memory, read during the call only.
+ * kind: la_feature_kind.  m: PRF feature count (ignored for ELU1).
+ * W: DEVICE pointer to the m x D fp32 row-major projection (PRF; NULL for
+ * ELU1).  A NULL descriptor means ELU1. */
+typedef struct {
+    int kind;
+    int m;
+    const float *W;
+} la_feature_map;
+
+typedef enum {
+    LA_OK = 0,
+    LA_ERR_NULL = -1,    /* a required pointer is NULL */
+    LA_ERR_DIM = -2,     /* a size is negative or outside the supported set */
+    LA_ERR_DTYPE = -3,   /* dtype is not LA_F32 / LA_BF16 */
+    LA_ERR_FEATURE = -4, /* bad feature map (unknown kind, PRF without W, bad m) */
+    LA_ERR_CUDA = -5,    /* a CUDA launch, allocation or query failed */
+    LA_ERR_TIMEOUT = -6, /* a bounded device-side wait ran out (reported by la_check) */
+    LA_ERR_ALIGN = -7    /* a tensor pointer is not 16-byte aligned */
+} la_status;
+
+/*
+ * la_forward -- kernelized attention over whole sequences.
+ *   causal != 0: out_i uses the prefix sums S_i, z_i (j <= i).
+ *   causal == 0: out_i uses the full sums over j = 0..N-1.
+ * q, k, v (inputs) and out (output) as in the conventions above; `out` must
+ * not alias the inputs.
+ */
+int la_forward(const void *q, const void *k, const void *v, void *out,
+               int B, int H, int N, int D, int Dv, int causal,
+               const la_feature_map *fm, int dtype, void *stream);
+
+/*
+ * la_forward_ex -- la_forward that also exports the memories after the last
+ * position: S_out [B, H, Dphi, Dv] = sum_j phi(k_j) v_j^T and
+ * z_out [B, H, Dphi] = sum_j phi(k_j), fp32, device.  Either may be NULL.
+ * These are the RNN state that la_step continues from (the state after a
+ * prefix of the sequence is the checkpoint of the recurrence).
+ */
+int la_forward_ex(const void *q, const void *k, const void *v, void *out,
+                  int B, int H, int N, int D, int Dv, int causal,
+                  const la_feature_map *fm, int dtype, void *stream,
+                  float *S_out, float *z_out);
+
+/*
+ * la_step -- one recurrent decode step for B*H independent heads ("proposed
+ * method", bullet 5; "main results", bullet 3: the state is updated
+ * incrementally).  In place on the fp32 memories:
+ *     S += phi(k) v^T ;  z += phi(k) ;  out = phi(q)^T S / phi(q)^T z
+ * (update first, then read out, matching the inclusive sums of la_forward).
+ * S [B, H, Dphi, Dv] and z [B, H, Dphi] fp32 (in/out); q, k [B, H, D] and
+ * v [B, H, Dv] (in), out [B, H, Dv] (out), all in `dtype`, device.  Calling
+ * la_step N times from zero memories gives la_forward's causal outputs.
+ */
+int la_step(float *S, float *z, const void *q, const void *k, const void *v,
+            void *out, int B, int H, int D, int Dv,
+            const la_feature_map *fm, int dtype, void *stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *la_status_string(int status);
+
+/*
+ * la_check -- synchronise `stream` and report deferred device-side errors:
+ * LA_ERR_TIMEOUT if a bounded wait inside a kernel of this library ran out
+ * since the last la_check on this device (the flag is then cleared),
+ * LA_ERR_CUDA if the stream reports an error, else LA_OK.
+ */
+int la_check(void *stream);
+
+/* Release the library's memory pools on every device it used.  Must not be
+ * called while work from this library is still running. */
+void la_shutdown(void);
+
+/* LA_VERSION of the built library. */
+int la_version(void);
+
+/* Number of CUDA kernels this library has launched in this process (all
+ * devices, all entry points).  Host-side counter; for accounting only. */
+unsigned long long la_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LINATTN_H */

@@ -1,0 +1,109 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every entry point that include/*.h declares, and rejects bad arguments on
+the host with the documented status codes before touching the device."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from causal_linear_attention_map_b300 import build
+
+    build.build()
+    import causal_linear_attention_map_b300 as la
+
+    return la.load()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"^[A-Za-z_][\w\s\*]*?\b(la_\w+)\s*\(", text, flags=re.M))
+    return sorted(names)
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for required in ("la_forward", "la_forward_ex", "la_step", "la_status_string", "la_check"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_binding_names_match(lib):
+    import causal_linear_attention_map_b300 as la
+
+    for name in declared_functions():
+        assert hasattr(la, name), f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    import causal_linear_attention_map_b300 as la
+
+    for code, name in la.STATUS_NAMES.items():
+        assert la.la_status_string(code).startswith(name)
+    assert "unknown" in la.la_status_string(12345)
+    assert lib.la_version() == 100
+
+
+FAKE = 0x10000000  # never dereferenced: every call below fails validation first
+
+
+def _fwd(lib, B=1, H=1, N=8, D=64, Dv=64, causal=1, fm=None, dtype=1, ptrs=None, S=None, z=None):
+    q, k, v, o = ptrs or (FAKE, FAKE + 4096, FAKE + 8192, FAKE + 12288)
+    import causal_linear_attention_map_b300 as la
+
+    fmp = ctypes.byref(fm) if fm is not None else None
+    return lib.la_forward_ex(q, k, v, o, B, H, N, D, Dv, causal, fmp, dtype, None, S, z)
+
+
+def test_validation_codes(lib):
+    import causal_linear_attention_map_b300 as la
+
+    assert _fwd(lib, dtype=2) == -3
+    assert _fwd(lib, dtype=-1) == -3
+    assert _fwd(lib, D=48) == -2
+    assert _fwd(lib, Dv=256) == -2
+    assert _fwd(lib, D=8) == -2
+    assert _fwd(lib, B=-1) == -2
+    assert _fwd(lib, N=-5) == -2
+    assert _fwd(lib, fm=la.la_feature_map(7, 0, None)) == -4
+    assert _fwd(lib, fm=la.la_feature_map(1, 64, None)) == -4          # PRF without W
+    assert _fwd(lib, fm=la.la_feature_map(1, 100, FAKE)) == -4         # bad m
+    assert _fwd(lib, fm=la.la_feature_map(1, 64, FAKE + 4)) == -7      # unaligned W
+    assert _fwd(lib, ptrs=(0, FAKE, FAKE, FAKE)) == -1
+    assert _fwd(lib, ptrs=(FAKE, FAKE, FAKE, 0)) == -1
+    assert _fwd(lib, ptrs=(FAKE + 2, FAKE, FAKE, FAKE)) == -7
+    assert _fwd(lib, S=FAKE + 8) == -7
+    # zero heads: a no-op that succeeds without touching the device
+    assert _fwd(lib, B=0) == 0
+    assert _fwd(lib, H=0, ptrs=(0, 0, 0, 0)) == 0
+
+
+def test_step_validation_codes(lib):
+    import causal_linear_attention_map_b300 as la
+
+    p = [FAKE + 256 * i for i in range(6)]
+
+    def st(*, B=2, H=2, D=64, Dv=64, fm=None, dtype=1, ptrs=p):
+        fmp = ctypes.byref(fm) if fm is not None else None
+        return lib.la_step(*ptrs, B, H, D, Dv, fmp, dtype, None)
+
+    assert st(dtype=5) == -3
+    assert st(D=12) == -2
+    assert st(fm=la.la_feature_map(1, 0, FAKE)) == -4
+    assert st(ptrs=[0] + p[1:]) == -1
+    assert st(ptrs=p[:5] + [0]) == -1
+    assert st(ptrs=[FAKE + 8] + p[1:]) == -7
+    assert st(B=0) == 0
