@@ -30,7 +30,7 @@ STATUS_NAMES = {0: "LA_OK", -1: "LA_ERR_NULL", -2: "LA_ERR_DIM", -3: "LA_ERR_DTY
                 -4: "LA_ERR_FEATURE", -5: "LA_ERR_CUDA", -6: "LA_ERR_TIMEOUT",
                 -7: "LA_ERR_ALIGN"}
 EXPORTED = ("la_forward", "la_forward_ex", "la_step", "la_status_string", "la_check",
-            "la_shutdown", "la_version", "la_launch_count")
+            "la_shutdown", "la_version", "la_launch_count", "la_forward_noncausal_noalloc")
 
 _DT = {torch.float32: LA_F32, torch.bfloat16: LA_BF16}
 
@@ -102,6 +102,8 @@ def load(path: str | None = None):
     lib.la_version.restype = i
     lib.la_launch_count.argtypes = []
     lib.la_launch_count.restype = ctypes.c_ulonglong
+    lib.la_forward_noncausal_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, i, fm, i, vp]
+    lib.la_forward_noncausal_noalloc.restype = i
     if path is None:
         _lib = lib
     return lib
@@ -221,3 +223,21 @@ def la_version() -> int:
 def la_launch_count() -> int:
     """Kernels launched by the library so far in this process."""
     return load().la_launch_count()
+
+
+def la_forward_noncausal_noalloc(q, k, v, out, feature_map: FeatureMap | None = None,
+                                 stream=None):
+    """Non-causal forward that allocates no device memory: ``out`` must be
+    given (the caller owns every buffer); the library's scratch is a fixed
+    device array shared by all calls (see include/linattn.h)."""
+    B, H, N, D = q.shape
+    Dv = v.shape[-1]
+    if k.shape != q.shape or tuple(v.shape[:3]) != (B, H, N) or tuple(out.shape) != (B, H, N, Dv):
+        raise ValueError("shape mismatch between q, k, v, out")
+    dt = _check_tensors(q, k, v, out)
+    _, fmp = _fm(feature_map)
+    st = load().la_forward_noncausal_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                             out.data_ptr(), B, H, N, D, Dv, fmp, dt,
+                                             _stream(stream))
+    _raise(st)
+    return out

@@ -147,6 +147,28 @@ int la_version(void);
  * devices, all entry points).  Host-side counter; for accounting only. */
 unsigned long long la_launch_count(void);
 
+/*
+ * la_forward_noncausal_noalloc -- the non-causal la_forward (causal = 0) for
+ * callers that cannot allocate device memory: code running inside an
+ * allocator or a memory-budgeted embedder, or real-time paths that forbid
+ * cudaMalloc after start-up.  The method's pages have no counterpart; this
+ * is a library convenience.
+ *
+ * Same arguments, layouts and results as la_forward with causal = 0.  It
+ * allocates nothing: its scratch is a fixed device array of
+ * LA_NOALLOC_SCRATCH_BYTES that every GPU loading this library holds until
+ * exit.  A problem needs B * H * Dphi * (Dv + 1) * 4 bytes of it; larger
+ * problems return LA_ERR_DIM before anything is enqueued.  The first call on
+ * a device looks up the array's device address (cudaGetSymbolAddress with
+ * that device current); make it before any stream capture.  All calls share
+ * the array, which keeps the last call's contents (each call clears what it
+ * accumulates into); calls that overlap on the GPU race, so serialise them.
+ */
+#define LA_NOALLOC_SCRATCH_BYTES (4u << 20)
+int la_forward_noncausal_noalloc(const void *q, const void *k, const void *v, void *out,
+                                 int B, int H, int N, int D, int Dv,
+                                 const la_feature_map *fm, int dtype, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

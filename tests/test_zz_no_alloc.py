@@ -1,0 +1,61 @@
+"""la_forward_noncausal_noalloc: the non-causal forward for callers that
+cannot allocate device memory (allocator hooks, memory-budgeted embedders,
+real-time paths).  Its scratch is a fixed device array shared by all calls.
+
+Checked through the C ABI against la_forward (causal = 0) on the same
+inputs, on two calls in a row with different inputs, so that a stale
+accumulator left by the first call would show up in the second.  This file
+is named to be collected last.
+"""
+import ctypes
+
+import pytest
+import torch
+
+import workloads as wl
+from parity_util import assert_close, np64
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc(la, q, k, v, out, fm_struct, dtype_code):
+    B, H, N, D = q.shape
+    Dv = v.shape[-1]
+    lib = la.load()
+    fmp = ctypes.byref(fm_struct) if fm_struct is not None else None
+    return lib.la_forward_noncausal_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                            out.data_ptr(), B, H, N, D, Dv, fmp, dtype_code,
+                                            torch.cuda.current_stream().cuda_stream)
+
+
+@pytest.mark.parametrize("shape,dtype,feature,m", [
+    ((2, 4, 777, 64, 64), "bf16", "elu1", 0),
+    ((8, 8, 4096, 64, 64), "bf16", "elu1", 0),
+    ((1, 3, 300, 32, 16), "f32", "elu1", 0),
+    ((1, 2, 513, 64, 64), "bf16", "prf", 128),
+])
+def test_noalloc_matches_la_forward_twice(la, shape, dtype, feature, m):
+    B, H, N, D, Dv = shape
+    W = wl.make_W(m, D).cuda() if feature == "prf" else None
+    fm = la.FeatureMap("prf", W) if W is not None else la.FeatureMap()
+    code = la.LA_F32 if dtype == "f32" else la.LA_BF16
+    for call in range(2):
+        w = wl.small(B=B, H=H, N=N, D=D, Dv=Dv, causal=False, feature=feature, m=m,
+                     dtype=dtype, scaled=dtype == "bf16", seed=100 + call)
+        q, k, v = (t.cuda() for t in wl.make_qkv(w))
+        ref = la.la_forward(q, k, v, causal=False, feature_map=fm)
+        out = torch.full_like(ref, float("nan"))
+        st = _noalloc(la, q, k, v, out, fm.c_struct(), code)
+        assert st == la.LA_OK, la.la_status_string(st)
+        torch.cuda.synchronize()
+        assert_close(np64(out), np64(ref), dtype, what=f"call {call}")
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch(la):
+    # B*H*Dphi*(Dv+1)*4 bytes: 64 heads x 128 x 129 x 4 = 4.2 MB > 4 MiB
+    q = torch.zeros((4, 16, 8, 128), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(q)
+    st = _noalloc(la, q, q, q, out, la.FeatureMap().c_struct(), la.LA_BF16)
+    assert st == -2, la.la_status_string(st)
+    with pytest.raises(la.LinAttnError):
+        la.la_forward_noncausal_noalloc(q, q, q, out)
