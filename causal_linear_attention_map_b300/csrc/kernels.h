@@ -30,6 +30,14 @@ struct Problem {
 // does not take.
 cudaError_t simt_causal(const Problem &p, float *S_out, float *z_out, cudaStream_t s);
 
+// Tensor-core (tcgen05) chunked causal kernel: bf16, elu+1, D and Dv in
+// {64, 128}.  Scratch: per-segment states (0 bytes when one segment per head
+// fills the GPU).  `err` is the device word that bounded waits set on timeout.
+bool tc_causal_supported(const Problem &p);
+size_t tc_causal_scratch_bytes(const Problem &p);
+cudaError_t tc_causal(const Problem &p, void *scratch, float *S_out, float *z_out, int *err,
+                      cudaStream_t s);
+
 // Non-causal: KV = phi(K)^T V and ksum = sum phi(k) reduced over N into
 // fp32 scratch (KV [BH, P, Dv], ksum [BH, P]; zeroed here), then the readout.
 size_t noncausal_scratch_bytes(const Problem &p);

@@ -144,7 +144,16 @@ int forward_impl(const void *q, const void *k, const void *v, void *out, int B, 
     DeviceCtx *ctx = nullptr;
     if ((st = get_ctx(&ctx)) != LA_OK) return st;
 
-    if (causal) return cuda_status(la::simt_causal(p, S_out, z_out, s));
+    if (causal) {
+        if (!la::tc_causal_supported(p)) return cuda_status(la::simt_causal(p, S_out, z_out, s));
+        size_t bytes = la::tc_causal_scratch_bytes(p);
+        void *scratch = nullptr;
+        if (bytes && cudaMallocFromPoolAsync(&scratch, bytes, ctx->pool, s) != cudaSuccess)
+            return cuda_status(cudaErrorMemoryAllocation);
+        cudaError_t e = la::tc_causal(p, scratch, S_out, z_out, ctx->err_word, s);
+        cudaError_t e2 = scratch ? cudaFreeAsync(scratch, s) : cudaSuccess;
+        return cuda_status(e != cudaSuccess ? e : e2);
+    }
 
     size_t bytes = la::noncausal_scratch_bytes(p);
     void *scratch = nullptr;

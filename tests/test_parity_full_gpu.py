@@ -1,0 +1,118 @@
+"""GPU parity at the method's full workload sizes, in the launch configuration
+the benchmark times (same entry points, same shapes, same segment plan).
+Where the fp64 oracle would take too long on every head, a fixed sample of
+heads is compared in full (all positions, all channels, and the exported
+memories)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from parity_util import assert_close, assert_state_close, np64, row_rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+def _heads(w, idx):
+    BH = w.B * w.H
+    return sorted(set(i % BH for i in idx))
+
+
+def _forward_and_check(la, w: wl.Workload, head_sample=None, state_tol=2e-2):
+    q, k, v = wl.make_qkv(w)
+    W = wl.make_W(w.m, w.D) if w.feature == "prf" else None
+    fm = la.FeatureMap("prf", W.cuda()) if W is not None else None
+    out, S, z = la.la_forward_ex(q.cuda(), k.cuda(), v.cuda(), causal=w.causal, feature_map=fm)
+    torch.cuda.synchronize()
+    BH = w.B * w.H
+    heads = list(range(BH)) if head_sample is None else _heads(w, head_sample)
+    qf = q.reshape(BH, w.N, w.D)[heads].unsqueeze(0)
+    kf = k.reshape(BH, w.N, w.D)[heads].unsqueeze(0)
+    vf = v.reshape(BH, w.N, w.Dv)[heads].unsqueeze(0)
+    Wn = W.double().numpy() if W is not None else None
+    if w.causal:
+        ref, Sref, zref = oracle.forward(np64(qf), np64(kf), np64(vf), causal=True,
+                                         feature=w.feature, W=Wn, return_state=True)
+    else:
+        ref = oracle.forward(np64(qf), np64(kf), np64(vf), causal=False, feature=w.feature, W=Wn)
+    got = np64(out.reshape(BH, w.N, w.Dv)[heads]).reshape(ref.shape)
+    err = assert_close(got, ref, w.dtype, what=w.name)
+    if w.causal:
+        P = w.phi_dim
+        Sg = np64(S.reshape(BH, P, w.Dv)[heads]).reshape(Sref.shape)
+        zg = np64(z.reshape(BH, P)[heads]).reshape(zref.shape)
+        assert_state_close(Sg, Sref, state_tol, what="S_out")
+        assert_state_close(zg, zref, state_tol, what="z_out")
+    return err, (q, k, v, S, z)
+
+
+def test_image_3072_causal(la):
+    _forward_and_check(la, wl.IMAGE_3072)
+
+
+def test_noncausal_4096(la):
+    _forward_and_check(la, wl.NONCAUSAL_4096)
+
+
+def test_long_65536_causal_sampled_heads(la):
+    _forward_and_check(la, wl.LONG_65536, head_sample=[0, 5, 10, 15])
+
+
+def test_prf_16384_causal_sampled_heads(la):
+    _forward_and_check(la, wl.PRF_16384, head_sample=[0, 7, 8, 15])
+
+
+def test_decode_from_long_state(la):
+    """B=64, H=16 decode from the long workload's final state (the same 16
+    heads' memories in every batch row), a few steps, every head checked;
+    both sides start from their own forward pass."""
+    w = wl.LONG_65536
+    q, k, v = wl.make_qkv(w)
+    _, S, z = la.la_forward_ex(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    B, H, D = wl.DECODE_B, wl.DECODE_H, wl.DECODE_D
+    Sd = S[0:1].expand(B, -1, -1, -1).contiguous()
+    zd = z[0:1].expand(B, -1, -1).contiguous()
+    _, Sr, zr = oracle.forward(np64(q), np64(k), np64(v), causal=True, return_state=True)
+    Sr = np.broadcast_to(Sr, (B, H, D, D)).copy()
+    zr = np.broadcast_to(zr, (B, H, D)).copy()
+    for t in range(6):
+        dq, dk, dv = wl.make_decode_qkv(t)
+        o = la.la_step(Sd, zd, dq.cuda(), dk.cuda(), dv.cuda())
+        torch.cuda.synchronize()
+        ref, Sr, zr = oracle.step(Sr, zr, np64(dq), np64(dk), np64(dv))
+        assert_close(np64(o), ref, "bf16", what=f"decode step {t}")
+    assert_state_close(np64(Sd), Sr, 2e-2, what="decode S")
+
+
+def test_segment_plan_matches_single_segment(la):
+    """The same head computed with many segments (small B*H) and with one
+    segment per head (B*H large enough to fill the GPU) agree."""
+    w = wl.small(B=1, H=1, N=4096, D=128, Dv=128, seed=21)
+    q, k, v = (t.cuda() for t in wl.make_qkv(w))
+    one = la.la_forward(q, k, v, causal=True)
+    rep = 160
+    many = la.la_forward(q.expand(rep, -1, -1, -1).contiguous(),
+                         k.expand(rep, -1, -1, -1).contiguous(),
+                         v.expand(rep, -1, -1, -1).contiguous(), causal=True)
+    torch.cuda.synchronize()
+    e = row_rel_err(np64(many[rep - 1:rep]), np64(one))
+    assert e <= 2e-2, e
+
+
+def test_tensor_core_path_is_used(la):
+    """bf16 elu+1 with D, Dv in {64, 128} runs the tcgen05 kernels: a
+    multi-segment problem launches the state pass, the scan and the output
+    pass (three kernels), the CUDA-core kernel would launch one."""
+    w = wl.small(B=1, H=2, N=2048, D=128, Dv=128, seed=5)
+    q, k, v = (t.cuda() for t in wl.make_qkv(w))
+    n0 = la.la_launch_count()
+    la.la_forward(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    assert la.la_launch_count() - n0 == 3
+    w = wl.small(B=1, H=2, N=2048, D=32, Dv=32, seed=5)
+    q, k, v = (t.cuda() for t in wl.make_qkv(w))
+    n0 = la.la_launch_count()
+    la.la_forward(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    assert la.la_launch_count() - n0 == 1
