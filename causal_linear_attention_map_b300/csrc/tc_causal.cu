@@ -12,23 +12,27 @@
 // segments handled by different CTAs, and the segment states are joined by
 // an exclusive prefix over segments:
 //   1. state pass: each (head, segment) CTA computes its segment's
-//      sum of phi(K)^T V and colsum(phi(K)) (one tensor-core contraction per
+//      sum of phi(K)^T V and colsum(phi(K)) (tensor-core contractions per
 //      chunk, accumulated in TMEM) and writes them to scratch;
 //   2. scan: exclusive prefix of those states over segments, per head;
 //   3. output pass: each (head, segment) CTA starts from its prefix state
 //      and runs the chunk recurrence above, writing out.
 // With a single segment per head, passes 1 and 2 are skipped.
 //
-// Per chunk (output pass) the four contractions are tcgen05.mma with fp32
-// accumulation in TMEM:
-//   MMA1  A    = phiQ . phiK^T        M=C, N=C,  K=Dphi  (both K-major)
-//   MMA3  num  = phiQ . S_prev        M=C, N=Dv, K=Dphi  (S_prev MN-major, bf16 copy)
-//   MMA4  S   += phiK^T . V           M=Dphi, N=Dv, K=C  (both MN-major)
-//   MMA2  num += P . V                M=C, N=Dv, K=C     (P = bf16 masked A)
-// phi is applied in place on the TMA-loaded Q/K tiles by the math warps
-// (phi never goes back to HBM), which also form the denominators on CUDA
-// cores: phi(q_i).z_prev while transforming row i, rowsum(A) while
-// extracting P.
+// Every contraction of a chunk is a tcgen05.mma with fp32 accumulation in
+// TMEM; the denominators and z ride along as narrow (N = 16) products with a
+// constant tile ONES (columns 0-7 = 1, 8-15 = 0) and a tile ZP holding
+// z_prev split into bf16 hi (columns 0-7) and lo (columns 8-15):
+//   MMA1   A    = phiQ . phiK^T        M=C,    N=C,  K=Dphi
+//   MMA3   NUM  = phiQ . S_prev        M=C,    N=Dv, K=Dphi   (bf16 copy of S)
+//   MMA3b  DEN  = phiQ . ZP            M=C,    N=16, K=Dphi
+//   MMA4   S   += phiK^T . V           M=Dphi, N=Dv, K=C
+//   MMA4b  Z   += phiK^T . ONES        M=Dphi, N=16, K=C      (Z[:,0] = z)
+//   MMA2   NUM += P . V                M=C,    N=Dv, K=C      (P from TMEM)
+//   MMA2b  DEN += P . ONES             M=C,    N=16, K=C
+// with P = bf16(tril(A)) written back into TMEM by the math warps, and
+// out = NUM / (DEN[:,0] + DEN[:,8]).  phi is applied in place on the
+// TMA-loaded Q/K tiles in shared memory; it never goes back to HBM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -41,29 +45,40 @@ namespace {
 
 using namespace tc;
 
-constexpr int kC = 128;            // chunk length (MMA M)
-constexpr int kMathThreads = 128;  // warps 0-3: TMEM lane quadrants 0-3
-constexpr int kThreads = kMathThreads + 64;  // + producer warp 4, MMA warp 5
+constexpr int kC = 128;          // chunk length (MMA M)
 constexpr int kErrTimeout = 1;
 
-// Shared-memory plan of the output pass for one (DP, DV).
+// Output pass: 16 math warps (4 column groups x 4 TMEM lane quadrants), a
+// TMA producer warp and an MMA warp.
+constexpr int kOutMathWarps = 16;
+constexpr int kOutThreads = (kOutMathWarps + 2) * 32;
+// State pass: 8 math warps (2 column groups x 4 quadrants) + producer + MMA.
+constexpr int kStateMathWarps = 8;
+constexpr int kStateThreads = (kStateMathWarps + 2) * 32;
+
+constexpr int ONES_BYTES = kC * 32;  // [C x 16] bf16, 32-byte swizzle
+
 template <int DP, int DV>
 struct OutPlan {
     static constexpr int QB = kC * DP * 2;  // one Q or K chunk tile (bytes)
     static constexpr int VB = kC * DV * 2;  // one V chunk tile
-    static constexpr int PB = kC * kC * 2;  // masked scores P (bf16)
     static constexpr int SB = DP * DV * 2;  // S_prev (bf16)
-    static constexpr int kBase = 2 * QB + 2 * QB + 2 * VB + PB + SB;
-    static constexpr int NQ = (kBase + 4096 <= 227 * 1024) ? 2 : 1;
+    static constexpr int ZB = DP * 32 < 1024 ? 1024 : DP * 32;   // ZP [DP x 16]
+    static constexpr int kRest = 2 * QB + 2 * VB + SB + ZB + ONES_BYTES;
+    static constexpr int NQ = (2 * QB + kRest + 3072 <= 227 * 1024) ? 2 : 1;
     static constexpr int Q0 = 0;
     static constexpr int K0 = Q0 + NQ * QB;
     static constexpr int V0 = K0 + 2 * QB;
-    static constexpr int P0 = V0 + 2 * VB;
-    static constexpr int S0 = P0 + PB;
-    static constexpr int TILES = S0 + SB;
-    static constexpr int SMEM = TILES + 1024 /* align */ + 1024 /* barriers, z */;
-    static constexpr int TMEM_S = 0, TMEM_NUM = DV, TMEM_A = 2 * DV;
-    static constexpr int TMEM_COLS = (2 * DV + kC) <= 256 ? 256 : 512;
+    static constexpr int S0 = V0 + 2 * VB;
+    static constexpr int Z0 = S0 + SB;
+    static constexpr int O0 = Z0 + ZB;
+    static constexpr int TILES = O0 + ONES_BYTES;
+    static constexpr int SMEM = TILES + 1024 /* align */ + 1024 /* barriers */;
+    // TMEM columns (32-aligned regions)
+    static constexpr int T_S = 0, T_Z = DV, T_NUM = DV + 32, T_DEN = 2 * DV + 32,
+                         T_A = 2 * DV + 64, T_P = 2 * DV + 192;
+    static constexpr int TMEM_COLS = 512;
+    static_assert(T_P + 64 <= 512, "TMEM plan too large");
     static_assert(SMEM <= 227 * 1024, "shared memory plan too large");
 };
 
@@ -71,12 +86,14 @@ template <int DP, int DV>
 struct StatePlan {
     static constexpr int QB = kC * DP * 2;
     static constexpr int VB = kC * DV * 2;
-    static constexpr int NS = ((QB + VB) * 3 + 2048 <= 227 * 1024) ? 3 : 2;
+    static constexpr int NS = ((QB + VB) * 3 + ONES_BYTES + 3072 <= 227 * 1024) ? 3 : 2;
     static constexpr int K0 = 0;
     static constexpr int V0 = NS * QB;
-    static constexpr int TILES = V0 + NS * VB;
+    static constexpr int O0 = V0 + NS * VB;
+    static constexpr int TILES = O0 + ONES_BYTES;
     static constexpr int SMEM = TILES + 1024 + 1024;
-    static constexpr int TMEM_COLS = DV <= 32 ? 32 : (DV <= 64 ? 64 : 128);
+    static constexpr int T_S = 0, T_Z = DV;
+    static constexpr int TMEM_COLS = DV + 32 <= 128 ? 128 : 256;
 };
 
 struct Geometry {
@@ -89,7 +106,11 @@ __device__ __forceinline__ unsigned char *align1k(unsigned char *p)
                                              ~uintptr_t(1023));
 }
 
-__device__ __forceinline__ void math_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+template <int NTHREADS>
+__device__ __forceinline__ void math_bar()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(NTHREADS) : "memory");
+}
 
 // Bounded wait that turns into a no-op once the CTA has aborted.  Threads
 // never leave their loops early: after an abort they run on without waiting
@@ -106,80 +127,89 @@ __device__ __forceinline__ bool wait_ok(uint64_t *bar, uint32_t parity, volatile
     return true;
 }
 
-// phi(x) = elu(x) + 1 on 8 packed bf16, in place; returns them as floats.
-__device__ __forceinline__ uint4 phi8(uint4 raw, float (&f)[8])
+// phi(x) = elu(x) + 1 on 8 packed bf16.
+__device__ __forceinline__ uint4 phi8(uint4 raw)
 {
     uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
     for (int t = 0; t < 4; t++) {
         float2 p = unpack_bf16x2(w[t]);
-        f[2 * t] = phi_elu1_fast(p.x);
-        f[2 * t + 1] = phi_elu1_fast(p.y);
-        w[t] = pack_bf16x2(f[2 * t], f[2 * t + 1]);
+        w[t] = pack_bf16x2(phi_elu1_fast(p.x), phi_elu1_fast(p.y));
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Transform row `r` of a [kC x DP] swizzled tile in place.  If `zero`, the
-// row is cleared (positions past the end of the sequence).  If zs != null,
-// returns phi(row) . zs using the bf16-rounded phi values.
-template <int DP>
-__device__ __forceinline__ float phi_row(unsigned char *tile, int r, bool zero, const float *zs)
+// phi in place on row `r` of a [kC x DP] 128B-swizzled tile, the 16 B chunks
+// j = g, g + NG, g + 2 NG, ... of the row (column group g of NG).  Rows past
+// the sequence end (`zero`) are cleared instead.
+template <int DP, int NG>
+__device__ __forceinline__ void phi_row_part(unsigned char *tile, int r, int g, bool zero)
 {
-    float dot = 0.f;
 #pragma unroll
-    for (int b = 0; b < DP / 64; b++) {
-        unsigned char *blk = tile + b * (kC * 128);
-#pragma unroll
-        for (int j = 0; j < 8; j++) {
-            uint4 *p = reinterpret_cast<uint4 *>(blk + sw128_off(r, j));
-            if (zero) {
-                *p = make_uint4(0, 0, 0, 0);
-                continue;
-            }
-            float f[8];
-            uint4 o = phi8(*p, f);
-            *p = o;
-            if (zs) {
-                const float *zz = zs + b * 64 + j * 8;
-                uint32_t w[4] = {o.x, o.y, o.z, o.w};
-#pragma unroll
-                for (int t = 0; t < 4; t++) {
-                    float2 q = unpack_bf16x2(w[t]);
-                    dot = fmaf(q.x, zz[2 * t], dot);
-                    dot = fmaf(q.y, zz[2 * t + 1], dot);
-                }
-            }
-        }
+    for (int j = g; j < DP / 8; j += NG) {
+        uint4 *p = reinterpret_cast<uint4 *>(tile + (j / 8) * (kC * 128) + sw128_off(r, j % 8));
+        *p = zero ? make_uint4(0, 0, 0, 0) : phi8(*p);
     }
-    return dot;
 }
 
-// Column sum of column d of a [kC x DP] swizzled bf16 tile.
-template <int DP>
-__device__ __forceinline__ float col_sum(const unsigned char *tile, int d)
+// TMEM load of NCOL (16 or 32) 32-bit columns, no wait.
+template <int NCOL>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[NCOL])
 {
-    const unsigned char *blk = tile + (d / 64) * (kC * 128);
-    const int cc = d % 64, j = cc / 8, e = cc % 8;
-    float s = 0.f;
-#pragma unroll 8
-    for (int r = 0; r < kC; r++) {
-        const __nv_bfloat16 *p =
-            reinterpret_cast<const __nv_bfloat16 *>(blk + sw128_off(r, j)) + e;
-        s += __bfloat162float(*p);
+    if constexpr (NCOL == 32)
+        tmem_ld32_nowait(taddr, r);
+    else
+        tmem_ld16_nowait(taddr, r);
+}
+
+// Write NCOL fp32 values as bf16 into row r, columns [c0, c0 + NCOL) of a
+// 128B-swizzled MN-major tile with `rows` rows per 64-column block.
+template <int NCOL>
+__device__ __forceinline__ void store_row_bf16(unsigned char *tile, int rows, int r, int c0,
+                                               const uint32_t (&v)[NCOL])
+{
+#pragma unroll
+    for (int j = 0; j < NCOL / 8; j++) {
+        const int col = c0 + 8 * j;
+        unsigned char *blk = tile + (col / 64) * (rows * 128);
+        *reinterpret_cast<uint4 *>(blk + sw128_off(r, (col % 64) / 8)) = make_uint4(
+            pack_bf16x2(__uint_as_float(v[8 * j]), __uint_as_float(v[8 * j + 1])),
+            pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+            pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+            pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
     }
-    return s;
+}
+
+// z (fp32) -> one row of the ZP tile: columns 0-7 bf16(z), 8-15 bf16(z - bf16(z)).
+__device__ __forceinline__ void store_zp_row(unsigned char *zp, int r, float z)
+{
+    const float hi = __bfloat162float(__float2bfloat16_rn(z));
+    const uint32_t h = pack_bf16x2(hi, hi), l = pack_bf16x2(z - hi, z - hi);
+    *reinterpret_cast<uint4 *>(zp + sw32_off(r, 0)) = make_uint4(h, h, h, h);
+    *reinterpret_cast<uint4 *>(zp + sw32_off(r, 1)) = make_uint4(l, l, l, l);
+}
+
+// The constant ONES tile [kC x 16]: columns 0-7 = 1, 8-15 = 0.
+__device__ __forceinline__ void fill_ones(unsigned char *ones, int tid, int nthreads)
+{
+    const uint32_t one = pack_bf16x2(1.f, 1.f);
+    for (int r = tid; r < kC; r += nthreads) {
+        *reinterpret_cast<uint4 *>(ones + sw32_off(r, 0)) = make_uint4(one, one, one, one);
+        *reinterpret_cast<uint4 *>(ones + sw32_off(r, 1)) = make_uint4(0, 0, 0, 0);
+    }
 }
 
 // ------------------------------------------------------------ state pass
 
 template <int DP, int DV>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kStateThreads, 1)
 tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 Geometry g, float *__restrict__ dS, float *__restrict__ dz, int *err)
 {
     using PL = StatePlan<DP, DV>;
     constexpr int NS = PL::NS;
+    constexpr int NMATH = kStateMathWarps * 32;
+    constexpr int NG = kStateMathWarps / 4;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = align1k(smem_raw);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + PL::TILES);
@@ -189,28 +219,29 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 
     const int seg = blockIdx.x, head = blockIdx.y;
     const int c_begin = seg * g.cps;
-    const int c_end = min(c_begin + g.cps, g.nchunks);
-    const int nc = c_end - c_begin;
+    const int nc = min(c_begin + g.cps, g.nchunks) - c_begin;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    constexpr int PRODUCER = kStateMathWarps, MMAW = kStateMathWarps + 1;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; i++) {
             mbar_init(&full[i], 1);
             mbar_init(&phi_done[i], 1);
-            mbar_init(&empty[i], 2);   // MMA commit + math (colsum done)
+            mbar_init(&empty[i], 1);
         }
         mbar_init(final_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 5) tmem_alloc(tslot, PL::TMEM_COLS);
+    if (warp < kStateMathWarps) fill_ones(sm + PL::O0, threadIdx.x, NMATH);
+    fence_proxy_async_smem();
+    if (warp == MMAW) tmem_alloc(tslot, PL::TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
-    if (warp == 4) {
-        // ---------------- TMA producer
+    if (warp == PRODUCER) {
         if (lane == 0) {
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
@@ -228,14 +259,14 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                                 row, head);
                 issued = c + 1;
             }
-            // drain: the loads issued last into each stage have landed
-            for (int c = max(0, issued - NS); c < issued; c++)
+            for (int c = max(0, issued - NS); c < issued; c++)   // drain in-flight loads
                 mbar_wait(&full[c % NS], (c / NS) & 1, err, kErrTimeout);
         }
-    } else if (warp == 5) {
-        // ---------------- MMA issuer: S += phiK^T V
+    } else if (warp == MMAW) {
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16(128, DV, 1, 1);
+            constexpr uint32_t id_kv = idesc_bf16(128, DV, 1, 1);
+            constexpr uint32_t id_z = idesc_bf16(128, 16, 1, 1);
+            const uint32_t ones = smem_u32(sm + PL::O0);
             for (int c = 0; c < nc; c++) {
                 const int st = c % NS;
                 if (!wait_ok(&phi_done[st], (c / NS) & 1, abort_flag, err)) continue;
@@ -244,55 +275,60 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 const uint32_t va = smem_u32(sm + PL::V0 + st * PL::VB);
 #pragma unroll
                 for (int k = 0; k < kC; k += 16) {
-                    uint64_t ad = sw128_desc(ka + (k / 8) * 1024, DP == 128 ? kC * 128 : 0, 1024);
-                    uint64_t bd = sw128_desc(va + (k / 8) * 1024, kC * 128, 1024);
-                    mma_bf16_ss(tmem, ad, bd, idesc, (c > 0 || k > 0) ? 1u : 0u);
+                    const uint64_t ad =
+                        sw128_desc(ka + (k / 8) * 1024, DP == 128 ? kC * 128 : 0, 1024);
+                    const uint32_t acc = (c > 0 || k > 0) ? 1u : 0u;
+                    mma_bf16_ss(tmem + PL::T_S, ad, sw128_desc(va + (k / 8) * 1024, kC * 128, 1024),
+                                id_kv, acc);
+                    mma_bf16_ss(tmem + PL::T_Z, ad, sw32_desc(ones + (k / 8) * 256, 256, 256), id_z,
+                                acc);
                 }
                 mma_commit(&empty[st]);
             }
-            mma_commit(final_bar);   // also the drain: every MMA issued above has completed
+            mma_commit(final_bar);   // also drains every MMA issued above
             mbar_wait(final_bar, 0, err, kErrTimeout);
         }
     } else {
-        // ---------------- math warps: phi(K) in place, colsum for z
-        const int t = threadIdx.x;
-        float zacc = 0.f;
+        const int q = warp & 3, grp = warp >> 2;
+        const int row = q * 32 + lane;
         for (int c = 0; c < nc; c++) {
             const int st = c % NS;
             wait_ok(&full[st], (c / NS) & 1, abort_flag, err);
             const int n_valid = min(kC, g.N - (c_begin + c) * kC);
-            unsigned char *ktile = sm + PL::K0 + st * PL::QB;
-            phi_row<DP>(ktile, t, t >= n_valid, nullptr);
+            phi_row_part<DP, NG>(sm + PL::K0 + st * PL::QB, row, grp, row >= n_valid);
             fence_proxy_async_smem();
-            math_bar();
-            if (t == 0) mbar_arrive(&phi_done[st]);
-            if (t < DP) zacc += col_sum<DP>(ktile, t);
-            math_bar();
-            if (t == 0) mbar_arrive(&empty[st]);   // colsum reads done: stage may be refilled
+            math_bar<NMATH>();
+            if (threadIdx.x == 0) mbar_arrive(&phi_done[st]);
         }
         // final state -> scratch (warp-uniform condition: tcgen05.ld is warp-collective)
         const bool done = wait_ok(final_bar, 0, abort_flag, err);
-        if (__all_sync(0xffffffffu, done)) {
+        if (__all_sync(0xffffffffu, done) && row < DP) {
             tc_fence_after();
             const long long base = ((long long)head * g.nseg + seg);
-            if (t < DP) {
-                float *dst = dS + base * DP * DV + (long long)t * DV;
+            constexpr int CW = DV / NG;   // columns per group
+            float *dst = dS + base * DP * DV + (long long)row * DV + grp * CW;
 #pragma unroll
-                for (int c0 = 0; c0 < DV; c0 += 32) {
-                    float v[32];
-                    tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
+            for (int c0 = 0; c0 < CW; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32_nowait(tmem + ((uint32_t)(q * 32) << 16) + PL::T_S + grp * CW + c0, v);
+                tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; i += 4)
-                        *reinterpret_cast<float4 *>(dst + c0 + i) =
-                            make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-                }
-                dz[base * DP + t] = zacc;
+                for (int i = 0; i < 32; i += 4)
+                    *reinterpret_cast<float4 *>(dst + c0 + i) =
+                        make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                    __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+            }
+            if (grp == 0) {
+                uint32_t zv[16];
+                tmem_ld16_nowait(tmem + ((uint32_t)(q * 32) << 16) + PL::T_Z, zv);
+                tmem_ld_wait();
+                dz[base * DP + row] = __uint_as_float(zv[0]);
             }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == MMAW) {
         tc_fence_after();
         tmem_dealloc(tmem, PL::TMEM_COLS);
     }
@@ -300,35 +336,42 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 
 // ------------------------------------------------------------ scan
 
-// Exclusive prefix over segments of the per-segment states, in place.
+// Exclusive prefix over segments of the per-segment states, in place.  Each
+// thread owns one state element of one head; loads are batched in registers.
 __global__ void seg_scan_kernel(float *__restrict__ dS, float *__restrict__ dz, int nseg, int sz_S,
                                 int sz_z)
 {
     const long long head = blockIdx.y;
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    float *p;
+    long long stride;
     if (e < sz_S) {
-        float *p = dS + head * nseg * (long long)sz_S + e;
-        float run = 0.f;
-        for (int s = 0; s < nseg; s++) {
-            float x = p[(long long)s * sz_S];
-            p[(long long)s * sz_S] = run;
-            run += x;
-        }
+        p = dS + head * nseg * (long long)sz_S + e;
+        stride = sz_S;
     } else if (e < sz_S + sz_z) {
-        float *p = dz + head * nseg * (long long)sz_z + (e - sz_S);
-        float run = 0.f;
-        for (int s = 0; s < nseg; s++) {
-            float x = p[(long long)s * sz_z];
-            p[(long long)s * sz_z] = run;
-            run += x;
-        }
+        p = dz + head * nseg * (long long)sz_z + (e - sz_S);
+        stride = sz_z;
+    } else {
+        return;
+    }
+    float run = 0.f;
+    for (int s0 = 0; s0 < nseg; s0 += 16) {
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; i++) x[i] = s0 + i < nseg ? p[(s0 + i) * stride] : 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; i++)
+            if (s0 + i < nseg) {
+                p[(s0 + i) * stride] = run;
+                run += x[i];
+            }
     }
 }
 
 // ------------------------------------------------------------ output pass
 
 template <int DP, int DV>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kOutThreads, 1)
 tc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, Geometry g,
               const float *__restrict__ preS, const float *__restrict__ prez,
@@ -337,11 +380,15 @@ tc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 {
     using PL = OutPlan<DP, DV>;
     constexpr int NQ = PL::NQ;
+    constexpr int NMATH = kOutMathWarps * 32;
+    constexpr int NG = kOutMathWarps / 4;   // column groups
+    constexpr int CW = DV / NG;             // NUM / S columns per thread (16 or 32)
+    constexpr int PRODUCER = kOutMathWarps, MMAW = kOutMathWarps + 1;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = align1k(smem_raw);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + PL::TILES);
-    uint64_t *qfull = bars;             // [NQ]
-    uint64_t *qempty = bars + 2;        // [NQ]
+    uint64_t *qfull = bars;             // [2]
+    uint64_t *qempty = bars + 2;        // [2]
     uint64_t *kvfull = bars + 4;        // [2]
     uint64_t *kvempty = bars + 6;       // [2]
     uint64_t *ops_ready = bars + 8;
@@ -352,14 +399,11 @@ tc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     uint64_t *drain_bar = bars + 13;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + 14);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
-    float *zs = reinterpret_cast<float *>(bars + 16);   // [DP]
 
     const int seg = blockIdx.x, head = blockIdx.y;
     const int c_begin = seg * g.cps;
-    const int c_end = min(c_begin + g.cps, g.nchunks);
-    const int nc = c_end - c_begin;
+    const int nc = min(c_begin + g.cps, g.nchunks) - c_begin;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const bool last_seg = (seg == g.nseg - 1);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; i++) {
@@ -377,14 +421,13 @@ tc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 5) tmem_alloc(tslot, PL::TMEM_COLS);
+    if (warp == MMAW) tmem_alloc(tslot, PL::TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
-    if (warp == 4) {
-        // ---------------- TMA producer
+    if (warp == PRODUCER) {
         if (lane == 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
@@ -409,22 +452,20 @@ tc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                                 b * 64, row, head);
                 issued_kv = c + 1;
             }
-            // drain: the loads issued last into each stage have landed
-            for (int c = max(0, issued_q - NQ); c < issued_q; c++)
+            for (int c = max(0, issued_q - NQ); c < issued_q; c++)   // drain in-flight loads
                 mbar_wait(&qfull[c % NQ], (c / NQ) & 1, err, kErrTimeout);
             for (int c = max(0, issued_kv - 2); c < issued_kv; c++)
                 mbar_wait(&kvfull[c % 2], (c / 2) & 1, err, kErrTimeout);
         }
-    } else if (warp == 5) {
-        // ---------------- MMA issuer
+    } else if (warp == MMAW) {
         if (lane == 0) {
             constexpr uint32_t id_qk = idesc_bf16(128, kC, 0, 0);
             constexpr uint32_t id_qs = idesc_bf16(128, DV, 0, 1);
+            constexpr uint32_t id_q16 = idesc_bf16(128, 16, 0, 1);
             constexpr uint32_t id_kv = idesc_bf16(128, DV, 1, 1);
-            constexpr uint32_t id_pv = idesc_bf16(128, DV, 0, 1);
-            const uint32_t t_S = tmem + PL::TMEM_S, t_num = tmem + PL::TMEM_NUM,
-                           t_A = tmem + PL::TMEM_A;
-            const uint32_t p_addr = smem_u32(sm + PL::P0), s_addr = smem_u32(sm + PL::S0);
+            constexpr uint32_t id_k16 = idesc_bf16(128, 16, 1, 1);
+            const uint32_t s_addr = smem_u32(sm + PL::S0), zp_addr = smem_u32(sm + PL::Z0),
+                           ones = smem_u32(sm + PL::O0);
             for (int c = 0; c < nc; c++) {
                 const int sq = c % NQ, skv = c % 2;
                 if (!wait_ok(ops_ready, c & 1, abort_flag, err)) continue;
@@ -436,199 +477,187 @@ tc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
                 for (int k = 0; k < DP; k += 16) {
                     const uint32_t off = (k / 64) * (kC * 128) + (k % 64) * 2;
-                    mma_bf16_ss(t_A, sw128_desc(qa + off, 16, 1024), sw128_desc(ka + off, 16, 1024),
-                                id_qk, k > 0 ? 1u : 0u);
+                    mma_bf16_ss(tmem + PL::T_A, sw128_desc(qa + off, 16, 1024),
+                                sw128_desc(ka + off, 16, 1024), id_qk, k > 0 ? 1u : 0u);
                 }
                 mma_commit(mma1_bar);
-                // MMA3: num = phiQ S_prev
+                // MMA3 / MMA3b: NUM = phiQ S_prev, DEN = phiQ ZP
 #pragma unroll
                 for (int k = 0; k < DP; k += 16) {
-                    const uint32_t aoff = (k / 64) * (kC * 128) + (k % 64) * 2;
-                    mma_bf16_ss(t_num, sw128_desc(qa + aoff, 16, 1024),
+                    const uint64_t ad = sw128_desc(qa + (k / 64) * (kC * 128) + (k % 64) * 2, 16, 1024);
+                    mma_bf16_ss(tmem + PL::T_NUM, ad,
                                 sw128_desc(s_addr + (k / 8) * 1024, DP * 128, 1024), id_qs,
                                 k > 0 ? 1u : 0u);
+                    mma_bf16_ss(tmem + PL::T_DEN, ad, sw32_desc(zp_addr + (k / 8) * 256, 256, 256),
+                                id_q16, k > 0 ? 1u : 0u);
                 }
-                // MMA4: S += phiK^T V
+                // MMA4 / MMA4b: S += phiK^T V, Z += phiK^T ONES
 #pragma unroll
                 for (int k = 0; k < kC; k += 16) {
-                    mma_bf16_ss(t_S, sw128_desc(ka + (k / 8) * 1024, DP == 128 ? kC * 128 : 0, 1024),
-                                sw128_desc(va + (k / 8) * 1024, kC * 128, 1024), id_kv, 1u);
+                    const uint64_t ad =
+                        sw128_desc(ka + (k / 8) * 1024, DP == 128 ? kC * 128 : 0, 1024);
+                    mma_bf16_ss(tmem + PL::T_S, ad, sw128_desc(va + (k / 8) * 1024, kC * 128, 1024),
+                                id_kv, 1u);
+                    mma_bf16_ss(tmem + PL::T_Z, ad, sw32_desc(ones + (k / 8) * 256, 256, 256),
+                                id_k16, 1u);
                 }
                 mma_commit(mma4_bar);
                 mma_commit(&qempty[sq]);
-                // MMA2: num += P V
+                // MMA2 / MMA2b: NUM += P V, DEN += P ONES  (P in TMEM)
                 if (!wait_ok(p_ready, c & 1, abort_flag, err)) continue;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < kC; k += 16) {
-                    const uint32_t aoff = (k / 64) * (kC * 128) + (k % 64) * 2;
-                    mma_bf16_ss(t_num, sw128_desc(p_addr + aoff, 16, 1024),
-                                sw128_desc(va + (k / 8) * 1024, kC * 128, 1024), id_pv, 1u);
+                    const uint32_t pa = tmem + PL::T_P + k / 2;
+                    mma_bf16_ts(tmem + PL::T_NUM, pa,
+                                sw128_desc(va + (k / 8) * 1024, kC * 128, 1024), id_qs, 1u);
+                    mma_bf16_ts(tmem + PL::T_DEN, pa, sw32_desc(ones + (k / 8) * 256, 256, 256),
+                                id_q16, 1u);
                 }
                 mma_commit(mma2_bar);
                 mma_commit(&kvempty[skv]);
             }
-            // drain: every MMA issued above has completed before TMEM is freed
-            mma_commit(drain_bar);
+            mma_commit(drain_bar);   // every MMA issued above has completed
             mbar_wait(drain_bar, 0, err, kErrTimeout);
         }
     } else {
-        // ---------------- math warps (thread t owns query row t / state row t)
-        const int t = threadIdx.x;
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        unsigned char *Pt = sm + PL::P0;
+        // ---------------- math warps: thread (row, grp), row = TMEM lane
+        const int q = warp & 3, grp = warp >> 2;
+        const int row = q * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         unsigned char *St = sm + PL::S0;
+        unsigned char *Zt = sm + PL::Z0;
         const long long pre_base = ((long long)head * g.nseg + seg);
+        const int srow = row % DP;   // state row (rows >= DP duplicate rows - DP)
 
-        // initial state: TMEM S (all 128 lanes; rows >= DP duplicate rows - DP),
-        // S_prev bf16 copy, z_prev.
+        fill_ones(sm + PL::O0, threadIdx.x, NMATH);
+        // initial state: TMEM S and Z, the bf16 S_prev copy, ZP
         {
-            const int r = t % DP;
-            const float *src = preS ? preS + pre_base * DP * DV + (long long)r * DV : nullptr;
+            uint32_t v[CW];
+            const float *src = preS ? preS + pre_base * DP * DV + (long long)srow * DV + grp * CW
+                                    : nullptr;
 #pragma unroll
-            for (int c0 = 0; c0 < DV; c0 += 32) {
-                float v[32];
-#pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    float4 x = src ? *reinterpret_cast<const float4 *>(src + c0 + i)
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-                    v[i] = x.x; v[i + 1] = x.y; v[i + 2] = x.z; v[i + 3] = x.w;
-                }
-                tmem_st32(tmem + lane_base + PL::TMEM_S + c0, v);
-                if (t < DP) {
-                    unsigned char *blk = St + (c0 / 64) * (DP * 128);
-#pragma unroll
-                    for (int j = 0; j < 4; j++) {
-                        const int chunk = (c0 % 64) / 8 + j;
-                        *reinterpret_cast<uint4 *>(blk + sw128_off(t, chunk)) =
-                            make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]),
-                                       pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
-                                       pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
-                                       pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
-                    }
-                }
+            for (int i = 0; i < CW; i += 4) {
+                const float4 x = src ? *reinterpret_cast<const float4 *>(src + i)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+                v[i] = __float_as_uint(x.x);
+                v[i + 1] = __float_as_uint(x.y);
+                v[i + 2] = __float_as_uint(x.z);
+                v[i + 3] = __float_as_uint(x.w);
             }
-            if (t < DP) zs[t] = prez ? prez[pre_base * DP + t] : 0.f;
+#pragma unroll
+            for (int c0 = 0; c0 < CW; c0 += 16) {
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; i++) w[i] = v[c0 + i];
+                tmem_st16_nowait(tmem + lane_base + PL::T_S + grp * CW + c0, w);
+            }
+            if (row < DP) store_row_bf16<CW>(St, DP, row, grp * CW, v);
+            if (grp == 0) {
+                const float z0 = prez ? prez[pre_base * DP + srow] : 0.f;
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; i++) w[i] = i < 8 ? __float_as_uint(z0) : 0u;
+                tmem_st16_nowait(tmem + lane_base + PL::T_Z, w);
+                if (row < DP) store_zp_row(Zt, row, z0);
+            }
+            tmem_st_wait();
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        math_bar();
+        math_bar<NMATH>();
 
         for (int c = 0; c < nc; c++) {
             const int sq = c % NQ, skv = c % 2;
             const int n_valid = min(kC, g.N - (c_begin + c) * kC);
-            unsigned char *qt = sm + PL::Q0 + sq * PL::QB;
-            unsigned char *kt = sm + PL::K0 + skv * PL::QB;
-            // 1. phi(Q) (+ phi(q_t) . z_prev) and phi(K) in place
+            // 1. phi in place on this chunk's Q and K tiles
             wait_ok(&qfull[sq], (c / NQ) & 1, abort_flag, err);
-            const float den_inter = phi_row<DP>(qt, t, false, zs);
+            phi_row_part<DP, NG>(sm + PL::Q0 + sq * PL::QB, row, grp, false);
             wait_ok(&kvfull[skv], (c / 2) & 1, abort_flag, err);
-            phi_row<DP>(kt, t, t >= n_valid, nullptr);
-            fence_proxy_async_smem();
-            math_bar();
-            if (t < DP) zs[t] += col_sum<DP>(kt, t);   // z for the next chunk
-            // 2. S_prev for this chunk from S after the previous chunk
+            phi_row_part<DP, NG>(sm + PL::K0 + skv * PL::QB, row, grp, row >= n_valid);
+            // 2. S_prev and ZP from the state after the previous chunk
             if (c > 0) {
                 wait_ok(mma4_bar, (c - 1) & 1, abort_flag, err);
                 tc_fence_after();
-                if (warp < (DP + 31) / 32) {
-#pragma unroll
-                    for (int c0 = 0; c0 < DV; c0 += 32) {
-                        float v[32];
-                        tmem_ld32(tmem + lane_base + PL::TMEM_S + c0, v);
-                        unsigned char *blk = St + (c0 / 64) * (DP * 128);
-#pragma unroll
-                        for (int j = 0; j < 4; j++) {
-                            const int chunk = (c0 % 64) / 8 + j;
-                            *reinterpret_cast<uint4 *>(blk + sw128_off(t, chunk)) =
-                                make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]),
-                                           pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
-                                           pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
-                                           pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
-                        }
-                    }
-                    fence_proxy_async_smem();
-                }
-            }
-            tc_fence_before();
-            math_bar();
-            if (t == 0) mbar_arrive(ops_ready);
-            // 3. P = bf16(tril(A)), den_intra = rowsum
-            wait_ok(mma1_bar, c & 1, abort_flag, err);
-            tc_fence_after();
-            float den_intra = 0.f;
-#pragma unroll
-            for (int c0 = 0; c0 < kC; c0 += 32) {
-                float v[32];
-                tmem_ld32(tmem + lane_base + PL::TMEM_A + c0, v);
-                unsigned char *blk = Pt + (c0 / 64) * (kC * 128);
-#pragma unroll
-                for (int j = 0; j < 4; j++) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; e++) {
-                        const int col = c0 + 8 * j + 2 * e;
-                        float a0 = col <= t ? v[8 * j + 2 * e] : 0.f;
-                        float a1 = col + 1 <= t ? v[8 * j + 2 * e + 1] : 0.f;
-                        w[e] = pack_bf16x2(a0, a1);
-                        float2 r = unpack_bf16x2(w[e]);
-                        den_intra += r.x + r.y;
-                    }
-                    const int chunk = (c0 % 64) / 8 + j;
-                    *reinterpret_cast<uint4 *>(blk + sw128_off(t, chunk)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
+                if (q * 32 < DP) {   // warp-uniform
+                    uint32_t v[CW];
+                    tmem_ld_cols<CW>(tmem + lane_base + PL::T_S + grp * CW, v);
+                    uint32_t zv[16];
+                    if (grp == 0) tmem_ld16_nowait(tmem + lane_base + PL::T_Z, zv);
+                    tmem_ld_wait();
+                    store_row_bf16<CW>(St, DP, row, grp * CW, v);
+                    if (grp == 0) store_zp_row(Zt, row, __uint_as_float(zv[0]));
                 }
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            math_bar();
-            if (t == 0) mbar_arrive(p_ready);
-            // 4. out = num / den
+            math_bar<NMATH>();
+            if (threadIdx.x == 0) mbar_arrive(ops_ready);
+            // 3. P = bf16(tril(A)) into TMEM
+            wait_ok(mma1_bar, c & 1, abort_flag, err);
+            tc_fence_after();
+            {
+                uint32_t a[32], pk[16];
+                tmem_ld32_nowait(tmem + lane_base + PL::T_A + grp * 32, a);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; i++) {
+                    const int col = grp * 32 + 2 * i;
+                    pk[i] = pack_bf16x2(col <= row ? __uint_as_float(a[2 * i]) : 0.f,
+                                        col + 1 <= row ? __uint_as_float(a[2 * i + 1]) : 0.f);
+                }
+                tmem_st16_nowait(tmem + lane_base + PL::T_P + grp * 16, pk);
+                tmem_st_wait();
+            }
+            tc_fence_before();
+            math_bar<NMATH>();
+            if (threadIdx.x == 0) mbar_arrive(p_ready);
+            // 4. out = NUM / (DEN[0] + DEN[8])
             const bool ok = wait_ok(mma2_bar, c & 1, abort_flag, err);
             tc_fence_after();
-            const float inv = 1.f / (den_intra + den_inter);
-            __nv_bfloat16 *orow =
-                out + ((long long)head * g.N + (long long)(c_begin + c) * kC + t) * DV;
+            {
+                uint32_t v[CW], d[16];
+                tmem_ld_cols<CW>(tmem + lane_base + PL::T_NUM + grp * CW, v);
+                tmem_ld16_nowait(tmem + lane_base + PL::T_DEN, d);
+                tmem_ld_wait();
+                const float inv = 1.f / (__uint_as_float(d[0]) + __uint_as_float(d[8]));
+                if (ok && row < n_valid) {
+                    __nv_bfloat16 *orow =
+                        out + ((long long)head * g.N + (long long)(c_begin + c) * kC + row) * DV +
+                        grp * CW;
 #pragma unroll
-            for (int c0 = 0; c0 < DV; c0 += 32) {
-                float v[32];
-                tmem_ld32(tmem + lane_base + PL::TMEM_NUM + c0, v);
-                if (ok && t < n_valid) {
-#pragma unroll
-                    for (int j = 0; j < 4; j++)
-                        *reinterpret_cast<uint4 *>(orow + c0 + 8 * j) =
-                            make_uint4(pack_bf16x2(v[8 * j] * inv, v[8 * j + 1] * inv),
-                                       pack_bf16x2(v[8 * j + 2] * inv, v[8 * j + 3] * inv),
-                                       pack_bf16x2(v[8 * j + 4] * inv, v[8 * j + 5] * inv),
-                                       pack_bf16x2(v[8 * j + 6] * inv, v[8 * j + 7] * inv));
+                    for (int j = 0; j < CW / 8; j++)
+                        *reinterpret_cast<uint4 *>(orow + 8 * j) = make_uint4(
+                            pack_bf16x2(__uint_as_float(v[8 * j]) * inv, __uint_as_float(v[8 * j + 1]) * inv),
+                            pack_bf16x2(__uint_as_float(v[8 * j + 2]) * inv, __uint_as_float(v[8 * j + 3]) * inv),
+                            pack_bf16x2(__uint_as_float(v[8 * j + 4]) * inv, __uint_as_float(v[8 * j + 5]) * inv),
+                            pack_bf16x2(__uint_as_float(v[8 * j + 6]) * inv, __uint_as_float(v[8 * j + 7]) * inv));
                 }
             }
             tc_fence_before();
         }
         // final state of the last segment -> S_out, z_out
         const bool aborted = __any_sync(0xffffffffu, *abort_flag != 0);   // warp-uniform
-        if (last_seg && (S_out || z_out) && !aborted) {
+        if (seg == g.nseg - 1 && (S_out || z_out) && !aborted && q * 32 < DP) {
             tc_fence_after();
-            if (warp < (DP + 31) / 32) {
+            uint32_t v[CW], zv[16];
+            tmem_ld_cols<CW>(tmem + lane_base + PL::T_S + grp * CW, v);
+            tmem_ld16_nowait(tmem + lane_base + PL::T_Z, zv);
+            tmem_ld_wait();
+            if (S_out) {
+                float *dst = S_out + ((long long)head * DP + row) * DV + grp * CW;
 #pragma unroll
-                for (int c0 = 0; c0 < DV; c0 += 32) {
-                    float v[32];
-                    tmem_ld32(tmem + lane_base + PL::TMEM_S + c0, v);
-                    if (S_out) {
-                        float *dst = S_out + ((long long)head * DP + t) * DV + c0;
-#pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            *reinterpret_cast<float4 *>(dst + i) =
-                                make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-                    }
-                }
-                if (z_out && t < DP) z_out[(long long)head * DP + t] = zs[t];
+                for (int i = 0; i < CW; i += 4)
+                    *reinterpret_cast<float4 *>(dst + i) =
+                        make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                    __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
             }
+            if (z_out && grp == 0) z_out[(long long)head * DP + row] = __uint_as_float(zv[0]);
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == MMAW) {
         tc_fence_after();
         tmem_dealloc(tmem, PL::TMEM_COLS);
     }
@@ -712,7 +741,7 @@ cudaError_t run(const Problem &p, void *scratch, float *S_out, float *z_out, int
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SP::SMEM)) !=
             cudaSuccess)
             return e;
-        tc_state_kernel<DP, DV><<<dim3(g.nseg, (unsigned)p.BH), kThreads, SP::SMEM, s>>>(
+        tc_state_kernel<DP, DV><<<dim3(g.nseg, (unsigned)p.BH), kStateThreads, SP::SMEM, s>>>(
             tk, tv, g, dS, dz, err);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         const int sz = DP * DV + DP;
@@ -724,7 +753,7 @@ cudaError_t run(const Problem &p, void *scratch, float *S_out, float *z_out, int
     if ((e = cudaFuncSetAttribute(tc_out_kernel<DP, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   OP::SMEM)) != cudaSuccess)
         return e;
-    tc_out_kernel<DP, DV><<<dim3(g.nseg, (unsigned)p.BH), kThreads, OP::SMEM, s>>>(
+    tc_out_kernel<DP, DV><<<dim3(g.nseg, (unsigned)p.BH), kOutThreads, OP::SMEM, s>>>(
         tq, tk, tv, g, dS, dz, (__nv_bfloat16 *)p.out, S_out, z_out, err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     note_launches(launches + 1);
