@@ -77,6 +77,39 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *e
     return true;
 }
 
+// ------------------------------------------------------------ shared memory
+
+// 16-byte shared-memory load / store at a shared-window address.
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// ------------------------------------------------------- global flags
+
+__device__ __forceinline__ int ld_acquire_gpu(const int *p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(int *p, int v)
+{
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 
 // 3-D tiled TMA load (coordinates innermost first) into shared memory,
@@ -89,6 +122,42 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *tmap, ui
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
         : "memory");
+}
+
+// L2 cache policies for TMA loads: keep (data read again soon) or stream.
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// tma_load_3d with an L2 cache policy.
+__device__ __forceinline__ void tma_load_3d_hint(void *smem_dst, const void *tmap, uint64_t *bar,
+                                                 int c0, int c1, int c2, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
+        "l"(policy)
+        : "memory");
+}
+
+// Prefetch one 3-D box of a tensor map into L2 (no shared memory involved).
+__device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int c0, int c1, int c2)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const void *tmap)
@@ -223,6 +292,21 @@ __device__ __forceinline__ void tmem_st16_nowait(uint32_t taddr, const uint32_t 
         : "memory");
 }
 
+// Store 32 consecutive 32-bit columns of this thread's TMEM lane (no wait).
+__device__ __forceinline__ void tmem_st32_nowait(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
 // Store 32 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32])
 {
@@ -307,6 +391,33 @@ __device__ __forceinline__ uint32_t sw32_off(int row, int chunk)
 __device__ __forceinline__ uint32_t sw128_off(int row, int chunk)
 {
     return (uint32_t)row * 128u + ((uint32_t)(chunk ^ (row & 7)) << 4);
+}
+
+// phi(x) = elu(x) + 1 on two packed bf16, in bf16x2 arithmetic:
+//   phi(x) = 2^(min(x, 0) * log2(e)) + max(x, 0),
+// which is exp(x) for x <= 0 and 1 + x for x > 0.  log2(e) is applied as a
+// bf16 hi + lo pair (1.4453125 - 0.00262451171875, within 7.1e-6 of log2 e)
+// so that the only roundings are those of the bf16 operations themselves;
+// the power of two is the ex2.approx.bf16x2 instruction.
+__device__ __forceinline__ uint32_t phi_elu1_bf16x2(uint32_t x)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b32 mn, mx, t, y, e;\n\t"
+        "min.bf16x2 mn, %1, %2;\n\t"
+        "max.bf16x2 mx, %1, %2;\n\t"
+        "mul.rn.bf16x2 t, mn, %4;\n\t"
+        "fma.rn.bf16x2 y, mn, %3, t;\n\t"
+        "ex2.approx.ftz.bf16x2 e, y;\n\t"
+        "add.rn.bf16x2 %0, e, mx;\n\t}"
+        : "=r"(r)
+        : "r"(x), "r"(0u), "r"(0x3FB93FB9u), "r"(0xBB2CBB2Cu));
+    return r;
+}
+
+__device__ __forceinline__ uint4 phi_elu1_bf16x8(uint4 v)
+{
+    return make_uint4(phi_elu1_bf16x2(v.x), phi_elu1_bf16x2(v.y), phi_elu1_bf16x2(v.z),
+                      phi_elu1_bf16x2(v.w));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)

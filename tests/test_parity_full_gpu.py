@@ -100,19 +100,25 @@ def test_segment_plan_matches_single_segment(la):
     assert e <= 2e-2, e
 
 
-def test_tensor_core_path_is_used(la):
-    """bf16 elu+1 with D, Dv in {64, 128} runs the tcgen05 kernels: a
-    multi-segment problem launches the state pass, the scan and the output
-    pass (three kernels), the CUDA-core kernel would launch one."""
-    w = wl.small(B=1, H=2, N=2048, D=128, Dv=128, seed=5)
-    q, k, v = (t.cuda() for t in wl.make_qkv(w))
-    n0 = la.la_launch_count()
-    la.la_forward(q, k, v, causal=True)
-    torch.cuda.synchronize()
-    assert la.la_launch_count() - n0 == 3
-    w = wl.small(B=1, H=2, N=2048, D=32, Dv=32, seed=5)
-    q, k, v = (t.cuda() for t in wl.make_qkv(w))
-    n0 = la.la_launch_count()
-    la.la_forward(q, k, v, causal=True)
-    torch.cuda.synchronize()
-    assert la.la_launch_count() - n0 == 1
+def test_causal_forward_is_one_launch(la):
+    """The causal forward is one kernel launch whatever the segment plan:
+    the tensor-core kernel (bf16 elu+1, D and Dv in {64, 128}) chains its
+    segments inside the launch, and the CUDA-core kernel walks whole heads."""
+    for D in (128, 32):
+        w = wl.small(B=1, H=2, N=2048, D=D, Dv=D, seed=5)
+        q, k, v = (t.cuda() for t in wl.make_qkv(w))
+        n0 = la.la_launch_count()
+        la.la_forward(q, k, v, causal=True)
+        torch.cuda.synchronize()
+        assert la.la_launch_count() - n0 == 1
+
+
+@pytest.mark.parametrize("H,N,D,Dv", [(3, 128 * 37 + 5, 128, 128), (2, 128 * 21 + 77, 64, 128),
+                                      (5, 128 * 11 + 1, 128, 64), (1, 128 * 64, 64, 64)])
+def test_long_segment_chain_all_heads(la, H, N, D, Dv):
+    """Few heads and many chunks: the heads are cut into short segments whose
+    states are chained across CTAs; every head, every position is checked,
+    including a ragged last chunk."""
+    w = wl.small(B=1, H=H, N=N, D=D, Dv=Dv, seed=N + H)
+    err, _ = _forward_and_check(la, w)
+    assert err <= 2e-2
