@@ -10,40 +10,41 @@
 //   out  = (A V_c + phi(Q_c) S_prev) / (rowsum(A) + phi(Q_c) z_prev)
 //   S   += phi(K_c)^T V_c,   z += colsum(phi(K_c)).
 //
-// Work items.  Each head's chunks are grouped into segments of L chunks; an
-// item is one (head, segment).  Items are numbered segment-major and handed
-// out in that order from a global ticket counter, so an item's predecessor
-// (same head, previous segment) is always taken by a CTA that is already
-// running.  Per item a CTA runs
-//   phase A  the segment's own sums  S_loc = phi(K)^T V,  z_loc = colsum phi(K)
-//            (skipped for the last segment of a head, whose sums nobody needs);
-//   phase B  waits for the predecessor's inclusive state (S, z after the
-//            previous segment), publishes its own = that + (S_loc, z_loc),
-//            and starts the chunk recurrence from the predecessor's state;
-//   phase C  the chunk recurrence above over the segment, writing out.
-// Phase C re-reads the K, V tiles that phase A loaded a few microseconds
-// earlier; segments are short enough (L <= 8 chunks) for that re-read to be
-// served by L2, so HBM sees q, k, v and out once.  This is the exclusive
-// prefix over segments of the "RNN with two memories" view, chained through
-// global memory with acquire/release flags.  With one segment per head
-// (B*H >= the number of SMs) phases A and B reduce to zeroing the state.
+// Work items.  When B*H is below the number of SMs, each head's chunks are
+// cut into segments so that every SM gets one (head, segment) item; an item
+// needs the state (S, z) after the previous segments of its head.  That
+// prefix comes from a separate pass over K, V: the kernel runs first in its
+// aggregate form (AGG = true: each item only sums phi(K)^T V and colsum
+// phi(K) over its segment, into scratch), a small scan turns those sums into
+// exclusive prefixes over segments, and the output form (AGG = false) starts
+// each segment's chunk recurrence from its prefix.  Items are handed out from
+// a global ticket counter.  (Chaining the segment states from CTA to CTA in
+// one pass was measured slower: under a full HBM load every link costs
+// several microseconds of global-memory round trips, and the chain advances
+// one segment per link.)
 //
 // Warp roles (16 warps, 4 per SM sub-partition, so 128 registers):
-//   warps 0-7   TMEM warps: the state copy S_prev / ZP for each chunk, the
-//               masked scores P, the epilogue, phase B.  Warp w owns TMEM lane
-//               quadrant w % 4 (rows 32 (w%4) ..) and column half w / 4.
+//   warps 0-7   TMEM warps: phi(Q) in place on the Q tile, masked scores P,
+//               the state copy S_prev / ZP for the next chunk, the epilogue,
+//               phase B.  Warp w owns TMEM lane quadrant w % 4 (rows 32 (w%4)
+//               ..) and column half w / 4.
 //   warps 8-11  phi warps, one per lane quadrant (one tile row per thread):
-//               phi(Q) written straight into TMEM as the A operand of the
-//               Q-side products, phi(K) applied in place on the K tile.
+//               phi(K) in place on the K tile in shared memory.
 //   warp 12     TMA producer of Q tiles and item scheduler.
-//   warp 13     TMA producer of K tiles (freed after MMA4).
-//   warp 14     TMA producer of V tiles (freed after MMA2).
+//   warp 13     TMA producer of K tiles.
+//   warp 14     TMA producer of V tiles (lane 0) and TMA store of the output
+//               tiles (lane 1).
 //   warp 15     MMA issuer (one thread).
-// The producers prefetch tiles two chunks ahead into L2, so the loads into
-// shared memory (whose buffers free up only as the pipeline drains them)
-// wait for L2 rather than HBM.
-// Per chunk, all tcgen05.mma with fp32 accumulation in TMEM:
-//   MMA1   A    = phiQ . phiK^T        M=C, N=C,  K=Dphi   (phiQ from TMEM)
+// The epilogue writes each output tile into the shared-memory slot of that
+// chunk's V tile (V is dead once MMA2 has read it; the two tiles have the
+// same shape and swizzle), and one thread stores it with a TMA tile store,
+// releasing the V slot once the store has read it.
+// The producers prefetch a tile ahead into L2.  Q, K and V have their own
+// rings because they free up at different points: Q after MMA3, K after
+// MMA4, V after MMA2.
+//
+// Per chunk c, all tcgen05.mma with fp32 accumulation in TMEM:
+//   MMA1   A    = phiQ . phiK^T        M=C, N=C,  K=Dphi
 //   MMA3   NUM  = phiQ . S_prev        M=C, N=Dv, K=Dphi   (S_prev bf16 in smem)
 //   MMA3b  DEN  = phiQ . ZP            M=C, N=16, K=Dphi
 //   MMA4   S   += phiK^T . V           M=Dphi, N=Dv, K=C
@@ -53,6 +54,15 @@
 // ONES is a constant [C x 16] tile (columns 0-7 = 1, 8-15 = 0) and ZP holds
 // z_prev split into bf16 hi (columns 0-7) and lo (columns 8-15), so that
 // out = NUM / (DEN[:,0] + DEN[:,8]).  phi never goes back to HBM.
+// TMEM holds two 128-column regions R0, R1 that chunks use alternately:
+// chunk k's scores A(k) land in R[k % 2], and once the TMEM warps have read
+// them into registers (as the masked bf16 P, which gets its own slot) the
+// same region takes NUM(k).  So MMA3(k) never waits for the epilogue of
+// k - 1; only MMA1(k + 2) needs R[k % 2] back.  The issue order per chunk is
+// MMA3(k), MMA4(k), MMA1(k+1), MMA2(k), which keeps independent work in the
+// tensor pipe while the TMEM warps convert A(k + 1) and drain NUM(k).  At D = Dv = 128 S_prev is staged in
+// two 64-row halves (the second written once MMA3 has read the first), which
+// leaves shared memory for two-deep Q, K and V rings.
 //
 // Every wait is bounded (clock64 budget).  On expiry the kernel sets the
 // library's device error word, raises a per-launch abort word that every
@@ -72,7 +82,6 @@ using namespace tc;
 constexpr int kC = 128;               // chunk length (MMA M)
 constexpr int kErrTimeout = 1;
 constexpr long long kWaitBudget = 4000000000LL;   // SM cycles (~2 s)
-constexpr int kMaxItemChunks = 8;     // L <= 8 keeps the phase-C re-read in L2
 
 constexpr int kTmemWarps = 8;
 constexpr int kPhiWarps = 4;
@@ -81,50 +90,53 @@ constexpr int kKWarp = kProducerWarp + 1;               // 13: K tiles
 constexpr int kVWarp = kKWarp + 1;                      // 14: V tiles
 constexpr int kMmaWarp = kVWarp + 1;                    // 15
 constexpr int kThreads = (kMmaWarp + 1) * 32;           // 512
-constexpr int kPrefetch = 3;                            // chunks of L2 prefetch ahead
-constexpr int kItemConsumers = kTmemWarps + kPhiWarps + 3;
+constexpr int kPrefetch = 1;                            // chunks of L2 prefetch ahead
+constexpr int kItemConsumers = kTmemWarps + kPhiWarps + 4;
 
 template <int DP, int DV>
 struct Plan {
     static constexpr int QB = kC * DP * 2;   // one Q or K chunk tile (bytes)
     static constexpr int VB = kC * DV * 2;   // one V chunk tile
-    static constexpr int SB = DP * DV * 2;   // S_prev, bf16
     static constexpr int ZB = DP * 32;       // ZP [DP x 16] bf16, 32-byte swizzle
     static constexpr int OB = kC * 32;       // ONES [C x 16]
-    static constexpr int kFixed = SB + ZB + OB;
     static constexpr int kBudget = 227 * 1024 - 2048;
-    static constexpr int NS = (kFixed + QB + 4 * (QB + VB) <= kBudget)   ? 4
-                              : (kFixed + QB + 3 * (QB + VB) <= kBudget) ? 3
-                                                                          : 2;
-    static constexpr int NQ = (kFixed + 2 * QB + NS * (QB + VB) <= kBudget) ? 2 : 1;
+    // S_prev pieces along Dphi: one, or two 64-row halves when that is what
+    // lets two-deep rings fit
+    static constexpr int NSP = (2 * (2 * QB + VB) + DP * DV * 2 + ZB + OB <= kBudget) ? 1 : 2;
+    static constexpr int PR = DP / NSP;      // S_prev rows per piece
+    static constexpr int SB = PR * DV * 2;
+    static constexpr int kFixed = SB + ZB + OB;
+    static constexpr int NS = (kFixed + 4 * (2 * QB + VB) <= kBudget)   ? 4
+                              : (kFixed + 3 * (2 * QB + VB) <= kBudget) ? 3
+                                                                         : 2;
     static constexpr int Q0 = 0;
-    static constexpr int K0 = Q0 + NQ * QB;
+    static constexpr int K0 = Q0 + NS * QB;
     static constexpr int V0 = K0 + NS * QB;
     static constexpr int S0 = V0 + NS * VB;
     static constexpr int Z0 = S0 + SB;
     static constexpr int O0 = Z0 + ZB;
     static constexpr int TILES = O0 + OB;
     static constexpr int SMEM = TILES + 1024 /* alignment */ + 1024 /* barriers */;
-    // TMEM columns
-    static constexpr int T_S = 0, T_Z = DV, T_DEN = DV + 32, T_NUM = DV + 64, T_A = 2 * DV + 64,
-                         T_Q = 2 * DV + 192;
+    // TMEM columns: state S, z; the denominators of the two regions; the
+    // regions R0, R1 (A then NUM of alternate chunks); the bf16 P
+    static constexpr int T_S = 0, T_Z = DV, T_DEN0 = DV + 16, T_R0 = DV + 64, T_P = DV + 320;
     static constexpr int TMEM_COLS = 512;
-    static_assert(T_Q + DP / 2 <= TMEM_COLS, "TMEM plan too large");
+    static_assert(T_P + kC / 2 <= TMEM_COLS, "TMEM plan too large");
     static_assert(SMEM <= 227 * 1024, "shared memory plan too large");
+    static_assert(SMEM > 114 * 1024, "one CTA per SM: the kernel holds all 512 TMEM columns");
 };
 
 struct Geo {
     int BH, N, NC;   // heads, positions, chunks per head
     int L, nseg;     // chunks per segment, segments per head
-    int n_items;     // BH * nseg
+    int n_items;     // items of this launch: B*H*(nseg-1) (aggregate form) or B*H*nseg
 };
 
 struct Scratch {
     int *ticket;     // next item to hand out
     int *abort;      // raised by any CTA whose wait ran out
-    int *flags;      // [BH * nseg]: 1 once the inclusive state of (head, seg) is published
-    float *inclS;    // [BH * nseg, DP, DV]
-    float *inclz;    // [BH * nseg, DP]
+    float *preS;     // [BH, nseg, DP, DV]: segment sums, then their exclusive prefixes
+    float *prez;     // [BH, nseg, DP]
 };
 
 struct Ctl {
@@ -165,14 +177,14 @@ __device__ __forceinline__ uint32_t tile_off(int r, int j)
 }
 
 // One S_prev row block: 32 fp32 state values -> bf16 at row r, columns
-// [c0, c0 + 32) of the MN-major [DP x DV] tile (DV / 64 blocks of DP rows).
-template <int DP>
+// [c0, c0 + 32) of an MN-major [PR x DV] piece (DV / 64 blocks of PR rows).
+template <int PR>
 __device__ __forceinline__ void sprev_store32(uint32_t st, int r, int c0, const uint32_t (&v)[32])
 {
 #pragma unroll
     for (int j = 0; j < 4; j++) {
         const int col = c0 + 8 * j;
-        const uint32_t a = st + (uint32_t)(col >> 6) * (DP * 128) + sw128_off(r, (col & 63) >> 3);
+        const uint32_t a = st + (uint32_t)(col >> 6) * (PR * 128) + sw128_off(r, (col & 63) >> 3);
         sts128(a, make_uint4(
                       pack_bf16x2(__uint_as_float(v[8 * j]), __uint_as_float(v[8 * j + 1])),
                       pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
@@ -192,67 +204,71 @@ __device__ __forceinline__ void zp_store(uint32_t zp, int r, float z)
 
 // ---------------------------------------------------------------- kernel
 
-template <int DP, int DV>
+template <int DP, int DV, bool AGG>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, Geo g, Scratch sc,
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                 Geo g, Scratch sc,
                  __nv_bfloat16 *__restrict__ out, float *__restrict__ S_out,
                  float *__restrict__ z_out, int *err)
 {
     using PL = Plan<DP, DV>;
-    constexpr int NS = PL::NS, NQ = PL::NQ;
+    constexpr int NS = PL::NS, NSP = PL::NSP, PR = PL::PR;
     constexpr int HALF = DV / 2;   // state / NUM columns per TMEM warp
     extern __shared__ unsigned char smem_raw[];
     const uint32_t base = align1k(smem_u32(smem_raw));
     unsigned char *gbase = smem_raw + (base - smem_u32(smem_raw));   // generic view of `base`
     uint64_t *bar = reinterpret_cast<uint64_t *>(gbase + PL::TILES);
-    uint64_t *k_full = bar, *k_ready = bar + 4, *k_empty = bar + 8;
-    uint64_t *v_full = bar + 12, *v_empty = bar + 16;
-    uint64_t *q_full = bar + 20, *q_empty = bar + 22;
-    uint64_t *item_full = bar + 24, *item_empty = bar + 26;
-    uint64_t *tq_full = bar + 28, *tq_free = bar + 29, *a_full = bar + 30, *p_ready = bar + 31,
-             *sprev_ready = bar + 32, *s_done = bar + 33, *num_full = bar + 34,
-             *num_free = bar + 35, *sloc_done = bar + 36, *drain = bar + 37,
-             *chain_ok = bar + 38, *pub_ready = bar + 39;
-    volatile int *item_slot = reinterpret_cast<volatile int *>(bar + 40);   // [2]
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 41);
-    volatile int *abort_cta = reinterpret_cast<volatile int *>(bar + 42);
+    uint64_t *q_full = bar, *q_ready = bar + 4, *q_empty = bar + 8;
+    uint64_t *k_full = bar + 12, *k_ready = bar + 16, *k_empty = bar + 20;
+    uint64_t *v_full = bar + 24, *v_empty = bar + 28;
+    uint64_t *item_full = bar + 32, *item_empty = bar + 34;
+    uint64_t *sp_ready = bar + 36;   // [2] S_prev piece written
+    uint64_t *a_full = bar + 38, *a_free = bar + 39, *p_ready = bar + 40, *sp_free = bar + 41,
+             *s_done = bar + 42, *num_full = bar + 43, *sloc_done = bar + 45, *drain = bar + 46;
+    uint64_t *sloc_read = bar + 47;   // [2] aggregate form: the sums in region r have been read
+    uint64_t *num_free = bar + 53;   // [2]: the epilogue has read NUM from region r
+    uint64_t *out_ready = bar + 56;  // [NS]: the output tile of a chunk is in its V slot
+    volatile int *item_slot = reinterpret_cast<volatile int *>(bar + 50);   // [2]
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 51);
+    volatile int *abort_cta = reinterpret_cast<volatile int *>(bar + 52);   // bar + 53, 54: num_free
     const Ctl ctl{abort_cta, sc.abort, err};
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; i++) {
+            mbar_init(&q_full[i], 1);
+            mbar_init(&q_ready[i], kTmemWarps);
+            mbar_init(&q_empty[i], 1);
             mbar_init(&k_full[i], 1);
             mbar_init(&k_ready[i], kPhiWarps);
             mbar_init(&k_empty[i], 1);
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
         }
-        for (int i = 0; i < NQ; i++) {
-            mbar_init(&q_full[i], 1);
-            mbar_init(&q_empty[i], kPhiWarps);
-        }
         for (int i = 0; i < 2; i++) {
             mbar_init(&item_full[i], 1);
-            mbar_init(&item_empty[i], kItemConsumers);
+            mbar_init(&item_empty[i], AGG ? kItemConsumers - 1 : kItemConsumers);   // no store lane in AGG
+            mbar_init(&sp_ready[i], NSP == 1 ? kTmemWarps : kTmemWarps / 2);
         }
-        mbar_init(tq_full, kPhiWarps);
-        mbar_init(tq_free, 1);
         mbar_init(a_full, 1);
+        mbar_init(a_free, kTmemWarps);
         mbar_init(p_ready, kTmemWarps);
-        mbar_init(sprev_ready, kTmemWarps);
+        mbar_init(sp_free, 1);
         mbar_init(s_done, 1);
         mbar_init(num_full, 1);
-        mbar_init(num_free, kTmemWarps);
+        mbar_init(&num_free[0], kTmemWarps);
+        mbar_init(&num_free[1], kTmemWarps);
+        for (int i = 0; i < NS; i++) mbar_init(&out_ready[i], kTmemWarps);
+        mbar_init(&sloc_read[0], kTmemWarps);
+        mbar_init(&sloc_read[1], kTmemWarps);
         mbar_init(sloc_done, 1);
         mbar_init(drain, 1);
-        mbar_init(chain_ok, 1);
-        mbar_init(pub_ready, kTmemWarps);
         *abort_cta = 0;
         fence_mbar_init();
     }
-    if (warp < kTmemWarps) {   // the constant ONES tile
+    if (warp < kTmemWarps) {   // the constant ONES tile (bar + 47 .. 48: sloc_read)
         const uint32_t one = pack_bf16x2(1.f, 1.f);
         const uint32_t ones = base + PL::O0;
         for (int r = threadIdx.x; r < kC; r += kTmemWarps * 32) {
@@ -267,59 +283,21 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
-    if (warp == kProducerWarp) {
-        // ------------------------------------------ Q producer / scheduler
+    if (warp == kProducerWarp || warp == kKWarp || warp == kVWarp) {
+        // ---------------------------------------- Q / K / V tile producers
+        // The Q producer also hands out the items.  Phase A streams the
+        // segment's K, V from HBM (kept in L2 for phase C); phase C reads Q
+        // from HBM and K, V again (from L2 when phase A ran).
         if (lane == 0) {
-            prefetch_tmap(&tm_q);
-            const uint64_t stream = policy_evict_first();
-            uint32_t nq = 0;
-            for (int it = 0;; it++) {
-                const int slot = it & 1;
-                bool ok = it < 2 || wait_bar(&item_empty[slot], ((it >> 1) - 1) & 1, ctl);
-                int item = -1;
-                if (ok && !*abort_cta) {
-                    item = atomicAdd(sc.ticket, 1);
-                    if (item >= g.n_items) item = -1;
-                }
-                item_slot[slot] = item;
-                mbar_arrive(&item_full[slot]);
-                if (item < 0) break;
-                const int s = item / g.BH, h = item % g.BH;
-                const int c0 = s * g.L, nc = min(g.L, g.NC - c0);
-                for (int c = 0; c < nc && c < kPrefetch; c++)
-                    for (int b = 0; b < DP / 64; b++) tma_prefetch_3d(&tm_q, b * 64, (c0 + c) * kC, h);
-                for (int c = 0; c < nc && ok; c++) {
-                    if (c + kPrefetch < nc)
-                        for (int b = 0; b < DP / 64; b++)
-                            tma_prefetch_3d(&tm_q, b * 64, (c0 + c + kPrefetch) * kC, h);
-                    const int st = nq % NQ;
-                    if (nq >= NQ && !wait_bar(&q_empty[st], ((nq / NQ) - 1) & 1, ctl)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&q_full[st], PL::QB);
-#pragma unroll
-                    for (int b = 0; b < DP / 64; b++)
-                        tma_load_3d_hint(gbase + PL::Q0 + st * PL::QB + b * kC * 128, &tm_q, &q_full[st],
-                                         b * 64, (c0 + c) * kC, h, stream);
-                    nq++;
-                }
-            }
-            // drain loads still in flight (only possible after an abort)
-            for (uint32_t n = nq > NQ ? nq - NQ : 0; n < nq; n++)
-                mbar_wait(&q_full[n % NQ], (n / NQ) & 1, nullptr, 0);
-        }
-    } else if (warp == kKWarp || warp == kVWarp) {
-        // ------------------------------------------- K or V tile producer
-        if (lane == 0) {
-            const bool isK = warp == kKWarp;
-            const CUtensorMap *tm = isK ? &tm_k : &tm_v;
-            const int nb = isK ? DP / 64 : DV / 64;   // 64-column boxes per tile
-            const int tb = isK ? PL::QB : PL::VB;     // tile bytes
-            unsigned char *ring = gbase + (isK ? PL::K0 : PL::V0);
-            uint64_t *full = isK ? k_full : v_full, *empty = isK ? k_empty : v_empty;
+            const int role = warp - kProducerWarp;   // 0 Q, 1 K, 2 V
+            const CUtensorMap *tm = role == 0 ? &tm_q : role == 1 ? &tm_k : &tm_v;
+            const int nb = role == 2 ? DV / 64 : DP / 64;   // 64-column boxes per tile
+            const int tb = role == 2 ? PL::VB : PL::QB;     // tile bytes
+            unsigned char *ring = gbase + (role == 0 ? PL::Q0 : role == 1 ? PL::K0 : PL::V0);
+            uint64_t *full = role == 0 ? q_full : role == 1 ? k_full : v_full;
+            uint64_t *empty = role == 0 ? q_empty : role == 1 ? k_empty : v_empty;
             prefetch_tmap(tm);
-            const uint64_t keep = policy_evict_last(), stream = policy_evict_first();
+            const uint64_t stream = policy_evict_first();
             uint32_t n = 0;
             bool ok = true;
             auto prefetch = [&](int head, int chunk) {
@@ -337,28 +315,63 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             };
             for (int it = 0; ok; it++) {
                 const int slot = it & 1;
+                int item = -1;
+                if (role == 0) {
+                    ok = it < 2 || wait_bar(&item_empty[slot], ((it >> 1) - 1) & 1, ctl);
+                    if (ok && !*abort_cta) {
+                        item = atomicAdd(sc.ticket, 1);
+                        if (item >= g.n_items) item = -1;
+                    }
+                    item_slot[slot] = item;
+                    mbar_arrive(&item_full[slot]);
+                } else {
+                    if (!wait_bar(&item_full[slot], (it >> 1) & 1, ctl)) break;
+                    item = item_slot[slot];
+                    mbar_arrive(&item_empty[slot]);
+                }
+                if (item < 0) break;
+                const int s = item / g.BH, h = item % g.BH;
+                const int c0 = s * g.L, nc = min(g.L, g.NC - c0);
+                if (AGG && role == 0) continue;   // the aggregate form reads no Q
+                for (int c = 0; c < nc && c < kPrefetch; c++) prefetch(h, c0 + c);
+                for (int c = 0; c < nc && ok; c++) {
+                    if (c + kPrefetch < nc) prefetch(h, c0 + c + kPrefetch);
+                    ok = load(h, c0 + c, stream);
+                }
+            }
+            // drain loads still in flight (only possible after an abort)
+            for (uint32_t m = n > NS ? n - NS : 0; m < n; m++)
+                mbar_wait(&full[m % NS], (m / NS) & 1, nullptr, 0);
+        }
+        if (!AGG && warp == kVWarp && lane == 1) {
+            // ------------------------------------------ output tile stores
+            prefetch_tmap(&tm_o);
+            uint32_t nv = 0;        // V ring position
+            uint32_t oc[4] = {0, 0, 0, 0};   // output tiles seen per V slot
+            for (int it = 0;; it++) {
+                const int slot = it & 1;
                 if (!wait_bar(&item_full[slot], (it >> 1) & 1, ctl)) break;
                 const int item = item_slot[slot];
                 mbar_arrive(&item_empty[slot]);
                 if (item < 0) break;
                 const int s = item / g.BH, h = item % g.BH;
                 const int c0 = s * g.L, nc = min(g.L, g.NC - c0);
-                const bool hasA = s + 1 < g.nseg;
-                // phase A streams the segment from HBM (kept in L2 for phase C);
-                // phase C re-reads it (from L2 when phase A ran)
-                for (int c = 0; c < nc && c < kPrefetch; c++) prefetch(h, c0 + c);
-                if (hasA)
-                    for (int c = 0; c < nc && ok; c++) {
-                        if (c + kPrefetch < nc) prefetch(h, c0 + c + kPrefetch);
-                        ok = load(h, c0 + c, keep);
+                for (int c = 0; c < nc; c++, nv++) {
+                    const int st = nv % NS;
+                    const bool ok = wait_bar(&out_ready[st], oc[st] & 1, ctl);
+                    oc[st]++;
+                    if (ok) {
+                        const uint32_t src = base + PL::V0 + st * PL::VB;
+#pragma unroll
+                        for (int b = 0; b < DV / 64; b++)
+                            tma_store_3d(&tm_o, src + b * kC * 128, b * 64, (c0 + c) * kC, h);
+                        bulk_commit_group();
+                        bulk_wait_read_all();
                     }
-                for (int c = 0; c < nc && ok; c++) {
-                    if (!hasA && c + kPrefetch < nc) prefetch(h, c0 + c + kPrefetch);
-                    ok = load(h, c0 + c, stream);
+                    mbar_arrive(&v_empty[st]);
                 }
             }
-            for (uint32_t m = n > NS ? n - NS : 0; m < n; m++)
-                mbar_wait(&full[m % NS], (m / NS) & 1, nullptr, 0);
+            bulk_wait_all();
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------- MMA issuer
@@ -370,7 +383,38 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             constexpr uint32_t id_k16 = idesc_bf16(128, 16, 1, 1);
             constexpr uint32_t lbo_kT = DP == 128 ? kC * 128 : 0;   // DP = 64: rows 64-127 repeat 0-63
             const uint32_t s_addr = base + PL::S0, zp_addr = base + PL::Z0, ones = base + PL::O0;
-            uint32_t nkv = 0, nchunk = 0, nfree = 0;
+            uint32_t nkv = 0;    // K / V ring loads consumed (phase A and C)
+            uint32_t nq = 0;     // Q ring loads consumed
+            uint32_t ndone = 0;  // phase-C chunks whose MMA2 has been issued (global chunk index)
+            uint32_t nfree[2] = {0, 0};   // num_free phases seen per region
+            // region r = k % 2 is free once the epilogue of chunk k has read NUM
+            auto wait_epi = [&](uint32_t k) {
+                const int rr = k & 1;
+                const uint32_t ph = k >> 1;
+                if (nfree[rr] <= ph) {
+                    wait_bar(&num_free[rr], ph & 1, ctl);
+                    nfree[rr] = ph + 1;
+                }
+            };
+            // MMA1(k): A = phiQ phiK^T into region k % 2
+            auto mma1 = [&](uint32_t k, uint32_t qn, uint32_t kn) {
+                if (k >= 2) wait_epi(k - 2);
+                wait_bar(&q_ready[qn % NS], (qn / NS) & 1, ctl);
+                wait_bar(&k_ready[kn % NS], (kn / NS) & 1, ctl);
+                tc_fence_after();
+                const uint32_t qa = base + PL::Q0 + (qn % NS) * PL::QB;
+                const uint32_t ka = base + PL::K0 + (kn % NS) * PL::QB;
+                const uint32_t dst = tmem + PL::T_R0 + (k & 1) * 128;
+                if (!*abort_cta) {
+#pragma unroll
+                    for (int kk = 0; kk < DP; kk += 16) {
+                        const uint32_t off = (kk / 64) * (kC * 128) + (kk % 64) * 2;
+                        mma_bf16_ss(dst, sw128_desc(qa + off, 16, 1024), sw128_desc(ka + off, 16, 1024),
+                                    id_qk, kk > 0 ? 1u : 0u);
+                    }
+                }
+                mma_commit(a_full);
+            };
             for (int it = 0;; it++) {
                 const int slot = it & 1;
                 if (!wait_bar(&item_full[slot], (it >> 1) & 1, ctl)) break;
@@ -379,14 +423,13 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (item < 0) break;
                 const int s = item / g.BH;
                 const int c0 = s * g.L, nc = min(g.L, g.NC - c0);
-                const bool hasA = s + 1 < g.nseg;
-                if (hasA) {
-                    // phase A: S_loc -> T_NUM, z_loc -> T_DEN (the previous item's
-                    // last epilogue must have read T_NUM first)
-                    if (nchunk > 0) {
-                        wait_bar(num_free, nfree & 1, ctl);
-                        nfree++;
-                    }
+                if constexpr (AGG) {
+                    // the segment's sums S_loc, z_loc into region it % 2 and its
+                    // denominator slot, once the TMEM warps have read item it - 2's
+                    const int rr = it & 1;
+                    if (it >= 2) wait_bar(&sloc_read[rr], ((it >> 1) - 1) & 1, ctl);
+                    const uint32_t dS = tmem + PL::T_R0 + rr * 128;
+                    const uint32_t dz = tmem + PL::T_DEN0 + rr * 16;
                     for (int c = 0; c < nc; c++) {
                         const int st = nkv % NS;
                         wait_bar(&k_ready[st], (nkv / NS) & 1, ctl);
@@ -399,10 +442,9 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             for (int k = 0; k < kC; k += 16) {
                                 const uint64_t ad = sw128_desc(ka + (k / 8) * 1024, lbo_kT, 1024);
                                 const uint32_t acc = (c > 0 || k > 0) ? 1u : 0u;
-                                mma_bf16_ss(tmem + PL::T_NUM, ad,
-                                            sw128_desc(va + (k / 8) * 1024, kC * 128, 1024), id_kv, acc);
-                                mma_bf16_ss(tmem + PL::T_DEN, ad,
-                                            sw32_desc(ones + (k / 8) * 256, 256, 256), id_k16, acc);
+                                mma_bf16_ss(dS, ad, sw128_desc(va + (k / 8) * 1024, kC * 128, 1024), id_kv,
+                                            acc);
+                                mma_bf16_ss(dz, ad, sw32_desc(ones + (k / 8) * 256, 256, 256), id_k16, acc);
                             }
                         }
                         mma_commit(&k_empty[st]);
@@ -410,76 +452,72 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         nkv++;
                     }
                     mma_commit(sloc_done);
+                    continue;
                 }
+                const uint32_t G = ndone;   // global index of this item's first chunk
+                // phase C: MMA1(G); then per chunk k: MMA3(k), MMA4(k), MMA1(k+1), MMA2(k)
+                mma1(G, nq, nkv);
                 for (int c = 0; c < nc; c++) {
-                    const int st = nkv % NS;
+                    const uint32_t k = G + c;
+                    const int qs = nq % NS, st = nkv % NS;
+                    const uint32_t qa = base + PL::Q0 + qs * PL::QB;
                     const uint32_t ka = base + PL::K0 + st * PL::QB;
                     const uint32_t va = base + PL::V0 + st * PL::VB;
-                    wait_bar(tq_full, nchunk & 1, ctl);
-                    wait_bar(&k_ready[st], (nkv / NS) & 1, ctl);
-                    if (nchunk > 0) wait_bar(num_full, (nchunk - 1) & 1, ctl);   // P of the last chunk read
-                    tc_fence_after();
-                    const bool live = !*abort_cta;
-                    // MMA1: A = phiQ phiK^T
-                    if (live) {
+                    const uint32_t rnum = tmem + PL::T_R0 + (k & 1) * 128;
+                    const uint32_t rden = tmem + PL::T_DEN0 + (k & 1) * 16;
+                    // MMA3 / MMA3b: NUM = phiQ S_prev, DEN = phiQ ZP (A(k) has been read)
+                    wait_bar(a_free, k & 1, ctl);
 #pragma unroll
-                        for (int k = 0; k < DP; k += 16)
-                            mma_bf16_ts(tmem + PL::T_A, tmem + PL::T_Q + k / 2,
-                                        sw128_desc(ka + (k / 64) * (kC * 128) + (k % 64) * 2, 16, 1024),
-                                        id_qk, k > 0 ? 1u : 0u);
-                    }
-                    mma_commit(a_full);
-                    // MMA3 / MMA3b: NUM = phiQ S_prev, DEN = phiQ ZP
-                    wait_bar(sprev_ready, nchunk & 1, ctl);
-                    if (nfree < nchunk) {   // the previous chunk's epilogue has read NUM
-                        wait_bar(num_free, nfree & 1, ctl);
-                        nfree++;
-                    }
-                    tc_fence_after();
-                    if (!*abort_cta) {
+                    for (int pc = 0; pc < NSP; pc++) {
+                        wait_bar(&sp_ready[pc], k & 1, ctl);
+                        tc_fence_after();
+                        if (!*abort_cta) {
 #pragma unroll
-                        for (int k = 0; k < DP; k += 16) {
-                            mma_bf16_ts(tmem + PL::T_NUM, tmem + PL::T_Q + k / 2,
-                                        sw128_desc(s_addr + (k / 8) * 1024, DP * 128, 1024), id_qs,
-                                        k > 0 ? 1u : 0u);
-                            mma_bf16_ts(tmem + PL::T_DEN, tmem + PL::T_Q + k / 2,
-                                        sw32_desc(zp_addr + (k / 8) * 256, 256, 256), id_q16,
-                                        k > 0 ? 1u : 0u);
+                            for (int kk = 0; kk < PR; kk += 16) {
+                                const int kq = pc * PR + kk;
+                                const uint64_t ad =
+                                    sw128_desc(qa + (kq / 64) * (kC * 128) + (kq % 64) * 2, 16, 1024);
+                                mma_bf16_ss(rnum, ad, sw128_desc(s_addr + (kk / 8) * 1024, PR * 128, 1024),
+                                            id_qs, kq > 0 ? 1u : 0u);
+                                mma_bf16_ss(rden, ad, sw32_desc(zp_addr + (kq / 8) * 256, 256, 256), id_q16,
+                                            kq > 0 ? 1u : 0u);
+                            }
                         }
+                        if (pc + 1 < NSP) mma_commit(sp_free);
                     }
-                    mma_commit(tq_free);
+                    mma_commit(&q_empty[qs]);
                     // MMA4 / MMA4b: S += phiK^T V, Z += phiK^T ONES
                     wait_bar(&v_full[st], (nkv / NS) & 1, ctl);
                     tc_fence_after();
                     if (!*abort_cta) {
 #pragma unroll
-                        for (int k = 0; k < kC; k += 16) {
-                            const uint64_t ad = sw128_desc(ka + (k / 8) * 1024, lbo_kT, 1024);
-                            mma_bf16_ss(tmem + PL::T_S, ad,
-                                        sw128_desc(va + (k / 8) * 1024, kC * 128, 1024), id_kv, 1u);
-                            mma_bf16_ss(tmem + PL::T_Z, ad, sw32_desc(ones + (k / 8) * 256, 256, 256),
+                        for (int kk = 0; kk < kC; kk += 16) {
+                            const uint64_t ad = sw128_desc(ka + (kk / 8) * 1024, lbo_kT, 1024);
+                            mma_bf16_ss(tmem + PL::T_S, ad, sw128_desc(va + (kk / 8) * 1024, kC * 128, 1024),
+                                        id_kv, 1u);
+                            mma_bf16_ss(tmem + PL::T_Z, ad, sw32_desc(ones + (kk / 8) * 256, 256, 256),
                                         id_k16, 1u);
                         }
                     }
                     mma_commit(s_done);
                     mma_commit(&k_empty[st]);
+                    // MMA1(k+1) into the other region
+                    if (c + 1 < nc) mma1(k + 1, nq + 1, nkv + 1);
                     // MMA2 / MMA2b: NUM += P V, DEN += P ONES  (P in TMEM)
-                    wait_bar(p_ready, nchunk & 1, ctl);
+                    wait_bar(p_ready, k & 1, ctl);
                     tc_fence_after();
                     if (!*abort_cta) {
 #pragma unroll
-                        for (int k = 0; k < kC; k += 16) {
-                            const uint32_t pa = tmem + PL::T_A + (k / 64) * 64 + (k % 64) / 2;
-                            mma_bf16_ts(tmem + PL::T_NUM, pa,
-                                        sw128_desc(va + (k / 8) * 1024, kC * 128, 1024), id_qs, 1u);
-                            mma_bf16_ts(tmem + PL::T_DEN, pa, sw32_desc(ones + (k / 8) * 256, 256, 256),
-                                        id_q16, 1u);
+                        for (int kk = 0; kk < kC; kk += 16) {
+                            const uint32_t pa = tmem + PL::T_P + kk / 2;
+                            mma_bf16_ts(rnum, pa, sw128_desc(va + (kk / 8) * 1024, kC * 128, 1024), id_qs, 1u);
+                            mma_bf16_ts(rden, pa, sw32_desc(ones + (kk / 8) * 256, 256, 256), id_q16, 1u);
                         }
                     }
                     mma_commit(num_full);
-                    mma_commit(&v_empty[st]);
+                    nq++;
                     nkv++;
-                    nchunk++;
+                    ndone++;
                 }
             }
             mma_commit(drain);   // every MMA issued above has completed
@@ -488,16 +526,14 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     } else if (warp >= kTmemWarps) {
         // ----------------------------------------------------- phi warps
         const int qd = warp - kTmemWarps;      // lane quadrant
-        const int r = qd * 32 + lane;          // tile row = TMEM lane
-        const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+        const int r = qd * 32 + lane;          // tile row
         constexpr int JR = DP / 8;             // 16 B chunks per row
-        uint32_t nkv = 0, nq = 0, nchunk = 0;
-        // phi in place on the row of a K tile; all loads issued before any math
-        auto phi_k = [&](int c_abs) {
-            const int st = nkv % NS;
-            wait_bar(&k_full[st], (nkv / NS) & 1, ctl);
-            const bool zero = r >= g.N - c_abs * kC;   // rows past the sequence end add nothing
-            const uint32_t t = base + PL::K0 + st * PL::QB;
+        uint32_t nk = 0;
+        // phi in place on row r of a ring tile; all loads issued before any math
+        auto phi_tile = [&](uint64_t *full, uint64_t *ready, uint32_t ring, uint32_t &n, bool zero) {
+            const int st = n % NS;
+            wait_bar(&full[st], (n / NS) & 1, ctl);
+            const uint32_t t = ring + st * PL::QB;
 #pragma unroll
             for (int h8 = 0; h8 < JR; h8 += 8) {
                 uint4 x[8];
@@ -509,41 +545,8 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&k_ready[st]);
-            nkv++;
-        };
-        // phi(Q) of the chunk -> TMEM (A operand of MMA1 / MMA3), 64 values per step
-        auto phi_q = [&]() {
-            const int qs = nq % NQ;
-            wait_bar(&q_full[qs], (nq / NQ) & 1, ctl);
-            const uint32_t t = base + PL::Q0 + qs * PL::QB;
-            uint4 x[JR];
-#pragma unroll
-            for (int j = 0; j < JR; j++) x[j] = lds128(t + tile_off(r, j));
-            if (nchunk > 0) wait_bar(tq_free, (nchunk - 1) & 1, ctl);
-            tc_fence_after();
-#pragma unroll
-            for (int b = 0; b < DP / 64; b++) {
-                uint32_t w[32];
-#pragma unroll
-                for (int jj = 0; jj < 8; jj++) {
-                    const uint4 y = phi_elu1_bf16x8(x[8 * b + jj]);
-                    w[4 * jj] = y.x;
-                    w[4 * jj + 1] = y.y;
-                    w[4 * jj + 2] = y.z;
-                    w[4 * jj + 3] = y.w;
-                }
-                tmem_st32_nowait(tmem + lane_base + PL::T_Q + 32 * b, w);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&q_empty[qs]);
-                mbar_arrive(tq_full);
-            }
-            nq++;
-            nchunk++;
+            if (lane == 0) mbar_arrive(&ready[st]);
+            n++;
         };
         for (int it = 0;; it++) {
             const int slot = it & 1;
@@ -554,15 +557,9 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             if (item < 0) break;
             const int s = item / g.BH;
             const int c0 = s * g.L, nc = min(g.L, g.NC - c0);
-            if (s + 1 < g.nseg)
-                for (int c = 0; c < nc; c++) phi_k(c0 + c);
-            // phi(K) only needs its TMA load, so it runs one chunk ahead; phi(Q)
-            // also waits for the previous chunk's Q-side products (tq_free)
-            if (nc > 0) phi_k(c0);
-            for (int c = 0; c < nc; c++) {
-                phi_q();
-                if (c + 1 < nc) phi_k(c0 + c + 1);
-            }
+            // rows past the sequence end must add nothing to S, z
+            for (int c = 0; c < nc; c++)
+                phi_tile(k_full, k_ready, base + PL::K0, nk, r >= g.N - (c0 + c) * kC);
         }
     } else {
         // ----------------------------------------------------- TMEM warps
@@ -570,8 +567,99 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const int r = qd * 32 + lane;
         const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
         const bool srow = qd * 32 < DP;   // warp-uniform: this warp's rows hold state rows
+        const int piece = NSP == 1 ? 0 : qd / 2;   // S_prev piece of this warp's rows
+        // Warps of the second S_prev piece write it only once MMA3 has read the
+        // first, and MMA3(c+1) also needs the epilogue of c: so they write
+        // their piece for chunk c + 1 after that epilogue.
+        const bool late = NSP == 2 && piece == 1;
+        const int prow = r - piece * PR;           // row inside the piece
         const uint32_t s_addr = base + PL::S0, zp_addr = base + PL::Z0;
-        uint32_t nchunk = 0, nA = 0, nchain = 0, npub = 0;
+        uint32_t kg = 0;      // global index of the next chunk whose A is read
+        uint32_t nvr = 0;     // V ring position (phase A and C tiles)
+        uint32_t nsp = 0;     // S_prev copies made (one per chunk)
+        uint32_t nsd = 0;     // s_done phases consumed
+
+        // S_prev piece + ZP rows <- the state in T_S, T_Z; arrives sp_ready.
+        auto sprev_from_tmem = [&]() {
+            if (NSP == 2 && piece == 1) {   // the buffer holds piece 0 until MMA3 has read it
+                wait_bar(sp_free, nsp & 1, ctl);
+            }
+            tc_fence_after();
+            if (srow) {
+#pragma unroll
+                for (int cb = 0; cb < HALF; cb += 32) {
+                    uint32_t v[32];
+                    tmem_ld32_nowait(tmem + lane_base + PL::T_S + grp * HALF + cb, v);
+                    tmem_ld_wait();
+                    sprev_store32<PR>(s_addr, prow, grp * HALF + cb, v);
+                }
+                if (grp == 0) {
+                    uint32_t zv[16];
+                    tmem_ld16_nowait(tmem + lane_base + PL::T_Z, zv);
+                    tmem_ld_wait();
+                    zp_store(zp_addr, r, __uint_as_float(zv[0]));
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0 && (NSP == 1 || srow)) mbar_arrive(&sp_ready[piece]);
+            nsp++;
+        };
+        // phi(Q) in place on this thread's half row of the next Q tile
+        uint32_t nqt = 0;
+        auto phi_q = [&]() {
+            const int st = nqt % NS;
+            wait_bar(&q_full[st], (nqt / NS) & 1, ctl);
+            const uint32_t t = base + PL::Q0 + st * PL::QB;
+            constexpr int JH = DP / 16;   // 16 B chunks per half row
+            uint4 x[JH];
+#pragma unroll
+            for (int j = 0; j < JH; j++) x[j] = lds128(t + tile_off(r, grp * JH + j));
+#pragma unroll
+            for (int j = 0; j < JH; j++) sts128(t + tile_off(r, grp * JH + j), phi_elu1_bf16x8(x[j]));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&q_ready[st]);
+            nqt++;
+        };
+        // A(kg) from its region -> registers (masked, packed bf16 P), then a_free
+        auto load_p = [&](uint32_t (&pk)[32]) {
+            wait_bar(a_full, kg & 1, ctl);
+            tc_fence_after();
+            const uint32_t ra = tmem + lane_base + PL::T_R0 + (kg & 1) * 128 + grp * 64;
+            uint32_t a0[32], a1[32];
+            tmem_ld32_nowait(ra, a0);
+            tmem_ld32_nowait(ra + 32, a1);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(a_free);
+            const int cbase = grp * 64;
+#pragma unroll
+            for (int i = 0; i < 16; i++) {
+                const int col = cbase + 2 * i;
+                pk[i] = pack_bf16x2(col <= r ? __uint_as_float(a0[2 * i]) : 0.f,
+                                    col + 1 <= r ? __uint_as_float(a0[2 * i + 1]) : 0.f);
+                pk[16 + i] = pack_bf16x2(col + 32 <= r ? __uint_as_float(a1[2 * i]) : 0.f,
+                                         col + 33 <= r ? __uint_as_float(a1[2 * i + 1]) : 0.f);
+            }
+            kg++;
+        };
+        // P -> its TMEM slot (keys [64 grp, 64 grp + 64) -> columns [32 grp, 32 grp + 32))
+        auto store_p = [&](const uint32_t (&pk)[32]) {
+            tmem_st32_nowait(tmem + lane_base + PL::T_P + grp * 32, pk);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_ready);
+        };
+        auto wait_sdone = [&]() {
+            const bool ok = __all_sync(0xffffffffu, wait_bar(s_done, nsd & 1, ctl));
+            nsd++;
+            return ok;
+        };
+
         for (int it = 0;; it++) {
             const int slot = it & 1;
             if (!wait_bar(&item_full[slot], (it >> 1) & 1, ctl)) break;
@@ -581,169 +669,110 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             if (item < 0) break;
             const int s = item / g.BH, h = item % g.BH;
             const int c0 = s * g.L, nc = min(g.L, g.NC - c0);
-            const bool hasA = s + 1 < g.nseg;
-            const long long pub = (long long)h * g.nseg + s;   // this item's state slot
-
-            // ---- phase B: predecessor's state in, own inclusive state out
-            if (hasA) {
-                wait_bar(sloc_done, nA & 1, ctl);
-                nA++;
+            const long long slot_id = (long long)h * g.nseg + s;   // this (head, segment) in scratch
+            if constexpr (AGG) {
+                // the segment's sums (region it % 2 and its denominator slot) -> scratch
+                const int rr = it & 1;
+                wait_bar(sloc_done, it & 1, ctl);
                 tc_fence_after();
-            }
-            if (s > 0) {   // one thread polls the predecessor's flag, the rest wait on chain_ok
-                if (threadIdx.x == 0) {
-                    const int *f = sc.flags + (pub - 1);
-                    const long long t0 = clock64();
-                    while (!*abort_cta && ld_acquire_gpu(f) == 0) {
-                        if (*ctl.glob) {
-                            *abort_cta = 1;
-                            break;
-                        }
-                        if (clock64() - t0 > kWaitBudget) {
-                            raise_abort(ctl);
-                            break;
-                        }
-                        __nanosleep(64);
+                if (srow) {
+                    float4 *dst = reinterpret_cast<float4 *>(sc.preS + slot_id * DP * DV + (long long)r * DV +
+                                                             grp * HALF);
+#pragma unroll
+                    for (int cb = 0; cb < HALF; cb += 32) {
+                        uint32_t l[32];
+                        tmem_ld32_nowait(tmem + lane_base + PL::T_R0 + rr * 128 + grp * HALF + cb, l);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 8; i++)
+                            __stcg(dst + cb / 4 + i,
+                                   make_float4(__uint_as_float(l[4 * i]), __uint_as_float(l[4 * i + 1]),
+                                               __uint_as_float(l[4 * i + 2]), __uint_as_float(l[4 * i + 3])));
                     }
-                    mbar_arrive(chain_ok);
+                    if (grp == 0) {
+                        uint32_t d[16];
+                        tmem_ld16_nowait(tmem + lane_base + PL::T_DEN0 + rr * 16, d);
+                        tmem_ld_wait();
+                        __stcg(sc.prez + slot_id * DP + r, __uint_as_float(d[0]));
+                    }
                 }
-                wait_bar(chain_ok, nchain & 1, ctl);
-                nchain++;
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sloc_read[rr]);
+                continue;
             }
-            float zprev = 0.f;
+            const uint32_t G = kg;   // global index of chunk 0
+
+            phi_q();   // phi(Q) of chunk 0 first: MMA1 of chunk 0 does not wait for phase B
+
+            // ---- phase B: the state before this segment (the exclusive prefix of
+            // the head's earlier segments; zero for the first) -> T_S, T_Z
             if (srow) {
-                const float *prevS = s > 0 ? sc.inclS + (pub - 1) * DP * DV + (long long)r * DV : nullptr;
+                const float4 *src = reinterpret_cast<const float4 *>(sc.preS + slot_id * DP * DV +
+                                                                     (long long)r * DV + grp * HALF);
 #pragma unroll
                 for (int cb = 0; cb < HALF; cb += 32) {
-                    const int col = grp * HALF + cb;
                     uint32_t v[32];
 #pragma unroll
-                    for (int i = 0; i < 32; i += 4) {
-                        const float4 x = prevS ? __ldcg(reinterpret_cast<const float4 *>(prevS + col + i))
-                                               : make_float4(0.f, 0.f, 0.f, 0.f);
-                        v[i] = __float_as_uint(x.x);
-                        v[i + 1] = __float_as_uint(x.y);
-                        v[i + 2] = __float_as_uint(x.z);
-                        v[i + 3] = __float_as_uint(x.w);
+                    for (int i = 0; i < 8; i++) {
+                        const float4 pv = s > 0 ? __ldcg(src + cb / 4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        v[4 * i] = __float_as_uint(pv.x);
+                        v[4 * i + 1] = __float_as_uint(pv.y);
+                        v[4 * i + 2] = __float_as_uint(pv.z);
+                        v[4 * i + 3] = __float_as_uint(pv.w);
                     }
-                    if (hasA) {   // publish prev + S_loc
-                        uint32_t l[32];
-                        tmem_ld32_nowait(tmem + lane_base + PL::T_NUM + col, l);
-                        tmem_ld_wait();
-                        float *dst = sc.inclS + pub * DP * DV + (long long)r * DV + col;
-#pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            __stcg(reinterpret_cast<float4 *>(dst + i),
-                                   make_float4(__uint_as_float(v[i]) + __uint_as_float(l[i]),
-                                               __uint_as_float(v[i + 1]) + __uint_as_float(l[i + 1]),
-                                               __uint_as_float(v[i + 2]) + __uint_as_float(l[i + 2]),
-                                               __uint_as_float(v[i + 3]) + __uint_as_float(l[i + 3])));
-                    }
-                    tmem_st32_nowait(tmem + lane_base + PL::T_S + col, v);
-                    sprev_store32<DP>(s_addr, r, col, v);
+                    tmem_st32_nowait(tmem + lane_base + PL::T_S + grp * HALF + cb, v);
                 }
-                zprev = s > 0 ? __ldcg(sc.inclz + (pub - 1) * DP + r) : 0.f;
                 if (grp == 0) {
-                    if (hasA) {
-                        uint32_t d[16];
-                        tmem_ld16_nowait(tmem + lane_base + PL::T_DEN, d);
-                        tmem_ld_wait();
-                        __stcg(sc.inclz + pub * DP + r, zprev + __uint_as_float(d[0]));
-                    }
+                    const float zprev = s > 0 ? __ldcg(sc.prez + slot_id * DP + r) : 0.f;
                     uint32_t zw[16];
 #pragma unroll
                     for (int i = 0; i < 16; i++) zw[i] = i < 8 ? __float_as_uint(zprev) : 0u;
                     tmem_st16_nowait(tmem + lane_base + PL::T_Z, zw);
-                    zp_store(zp_addr, r, zprev);
                 }
-            }
-            if (hasA) {   // every writer fences, then one thread raises the flag
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(pub_ready);
-                if (threadIdx.x == 0 && wait_bar(pub_ready, npub & 1, ctl)) {
-                    __threadfence();
-                    st_release_gpu(sc.flags + pub, 1);
-                }
-                npub++;
             }
             tmem_st_wait();
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(sprev_ready);
+            if (!late) sprev_from_tmem();   // S_prev, ZP for chunk 0, read back from T_S, T_Z
 
-            // ---- phase C: the chunk recurrence.  Per chunk: P(c); then the
-            // state copy for chunk c + 1 (needs only MMA4(c), which finishes
-            // before MMA2(c)); then the epilogue of chunk c.
-            for (int c = 0; c < nc; c++, nchunk++) {
+            // ---- phase C.  Prologue: P(G).  Then per chunk k = G + c, in the
+            // order the tensor pipe completes their inputs: phi(Q(k+1)); S_prev
+            // for k + 1 (after MMA4(k)); A(k+1) -> registers (after MMA1(k+1));
+            // P(k+1) and the epilogue of k (after MMA2(k)).
+            uint32_t pk[32];
+            load_p(pk);
+            store_p(pk);   // the P slot is free: the last MMA2 has completed
+            if (late) sprev_from_tmem();
+            for (int c = 0; c < nc; c++) {
+                const uint32_t k = G + c;
                 const int row0 = (c0 + c) * kC;
-                // P = bf16(tril(A)): columns [64 grp, 64 grp + 64) of A -> the
-                // first 32 columns of the same region
-                wait_bar(a_full, nchunk & 1, ctl);
-                tc_fence_after();
-                {
-                    uint32_t a0[32], a1[32], pk[32];
-                    tmem_ld32_nowait(tmem + lane_base + PL::T_A + grp * 64, a0);
-                    tmem_ld32_nowait(tmem + lane_base + PL::T_A + grp * 64 + 32, a1);
-                    tmem_ld_wait();
-                    const int cbase = grp * 64;
-#pragma unroll
-                    for (int i = 0; i < 16; i++) {
-                        const int col = cbase + 2 * i;
-                        pk[i] = pack_bf16x2(col <= r ? __uint_as_float(a0[2 * i]) : 0.f,
-                                            col + 1 <= r ? __uint_as_float(a0[2 * i + 1]) : 0.f);
-                        pk[16 + i] = pack_bf16x2(col + 32 <= r ? __uint_as_float(a1[2 * i]) : 0.f,
-                                                 col + 33 <= r ? __uint_as_float(a1[2 * i + 1]) : 0.f);
-                    }
-                    tmem_st32_nowait(tmem + lane_base + PL::T_A + grp * 64, pk);
-                    tmem_st_wait();
+                const bool more = c + 1 < nc;
+                bool sd = true;
+                if (more) {
+                    phi_q();
+                    wait_sdone();
+                    if (!late) sprev_from_tmem();
+                    load_p(pk);
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(p_ready);
-                if (c + 1 < nc) {   // S_prev, ZP <- state after this chunk
-                    wait_bar(s_done, nchunk & 1, ctl);
-                    tc_fence_after();
-                    if (srow) {
-#pragma unroll
-                        for (int cb = 0; cb < HALF; cb += 32) {
-                            uint32_t v[32];
-                            tmem_ld32_nowait(tmem + lane_base + PL::T_S + grp * HALF + cb, v);
-                            tmem_ld_wait();
-                            sprev_store32<DP>(s_addr, r, grp * HALF + cb, v);
-                        }
-                        if (grp == 0) {
-                            uint32_t zv[16];
-                            tmem_ld16_nowait(tmem + lane_base + PL::T_Z, zv);
-                            tmem_ld_wait();
-                            zp_store(zp_addr, r, __uint_as_float(zv[0]));
-                        }
-                    }
-                    fence_proxy_async_smem();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(sprev_ready);
-                }
-                // out = NUM / (DEN[0] + DEN[8])
-                const bool ok = wait_bar(num_full, nchunk & 1, ctl);
+                const bool ok = __all_sync(0xffffffffu, wait_bar(num_full, k & 1, ctl));
+                if (more) store_p(pk);
                 tc_fence_after();
+                const uint32_t rn = tmem + lane_base + PL::T_R0 + (k & 1) * 128 + grp * HALF;
                 uint32_t d[16], n0[32], n1[32];
-                tmem_ld16_nowait(tmem + lane_base + PL::T_DEN, d);
-                tmem_ld32_nowait(tmem + lane_base + PL::T_NUM + grp * HALF, n0);
-                if constexpr (HALF == 64) tmem_ld32_nowait(tmem + lane_base + PL::T_NUM + grp * HALF + 32, n1);
+                tmem_ld16_nowait(tmem + lane_base + PL::T_DEN0 + (k & 1) * 16, d);
+                tmem_ld32_nowait(rn, n0);
+                if constexpr (HALF == 64) tmem_ld32_nowait(rn + 32, n1);
                 tmem_ld_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(num_free);
-                if (ok && r < g.N - row0) {
+                if (lane == 0) mbar_arrive(&num_free[k & 1]);
+                {   // out(k) = NUM / (DEN[0] + DEN[8]) -> the V slot of chunk k (bf16, swizzled)
+                    const int vs = nvr % NS;
                     const float inv = 1.f / (__uint_as_float(d[0]) + __uint_as_float(d[8]));
-                    uint4 *orow = reinterpret_cast<uint4 *>(
-                        out + ((long long)h * g.N + row0 + r) * DV + grp * HALF);
+                    const uint32_t vt = base + PL::V0 + vs * PL::VB + (grp * HALF / 64) * (kC * 128);
                     auto put = [&](const uint32_t(&v)[32], int j0) {
 #pragma unroll
                         for (int j = 0; j < 4; j++)
-                            __stcs(orow + j0 + j,
+                            sts128(vt + sw128_off(r, j0 + j),
                                    make_uint4(pack_bf16x2(__uint_as_float(v[8 * j]) * inv,
                                                           __uint_as_float(v[8 * j + 1]) * inv),
                                               pack_bf16x2(__uint_as_float(v[8 * j + 2]) * inv,
@@ -753,35 +782,43 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                               pack_bf16x2(__uint_as_float(v[8 * j + 6]) * inv,
                                                           __uint_as_float(v[8 * j + 7]) * inv)));
                     };
-                    put(n0, 0);
+                    // HALF = 64: this warp's half is one whole 64-column block;
+                    // HALF = 32: half a block, starting at chunk 4 * (grp % 2)
+                    put(n0, HALF == 64 ? 0 : 4 * grp);
                     if constexpr (HALF == 64) put(n1, 4);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&out_ready[vs]);
+                    nvr++;
                 }
-            }
-            // the last chunk's state update; export after the head's last segment
-            // (tcgen05.ld is warp-collective: the condition must be warp-uniform)
-            const bool fin = __all_sync(0xffffffffu, wait_bar(s_done, (nchunk - 1) & 1, ctl));
-            if (fin && s == g.nseg - 1 && srow && (S_out || z_out)) {
-                tc_fence_after();
+                (void)ok;
+                (void)row0;
+                if (!more) sd = wait_sdone();   // the last chunk's state update
+                // the head's final state after its last chunk
+                if (!more && sd && s == g.nseg - 1 && srow && (S_out || z_out)) {
+                    tc_fence_after();
 #pragma unroll
-                for (int cb = 0; cb < HALF; cb += 32) {
-                    uint32_t v[32];
-                    tmem_ld32_nowait(tmem + lane_base + PL::T_S + grp * HALF + cb, v);
-                    tmem_ld_wait();
-                    if (S_out) {
-                        float *dst = S_out + ((long long)h * DP + r) * DV + grp * HALF + cb;
+                    for (int cb = 0; cb < HALF; cb += 32) {
+                        uint32_t v[32];
+                        tmem_ld32_nowait(tmem + lane_base + PL::T_S + grp * HALF + cb, v);
+                        tmem_ld_wait();
+                        if (S_out) {
+                            float *dst = S_out + ((long long)h * DP + r) * DV + grp * HALF + cb;
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            *reinterpret_cast<float4 *>(dst + i) =
-                                make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                                            __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+                            for (int i = 0; i < 32; i += 4)
+                                *reinterpret_cast<float4 *>(dst + i) =
+                                    make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                                __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+                        }
+                    }
+                    if (z_out && grp == 0) {
+                        uint32_t zv[16];
+                        tmem_ld16_nowait(tmem + lane_base + PL::T_Z, zv);
+                        tmem_ld_wait();
+                        z_out[(long long)h * DP + r] = __uint_as_float(zv[0]);
                     }
                 }
-                if (z_out && grp == 0) {
-                    uint32_t zv[16];
-                    tmem_ld16_nowait(tmem + lane_base + PL::T_Z, zv);
-                    tmem_ld_wait();
-                    z_out[(long long)h * DP + r] = __uint_as_float(zv[0]);
-                }
+                if (more && late) sprev_from_tmem();
             }
             tc_fence_before();
         }
@@ -842,46 +879,59 @@ int num_sms()
 // Segment length L (chunks): the estimated makespan, in chunk-times, is
 // waves * (L + [segmented] (L / 2 + 1)): phase C costs one chunk-time per
 // chunk, phase A half of that (k, v only), and the chain about one more.
+// Segments per head: enough items to give every SM one (one wave), and no
+// segmentation once B*H alone fills the GPU.
 Geo plan(long long BH, int N, int sms)
 {
     Geo g;
     g.BH = (int)BH;
     g.N = N;
     g.NC = cdiv(N, kC);
-    int bestL = g.NC;   // one segment per head
-    if (BH < sms) {
-        double best = (double)((BH + sms - 1) / sms) * g.NC;
-        for (int L = 1; L <= min(g.NC - 1, kMaxItemChunks); L++) {
-            const int nseg = cdiv(g.NC, L);
-            const long long waves = (BH * nseg + sms - 1) / sms;
-            const double cost = (double)waves * (1.5 * L + 1.0);
-            if (cost <= best) {
-                best = cost;
-                bestL = L;
-            }
-        }
-    }
-    g.L = bestL;
+    const int want = BH >= sms ? 1 : (int)(sms / BH);
+    g.L = cdiv(g.NC, max(1, min(want, g.NC)));
     g.nseg = cdiv(g.NC, g.L);
     g.n_items = (int)(BH * g.nseg);
     return g;
 }
 
-struct ScratchLayout {
-    size_t flags, inclz, inclS, total, clear;
-};
+// Exclusive prefix over a head's segments of the segment sums, in place:
+// afterwards slot (h, s) holds the sums over segments 0 .. s-1 (zero for
+// s = 0).  The last segment's own sums are never computed or read.
+__global__ void seg_scan_kernel(float *__restrict__ preS, float *__restrict__ prez, int nseg, int szS,
+                                int szz)
+{
+    const long long head = blockIdx.y;
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    float *p;
+    int stride;
+    if (e < szS) {
+        p = preS + head * nseg * (long long)szS + e;
+        stride = szS;
+    } else if (e < szS + szz) {
+        p = prez + head * nseg * (long long)szz + (e - szS);
+        stride = szz;
+    } else {
+        return;
+    }
+    float run = 0.f;
+    for (int s0 = 0; s0 < nseg; s0 += 8) {
+        float x[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) x[i] = s0 + i < nseg - 1 ? p[(long long)(s0 + i) * stride] : 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; i++)
+            if (s0 + i < nseg) {
+                p[(long long)(s0 + i) * stride] = run;
+                run += x[i];
+            }
+    }
+}
 
 template <int DP, int DV>
-ScratchLayout scratch_layout(const Geo &g)
+size_t scratch_bytes(const Geo &g)
 {
-    ScratchLayout L;
-    const size_t n = (size_t)g.n_items;
-    L.flags = 16;
-    L.clear = L.flags + ((n * 4 + 15) & ~(size_t)15);
-    L.inclz = L.clear;
-    L.inclS = L.inclz + ((n * DP * 4 + 15) & ~(size_t)15);
-    L.total = g.nseg > 1 ? L.inclS + n * DP * DV * 4 : L.clear;
-    return L;
+    // ticket, abort word; then the segment sums / prefixes when segmented
+    return 16 + (g.nseg > 1 ? (size_t)g.BH * g.nseg * ((size_t)DP * DV + DP) * sizeof(float) : 0);
 }
 
 template <int DP, int DV>
@@ -889,31 +939,47 @@ cudaError_t run(const Problem &p, void *scratch, float *S_out, float *z_out, int
                 cudaStream_t s)
 {
     using PL = Plan<DP, DV>;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if (!make_map(&tq, p.q, p.BH, p.N, p.D) || !make_map(&tk, p.k, p.BH, p.N, p.D) ||
-        !make_map(&tv, p.v, p.BH, p.N, p.Dv))
+        !make_map(&tv, p.v, p.BH, p.N, p.Dv) || !make_map(&to, p.out, p.BH, p.N, p.Dv))
         return cudaErrorInvalidValue;
     const int sms = num_sms();
     Geo g = plan(p.BH, p.N, sms);
-    ScratchLayout L = scratch_layout<DP, DV>(g);
     unsigned char *b = (unsigned char *)scratch;
     Scratch sc;
     sc.ticket = (int *)b;
     sc.abort = (int *)(b + 4);
-    sc.flags = (int *)(b + L.flags);
-    sc.inclz = (float *)(b + L.inclz);
-    sc.inclS = (float *)(b + L.inclS);
+    sc.preS = (float *)(b + 16);
+    sc.prez = sc.preS + (size_t)g.BH * g.nseg * DP * DV;
     cudaError_t e;
-    if ((e = cudaMemsetAsync(scratch, 0, L.clear, s)) != cudaSuccess) return e;
-    if ((e = cudaFuncSetAttribute(tc_causal_kernel<DP, DV>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, PL::SMEM)) !=
-        cudaSuccess)
+    int launches = 0;
+    if ((e = cudaMemsetAsync(scratch, 0, 16, s)) != cudaSuccess) return e;
+    if (g.nseg > 1) {
+        // pass 1: the sums of every segment but the last of each head; then the scan
+        Geo ga = g;
+        ga.n_items = g.BH * (g.nseg - 1);
+        if ((e = cudaFuncSetAttribute(tc_causal_kernel<DP, DV, true>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, PL::SMEM)) !=
+            cudaSuccess)
+            return e;
+        tc_causal_kernel<DP, DV, true><<<min(ga.n_items, sms), kThreads, PL::SMEM, s>>>(
+            tq, tk, tv, to, ga, sc, (__nv_bfloat16 *)p.out, nullptr, nullptr, err);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        const int sz = DP * DV + DP;
+        seg_scan_kernel<<<dim3(cdiv(sz, 256), (unsigned)g.BH), 256, 0, s>>>(sc.preS, sc.prez, g.nseg,
+                                                                           DP * DV, DP);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = cudaMemsetAsync(scratch, 0, 4, s)) != cudaSuccess) return e;   // ticket
+        launches += 2;
+    }
+    // pass 2: the chunk recurrence of every segment from its prefix
+    if ((e = cudaFuncSetAttribute(tc_causal_kernel<DP, DV, false>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, PL::SMEM)) != cudaSuccess)
         return e;
-    const int grid = min(g.n_items, sms);
-    tc_causal_kernel<DP, DV><<<grid, kThreads, PL::SMEM, s>>>(tq, tk, tv, g, sc,
-                                                              (__nv_bfloat16 *)p.out, S_out, z_out, err);
+    tc_causal_kernel<DP, DV, false><<<min(g.n_items, sms), kThreads, PL::SMEM, s>>>(
+        tq, tk, tv, to, g, sc, (__nv_bfloat16 *)p.out, S_out, z_out, err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    note_launches(1);
+    note_launches(launches + 1);
     return cudaSuccess;
 }
 
@@ -928,10 +994,10 @@ bool tc_causal_supported(const Problem &p)
 size_t tc_causal_scratch_bytes(const Problem &p)
 {
     Geo g = plan(p.BH, p.N, num_sms());
-    if (p.D == 64 && p.Dv == 64) return scratch_layout<64, 64>(g).total;
-    if (p.D == 64 && p.Dv == 128) return scratch_layout<64, 128>(g).total;
-    if (p.D == 128 && p.Dv == 64) return scratch_layout<128, 64>(g).total;
-    return scratch_layout<128, 128>(g).total;
+    if (p.D == 64 && p.Dv == 64) return scratch_bytes<64, 64>(g);
+    if (p.D == 64 && p.Dv == 128) return scratch_bytes<64, 128>(g);
+    if (p.D == 128 && p.Dv == 64) return scratch_bytes<128, 64>(g);
+    return scratch_bytes<128, 128>(g);
 }
 
 cudaError_t tc_causal(const Problem &p, void *scratch, float *S_out, float *z_out, int *err,

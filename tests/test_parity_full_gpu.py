@@ -100,17 +100,18 @@ def test_segment_plan_matches_single_segment(la):
     assert e <= 2e-2, e
 
 
-def test_causal_forward_is_one_launch(la):
-    """The causal forward is one kernel launch whatever the segment plan:
-    the tensor-core kernel (bf16 elu+1, D and Dv in {64, 128}) chains its
-    segments inside the launch, and the CUDA-core kernel walks whole heads."""
-    for D in (128, 32):
-        w = wl.small(B=1, H=2, N=2048, D=D, Dv=D, seed=5)
+def test_causal_launch_plan(la):
+    """bf16 elu+1 with D, Dv in {64, 128} runs the tensor-core kernels: with
+    few heads (segments) that is the segment-sum pass, the scan and the
+    output pass (three kernels); with one segment per head only the output
+    pass.  Other shapes run the CUDA-core kernel (one launch)."""
+    for (B, H, D, expect) in ((1, 2, 128, 3), (1, 160, 64, 1), (1, 2, 32, 1)):
+        w = wl.small(B=B, H=H, N=1024 if H > 100 else 2048, D=D, Dv=D, seed=5)
         q, k, v = (t.cuda() for t in wl.make_qkv(w))
         n0 = la.la_launch_count()
         la.la_forward(q, k, v, causal=True)
         torch.cuda.synchronize()
-        assert la.la_launch_count() - n0 == 1
+        assert la.la_launch_count() - n0 == expect, (B, H, D)
 
 
 @pytest.mark.parametrize("H,N,D,Dv", [(3, 128 * 37 + 5, 128, 128), (2, 128 * 21 + 77, 64, 128),
