@@ -75,3 +75,21 @@ def test_pins_reject_planted_mistake(name, tmp_path):
         except (AssertionError, FloatingPointError, ValueError, ZeroDivisionError):
             caught.append(pin.__name__)
     assert caught, f"no pin rejects the planted mistake {name}"
+
+
+def test_oracle_matches_exact_rational_fixture(oracle_lib):
+    """The oracle against tests/golden/exact_elu1_causal.json: exact rational
+    outputs of the causal form on positive integer inputs (phi(x) = x + 1
+    there), written by tests/golden/make_exact_elu1.py without the oracle."""
+    import json
+    from fractions import Fraction
+
+    import numpy as np
+
+    doc = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "exact_elu1_causal.json")))
+    q = np.array(doc["q"], dtype=np.float64)[None]
+    k = np.array(doc["k"], dtype=np.float64)[None]
+    v = np.array(doc["v"], dtype=np.float64)[None]
+    got = oracle.forward(q, k, v, causal=True, lib=oracle_lib)[0]
+    want = np.array([[[float(Fraction(x)) for x in row] for row in head] for head in doc["out"]])
+    assert np.max(np.abs(got - want)) <= 1e-13 * np.max(np.abs(want))
