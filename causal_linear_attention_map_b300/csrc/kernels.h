@@ -38,6 +38,13 @@ size_t tc_causal_scratch_bytes(const Problem &p);
 cudaError_t tc_causal(const Problem &p, void *scratch, float *S_out, float *z_out, int *err,
                       cudaStream_t s);
 
+// Tensor-core non-causal forward (same shapes as tc_causal_supported): the
+// segment sums of tc_causal's first pass over every segment, their total per
+// head, then the readout.  Scratch: 16 B + B*H*nseg*(Dphi*Dv + Dphi)*4.
+size_t tc_noncausal_scratch_bytes(const Problem &p);
+cudaError_t tc_noncausal(const Problem &p, void *scratch, float *S_out, float *z_out, int *err,
+                         cudaStream_t s);
+
 // Non-causal: KV = phi(K)^T V and ksum = sum phi(k) reduced over N into
 // fp32 scratch (KV [BH, P, Dv], ksum [BH, P]; zeroed here), then the readout.
 size_t noncausal_scratch_bytes(const Problem &p);

@@ -155,11 +155,13 @@ int forward_impl(const void *q, const void *k, const void *v, void *out, int B, 
         return cuda_status(e != cudaSuccess ? e : e2);
     }
 
-    size_t bytes = la::noncausal_scratch_bytes(p);
+    const bool tc = la::tc_causal_supported(p);   // same shapes for both forms
+    size_t bytes = tc ? la::tc_noncausal_scratch_bytes(p) : la::noncausal_scratch_bytes(p);
     void *scratch = nullptr;
     if (cudaMallocFromPoolAsync(&scratch, bytes, ctx->pool, s) != cudaSuccess)
         return cuda_status(cudaErrorMemoryAllocation);
-    cudaError_t e = la::noncausal(p, scratch, S_out, z_out, s);
+    cudaError_t e = tc ? la::tc_noncausal(p, scratch, S_out, z_out, ctx->err_word, s)
+                       : la::noncausal(p, scratch, S_out, z_out, s);
     cudaError_t e2 = cudaFreeAsync(scratch, s);
     return cuda_status(e != cudaSuccess ? e : e2);
 }

@@ -831,6 +831,338 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
 }
 
+// ------------------------------------------------ non-causal readout kernel
+//
+// The non-causal form (review page "Transformers are RNNs", proposed method
+// b2: by associativity phi(K)^T V is formed once and reused by every query):
+// the segment-sum form of the kernel above, run over every segment, gives the
+// per-segment sums; nc_total_kernel adds them into S = phi(K)^T V and
+// z = colsum phi(K) per head; this kernel reads them out for every query,
+//   out = (phi(Q) S) / (phi(Q) z),
+// one tcgen05 product per 128-position chunk (NUM = phiQ . S, DEN = phiQ . ZP)
+// into one of two TMEM regions that alternate between chunks.
+// Roles (10 warps): 8 math warps (phi(Q) in place; S, ZP per item; the
+// epilogue), one producer warp (lane 0: Q tiles and items; lane 1: TMA stores
+// of the output tiles from a staging ring), one MMA warp.
+
+constexpr int kNcMath = 8;
+constexpr int kNcProducer = kNcMath;          // warp 8
+constexpr int kNcMma = kNcMath + 1;           // warp 9
+constexpr int kNcThreads = (kNcMma + 1) * 32; // 320
+constexpr int kNcItemConsumers = kNcMath + 2; // math warps, MMA thread, store lane
+
+template <int DP, int DV>
+struct NcPlan {
+    static constexpr int QB = kC * DP * 2;
+    static constexpr int OB = kC * DV * 2;
+    static constexpr int SB = DP * DV * 2;
+    static constexpr int ZB = DP * 32;
+    static constexpr int NO = 2;
+    static constexpr int kBudget = 227 * 1024 - 2048;
+    static constexpr int NQ0 = (kBudget - NO * OB - SB - ZB) / QB;
+    static constexpr int NQ = NQ0 > 6 ? 6 : NQ0;   // Q ring depth: what fits, at most 6
+    static_assert(NQ >= 2, "Q ring too shallow");
+    static constexpr int Q0 = 0;
+    static constexpr int O0 = Q0 + NQ * QB;
+    static constexpr int S0 = O0 + NO * OB;
+    static constexpr int Z0 = S0 + SB;
+    static constexpr int TILES = Z0 + ZB;
+    static constexpr int SMEM = TILES + 1024 + 1024;
+    // TMEM: NUM of region r at column 128 r (DV columns), its DEN (16
+    // columns) at T_DEN + 16 r
+    static constexpr int T_DEN = 256;
+    static constexpr int TMEM_COLS = 512;
+    static_assert(SMEM <= 227 * 1024, "shared memory plan too large");
+    static_assert(SMEM > 114 * 1024, "one CTA per SM: the kernel holds all 512 TMEM columns");
+};
+
+template <int DP, int DV>
+__global__ void __launch_bounds__(kNcThreads, 1)
+nc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o, Geo g,
+              Scratch sc, int *err)
+{
+    using PL = NcPlan<DP, DV>;
+    constexpr int NQ = PL::NQ, NO = PL::NO;
+    constexpr int HALF = DV / 2;
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t base = align1k(smem_u32(smem_raw));
+    unsigned char *gbase = smem_raw + (base - smem_u32(smem_raw));
+    // barrier map: three Q-ring arrays of NQ, then fixed pairs and words
+    uint64_t *bar = reinterpret_cast<uint64_t *>(gbase + PL::TILES);
+    uint64_t *q_full = bar, *q_ready = bar + NQ, *q_empty = bar + 2 * NQ;
+    uint64_t *num_full = bar + 3 * NQ, *num_free = num_full + 2;   // [2] per region
+    uint64_t *out_ready = num_free + 2, *out_free = out_ready + NO;  // [NO]
+    uint64_t *item_full = out_free + NO, *item_empty = item_full + 2;
+    uint64_t *s_ready = item_empty + 2, *s_free = s_ready + 1, *drain = s_free + 1;
+    volatile int *item_slot = reinterpret_cast<volatile int *>(drain + 1);   // [2]
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(drain + 2);
+    volatile int *abort_cta = reinterpret_cast<volatile int *>(drain + 3);
+    static_assert((3 * NQ + 4 + 2 * NO + 4 + 3 + 3) * 8 <= 1024, "barrier map exceeds its 1 KB");
+    const Ctl ctl{abort_cta, sc.abort, err};
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NQ; i++) {
+            mbar_init(&q_full[i], 1);
+            mbar_init(&q_ready[i], kNcMath);
+            mbar_init(&q_empty[i], 1);
+        }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(&num_full[i], 1);
+            mbar_init(&num_free[i], kNcMath);
+            mbar_init(&item_full[i], 1);
+            mbar_init(&item_empty[i], kNcItemConsumers);
+        }
+        for (int i = 0; i < NO; i++) {
+            mbar_init(&out_ready[i], kNcMath);
+            mbar_init(&out_free[i], 1);
+        }
+        mbar_init(s_ready, kNcMath);
+        mbar_init(s_free, 1);
+        mbar_init(drain, 1);
+        *abort_cta = 0;
+        fence_mbar_init();
+    }
+    if (warp == kNcMma) tmem_alloc(tslot, PL::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    // the item sequence, published by the Q producer
+    auto next_item = [&](int it, bool producer) {
+        const int slot = it & 1;
+        if (producer) {
+            const bool ok = it < 2 || wait_bar(&item_empty[slot], ((it >> 1) - 1) & 1, ctl);
+            int item = -1;
+            if (ok && !*abort_cta) {
+                item = atomicAdd(sc.ticket, 1);
+                if (item >= g.n_items) item = -1;
+            }
+            item_slot[slot] = item;
+            mbar_arrive(&item_full[slot]);
+            return item;
+        }
+        if (!wait_bar(&item_full[slot], (it >> 1) & 1, ctl)) return -1;
+        const int item = item_slot[slot];
+        __syncwarp(__activemask());
+        return item;
+    };
+
+    if (warp == kNcProducer) {
+        if (lane == 0) {
+            // ---------------------------------------------- Q tile producer
+            prefetch_tmap(&tm_q);
+            const uint64_t stream = policy_evict_first();
+            uint32_t n = 0;
+            for (int it = 0;; it++) {
+                const int item = next_item(it, true);
+                if (item < 0) break;
+                const int s = item / g.BH, h = item % g.BH;
+                const int c0 = s * g.L, nc = min(g.L, g.NC - c0);
+                bool ok = true;
+                for (int c = 0; c < nc && ok; c++) {
+                    if (c + 1 < nc)
+                        for (int b = 0; b < DP / 64; b++) tma_prefetch_3d(&tm_q, b * 64, (c0 + c + 1) * kC, h);
+                    const int st = n % NQ;
+                    if (n >= NQ && !wait_bar(&q_empty[st], ((n / NQ) - 1) & 1, ctl)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&q_full[st], PL::QB);
+                    for (int b = 0; b < DP / 64; b++)
+                        tma_load_3d_hint(gbase + PL::Q0 + st * PL::QB + b * kC * 128, &tm_q, &q_full[st], b * 64,
+                                         (c0 + c) * kC, h, stream);
+                    n++;
+                }
+            }
+            for (uint32_t m = n > NQ ? n - NQ : 0; m < n; m++)
+                mbar_wait(&q_full[m % NQ], (m / NQ) & 1, nullptr, 0);
+        } else if (lane == 1) {
+            // ------------------------------------------- output tile stores
+            prefetch_tmap(&tm_o);
+            uint32_t k = 0;
+            for (int it = 0;; it++) {
+                const int item = next_item(it, false);
+                mbar_arrive(&item_empty[it & 1]);
+                if (item < 0) break;
+                const int s = item / g.BH, h = item % g.BH;
+                const int c0 = s * g.L, nc = min(g.L, g.NC - c0);
+                for (int c = 0; c < nc; c++, k++) {
+                    const int st = k % NO;
+                    if (wait_bar(&out_ready[st], (k / NO) & 1, ctl)) {
+                        const uint32_t src = base + PL::O0 + st * PL::OB;
+                        for (int b = 0; b < DV / 64; b++)
+                            tma_store_3d(&tm_o, src + b * kC * 128, b * 64, (c0 + c) * kC, h);
+                        bulk_commit_group();
+                        bulk_wait_read_all();
+                    }
+                    mbar_arrive(&out_free[st]);
+                }
+            }
+            bulk_wait_all();
+        }
+    } else if (warp == kNcMma) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t id_qs = idesc_bf16(128, DV, 0, 1);
+            constexpr uint32_t id_q16 = idesc_bf16(128, 16, 0, 1);
+            const uint32_t s_addr = base + PL::S0, zp_addr = base + PL::Z0;
+            uint32_t k = 0, ni = 0;
+            for (int it = 0;; it++) {
+                const int item = next_item(it, false);
+                mbar_arrive(&item_empty[it & 1]);
+                if (item < 0) break;
+                const int s = item / g.BH;
+                const int c0 = s * g.L, nc = min(g.L, g.NC - c0);
+                wait_bar(s_ready, ni & 1, ctl);
+                for (int c = 0; c < nc; c++, k++) {
+                    const int st = k % NQ, rr = k & 1;
+                    wait_bar(&q_ready[st], (k / NQ) & 1, ctl);
+                    if (k >= 2) wait_bar(&num_free[rr], ((k >> 1) - 1) & 1, ctl);
+                    tc_fence_after();
+                    const uint32_t qa = base + PL::Q0 + st * PL::QB;
+                    if (!*abort_cta) {
+#pragma unroll
+                        for (int kk = 0; kk < DP; kk += 16) {
+                            const uint64_t ad =
+                                sw128_desc(qa + (kk / 64) * (kC * 128) + (kk % 64) * 2, 16, 1024);
+                            mma_bf16_ss(tmem + rr * 128, ad, sw128_desc(s_addr + (kk / 8) * 1024, DP * 128, 1024),
+                                        id_qs, kk > 0 ? 1u : 0u);
+                            mma_bf16_ss(tmem + PL::T_DEN + rr * 16, ad, sw32_desc(zp_addr + (kk / 8) * 256, 256, 256),
+                                        id_q16, kk > 0 ? 1u : 0u);
+                        }
+                    }
+                    mma_commit(&q_empty[st]);
+                    mma_commit(&num_full[rr]);
+                }
+                mma_commit(s_free);   // S, ZP of this item have been read
+                ni++;
+            }
+            mma_commit(drain);
+            mbar_wait(drain, 0, nullptr, 0);
+        }
+    } else {
+        // ----------------------------------------------------- math warps
+        const int qd = warp & 3, grp = warp >> 2;
+        const int r = qd * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+        const uint32_t s_addr = base + PL::S0, zp_addr = base + PL::Z0;
+        uint32_t k = 0, kq = 0, ni = 0;
+        auto phi_q = [&]() {
+            const int st = kq % NQ;
+            wait_bar(&q_full[st], (kq / NQ) & 1, ctl);
+            const uint32_t t = base + PL::Q0 + st * PL::QB;
+            constexpr int JH = DP / 16;
+            uint4 x[JH];
+#pragma unroll
+            for (int j = 0; j < JH; j++) x[j] = lds128(t + tile_off(r, grp * JH + j));
+#pragma unroll
+            for (int j = 0; j < JH; j++) sts128(t + tile_off(r, grp * JH + j), phi_elu1_bf16x8(x[j]));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&q_ready[st]);
+            kq++;
+        };
+        for (int it = 0;; it++) {
+            const int item = next_item(it, false);
+            if (lane == 0) mbar_arrive(&item_empty[it & 1]);
+            if (item < 0) break;
+            const int s = item / g.BH, h = item % g.BH;
+            const int c0 = s * g.L, nc = min(g.L, g.NC - c0);
+            // S (bf16) and ZP for this head, once the last item's products are done
+            if (ni > 0) wait_bar(s_free, (ni - 1) & 1, ctl);
+            if (r < DP) {
+                const float *src = sc.preS + (long long)h * g.nseg * DP * DV + (long long)r * DV + grp * HALF;
+#pragma unroll
+                for (int cb = 0; cb < HALF; cb += 32) {
+                    uint32_t v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        const float4 x = __ldcg(reinterpret_cast<const float4 *>(src + cb + i));
+                        v[i] = __float_as_uint(x.x);
+                        v[i + 1] = __float_as_uint(x.y);
+                        v[i + 2] = __float_as_uint(x.z);
+                        v[i + 3] = __float_as_uint(x.w);
+                    }
+                    sprev_store32<DP>(s_addr, r, grp * HALF + cb, v);
+                }
+                if (grp == 0) zp_store(zp_addr, r, __ldcg(sc.prez + (long long)h * g.nseg * DP + r));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_ready);
+            ni++;
+            phi_q();
+            for (int c = 0; c < nc; c++, k++) {
+                if (c + 1 < nc) phi_q();
+                // out = NUM / (DEN[0] + DEN[8]) for chunk k -> staging slot k % NO
+                const int rr = k & 1, os = k % NO;
+                wait_bar(&num_full[rr], (k >> 1) & 1, ctl);
+                tc_fence_after();
+                uint32_t d[16], n0[32], n1[32];
+                const uint32_t rn = tmem + lane_base + rr * 128 + grp * HALF;
+                tmem_ld16_nowait(tmem + lane_base + PL::T_DEN + rr * 16, d);
+                tmem_ld32_nowait(rn, n0);
+                if constexpr (HALF == 64) tmem_ld32_nowait(rn + 32, n1);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&num_free[rr]);
+                if (k >= NO) wait_bar(&out_free[os], ((k / NO) - 1) & 1, ctl);
+                const float inv = 1.f / (__uint_as_float(d[0]) + __uint_as_float(d[8]));
+                const uint32_t ot = base + PL::O0 + os * PL::OB + (grp * HALF / 64) * (kC * 128);
+                auto put = [&](const uint32_t(&v)[32], int j0) {
+#pragma unroll
+                    for (int j = 0; j < 4; j++)
+                        sts128(ot + sw128_off(r, j0 + j),
+                               make_uint4(pack_bf16x2(__uint_as_float(v[8 * j]) * inv,
+                                                      __uint_as_float(v[8 * j + 1]) * inv),
+                                          pack_bf16x2(__uint_as_float(v[8 * j + 2]) * inv,
+                                                      __uint_as_float(v[8 * j + 3]) * inv),
+                                          pack_bf16x2(__uint_as_float(v[8 * j + 4]) * inv,
+                                                      __uint_as_float(v[8 * j + 5]) * inv),
+                                          pack_bf16x2(__uint_as_float(v[8 * j + 6]) * inv,
+                                                      __uint_as_float(v[8 * j + 7]) * inv)));
+                };
+                put(n0, HALF == 64 ? 0 : 4 * grp);
+                if constexpr (HALF == 64) put(n1, 4);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&out_ready[os]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kNcMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, PL::TMEM_COLS);
+    }
+}
+
+// Per head: the sums over all segments into the head's first segment slot.
+__global__ void nc_total_kernel(float *__restrict__ preS, float *__restrict__ prez, int nseg, int szS,
+                                int szz)
+{
+    const long long head = blockIdx.y;
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    float *p;
+    int stride;
+    if (e < szS) {
+        p = preS + head * nseg * (long long)szS + e;
+        stride = szS;
+    } else if (e < szS + szz) {
+        p = prez + head * nseg * (long long)szz + (e - szS);
+        stride = szz;
+    } else {
+        return;
+    }
+    float t = 0.f;
+    for (int s = 0; s < nseg; s++) t += p[(long long)s * stride];
+    p[0] = t;
+}
+
 // ------------------------------------------------------------ host side
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode()
@@ -983,6 +1315,55 @@ cudaError_t run(const Problem &p, void *scratch, float *S_out, float *z_out, int
     return cudaSuccess;
 }
 
+template <int DP, int DV>
+cudaError_t run_nc(const Problem &p, void *scratch, float *S_out, float *z_out, int *err, cudaStream_t s)
+{
+    using PL = Plan<DP, DV>;
+    using NP = NcPlan<DP, DV>;
+    CUtensorMap tq, tk, tv, to;
+    if (!make_map(&tq, p.q, p.BH, p.N, p.D) || !make_map(&tk, p.k, p.BH, p.N, p.D) ||
+        !make_map(&tv, p.v, p.BH, p.N, p.Dv) || !make_map(&to, p.out, p.BH, p.N, p.Dv))
+        return cudaErrorInvalidValue;
+    const int sms = num_sms();
+    Geo g = plan(p.BH, p.N, sms);
+    unsigned char *b = (unsigned char *)scratch;
+    Scratch sc;
+    sc.ticket = (int *)b;
+    sc.abort = (int *)(b + 4);
+    sc.preS = (float *)(b + 16);
+    sc.prez = sc.preS + (size_t)g.BH * g.nseg * DP * DV;
+    cudaError_t e;
+    if ((e = cudaMemsetAsync(scratch, 0, 16, s)) != cudaSuccess) return e;
+    // pass 1: phi(K)^T V and colsum phi(K) of every segment
+    if ((e = cudaFuncSetAttribute(tc_causal_kernel<DP, DV, true>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, PL::SMEM)) != cudaSuccess)
+        return e;
+    tc_causal_kernel<DP, DV, true><<<min(g.n_items, sms), kThreads, PL::SMEM, s>>>(
+        tq, tk, tv, to, g, sc, (__nv_bfloat16 *)p.out, nullptr, nullptr, err);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int sz = DP * DV + DP;
+    nc_total_kernel<<<dim3(cdiv(sz, 256), (unsigned)g.BH), 256, 0, s>>>(sc.preS, sc.prez, g.nseg, DP * DV,
+                                                                       DP);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(scratch, 0, 4, s)) != cudaSuccess) return e;   // ticket
+    // pass 2: the readout
+    if ((e = cudaFuncSetAttribute(nc_out_kernel<DP, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  NP::SMEM)) != cudaSuccess)
+        return e;
+    nc_out_kernel<DP, DV><<<min(g.n_items, sms), kNcThreads, NP::SMEM, s>>>(tq, to, g, sc, err);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    note_launches(3);
+    // the memories (the totals) for la_forward_ex
+    if (S_out &&
+        (e = cudaMemcpy2DAsync(S_out, (size_t)DP * DV * 4, sc.preS, (size_t)g.nseg * DP * DV * 4,
+                               (size_t)DP * DV * 4, g.BH, cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
+        return e;
+    if (z_out && (e = cudaMemcpy2DAsync(z_out, (size_t)DP * 4, sc.prez, (size_t)g.nseg * DP * 4, (size_t)DP * 4,
+                                        g.BH, cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
+        return e;
+    return cudaSuccess;
+}
+
 }  // namespace
 
 bool tc_causal_supported(const Problem &p)
@@ -998,6 +1379,21 @@ size_t tc_causal_scratch_bytes(const Problem &p)
     if (p.D == 64 && p.Dv == 128) return scratch_bytes<64, 128>(g);
     if (p.D == 128 && p.Dv == 64) return scratch_bytes<128, 64>(g);
     return scratch_bytes<128, 128>(g);
+}
+
+size_t tc_noncausal_scratch_bytes(const Problem &p)
+{
+    Geo g = plan(p.BH, p.N, num_sms());
+    return 16 + (size_t)g.BH * g.nseg * ((size_t)p.P * p.Dv + p.P) * sizeof(float);
+}
+
+cudaError_t tc_noncausal(const Problem &p, void *scratch, float *S_out, float *z_out, int *err,
+                         cudaStream_t s)
+{
+    if (p.D == 64 && p.Dv == 64) return run_nc<64, 64>(p, scratch, S_out, z_out, err, s);
+    if (p.D == 64 && p.Dv == 128) return run_nc<64, 128>(p, scratch, S_out, z_out, err, s);
+    if (p.D == 128 && p.Dv == 64) return run_nc<128, 64>(p, scratch, S_out, z_out, err, s);
+    return run_nc<128, 128>(p, scratch, S_out, z_out, err, s);
 }
 
 cudaError_t tc_causal(const Problem &p, void *scratch, float *S_out, float *z_out, int *err,

@@ -38,12 +38,17 @@ def _forward_and_check(la, w: wl.Workload, head_sample=None, state_tol=2e-2):
         ref = oracle.forward(np64(qf), np64(kf), np64(vf), causal=False, feature=w.feature, W=Wn)
     got = np64(out.reshape(BH, w.N, w.Dv)[heads]).reshape(ref.shape)
     err = assert_close(got, ref, w.dtype, what=w.name)
-    if w.causal:
-        P = w.phi_dim
-        Sg = np64(S.reshape(BH, P, w.Dv)[heads]).reshape(Sref.shape)
-        zg = np64(z.reshape(BH, P)[heads]).reshape(zref.shape)
-        assert_state_close(Sg, Sref, state_tol, what="S_out")
-        assert_state_close(zg, zref, state_tol, what="z_out")
+    if not w.causal:
+        # the non-causal memories are the sums over every key: S = phi(K)^T V,
+        # z = sum_j phi(k_j)
+        pk = oracle.phi(np64(kf), feature=w.feature, W=Wn)
+        Sref = np.einsum("bhnp,bhnv->bhpv", pk, np64(vf))
+        zref = pk.sum(axis=2)
+    P = w.phi_dim
+    Sg = np64(S.reshape(BH, P, w.Dv)[heads]).reshape(Sref.shape)
+    zg = np64(z.reshape(BH, P)[heads]).reshape(zref.shape)
+    assert_state_close(Sg, Sref, state_tol, what="S_out")
+    assert_state_close(zg, zref, state_tol, what="z_out")
     return err, (q, k, v, S, z)
 
 
@@ -114,12 +119,27 @@ def test_causal_launch_plan(la):
         assert la.la_launch_count() - n0 == expect, (B, H, D)
 
 
+def test_noncausal_launch_plan(la):
+    """Non-causal bf16 elu+1 with D, Dv in {64, 128}: the segment-sum pass, the
+    per-head total and the readout (three kernels); other shapes: the
+    CUDA-core reduction and readout."""
+    for (H, D, expect) in ((2, 128, 3), (160, 64, 3)):
+        w = wl.small(B=1, H=H, N=1024, D=D, Dv=D, causal=False, seed=6)
+        q, k, v = (t.cuda() for t in wl.make_qkv(w))
+        n0 = la.la_launch_count()
+        la.la_forward(q, k, v, causal=False)
+        torch.cuda.synchronize()
+        assert la.la_launch_count() - n0 == expect, (H, D)
+
+
+@pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("H,N,D,Dv", [(3, 128 * 37 + 5, 128, 128), (2, 128 * 21 + 77, 64, 128),
                                       (5, 128 * 11 + 1, 128, 64), (1, 128 * 64, 64, 64)])
-def test_long_segment_chain_all_heads(la, H, N, D, Dv):
-    """Few heads and many chunks: the heads are cut into short segments whose
-    states are chained across CTAs; every head, every position is checked,
-    including a ragged last chunk."""
-    w = wl.small(B=1, H=H, N=N, D=D, Dv=Dv, seed=N + H)
+def test_long_segment_chain_all_heads(la, H, N, D, Dv, causal):
+    """Few heads and many chunks: the heads are cut into short segments
+    (causal: whose states are chained across CTAs; non-causal: whose sums are
+    totalled per head); every head, every position and both memories are
+    checked, including a ragged last chunk."""
+    w = wl.small(B=1, H=H, N=N, D=D, Dv=Dv, causal=causal, seed=N + H)
     err, _ = _forward_and_check(la, w)
     assert err <= 2e-2
