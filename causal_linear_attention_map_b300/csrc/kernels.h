@@ -30,20 +30,20 @@ struct Problem {
 // does not take.
 cudaError_t simt_causal(const Problem &p, float *S_out, float *z_out, cudaStream_t s);
 
-// Tensor-core (tcgen05) chunked causal kernel: bf16, elu+1, D and Dv in
-// {64, 128}.  Scratch: per-segment states (0 bytes when one segment per head
-// fills the GPU).  `err` is the device word that bounded waits set on timeout.
+// Tensor-core (tcgen05) forward, causal or not, bf16:
+//   elu + 1 with D, Dv in {64, 128} (tc_causal_supported), applied in the
+//   tile loads;
+//   random features with D = 64 and (m = 128, Dv in {64, 128}) or
+//   (m = 256, Dv = 64) (tc_prf_supported): phi(q), phi(k) materialised in
+//   bf16 scratch by a tcgen05 projection kernel, then the same chunk kernels.
+// Scratch (tc_scratch_bytes): control words, segment sums, per-head totals
+// (non-causal), phi tiles and partial sums (random features).  `err` is the
+// device word that bounded waits set on timeout.
 bool tc_causal_supported(const Problem &p);
-size_t tc_causal_scratch_bytes(const Problem &p);
-cudaError_t tc_causal(const Problem &p, void *scratch, float *S_out, float *z_out, int *err,
-                      cudaStream_t s);
-
-// Tensor-core non-causal forward (same shapes as tc_causal_supported): the
-// segment sums of tc_causal's first pass over every segment, their total per
-// head, then the readout.  Scratch: 16 B + B*H*nseg*(Dphi*Dv + Dphi)*4.
-size_t tc_noncausal_scratch_bytes(const Problem &p);
-cudaError_t tc_noncausal(const Problem &p, void *scratch, float *S_out, float *z_out, int *err,
-                         cudaStream_t s);
+bool tc_prf_supported(const Problem &p);
+size_t tc_scratch_bytes(const Problem &p, bool causal);
+cudaError_t tc_forward(const Problem &p, bool causal, void *scratch, float *S_out, float *z_out, int *err,
+                       cudaStream_t s);
 
 // Non-causal: KV = phi(K)^T V and ksum = sum phi(k) reduced over N into
 // fp32 scratch (KV [BH, P, Dv], ksum [BH, P]; zeroed here), then the readout.

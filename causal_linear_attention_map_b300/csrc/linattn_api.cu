@@ -144,25 +144,15 @@ int forward_impl(const void *q, const void *k, const void *v, void *out, int B, 
     DeviceCtx *ctx = nullptr;
     if ((st = get_ctx(&ctx)) != LA_OK) return st;
 
-    if (causal) {
-        if (!la::tc_causal_supported(p)) return cuda_status(la::simt_causal(p, S_out, z_out, s));
-        size_t bytes = la::tc_causal_scratch_bytes(p);
-        void *scratch = nullptr;
-        if (bytes && cudaMallocFromPoolAsync(&scratch, bytes, ctx->pool, s) != cudaSuccess)
-            return cuda_status(cudaErrorMemoryAllocation);
-        cudaError_t e = la::tc_causal(p, scratch, S_out, z_out, ctx->err_word, s);
-        cudaError_t e2 = scratch ? cudaFreeAsync(scratch, s) : cudaSuccess;
-        return cuda_status(e != cudaSuccess ? e : e2);
-    }
-
-    const bool tc = la::tc_causal_supported(p);   // same shapes for both forms
-    size_t bytes = tc ? la::tc_noncausal_scratch_bytes(p) : la::noncausal_scratch_bytes(p);
+    const bool tc = la::tc_causal_supported(p) || la::tc_prf_supported(p);
+    if (causal && !tc) return cuda_status(la::simt_causal(p, S_out, z_out, s));
+    size_t bytes = tc ? la::tc_scratch_bytes(p, causal != 0) : la::noncausal_scratch_bytes(p);
     void *scratch = nullptr;
-    if (cudaMallocFromPoolAsync(&scratch, bytes, ctx->pool, s) != cudaSuccess)
+    if (bytes && cudaMallocFromPoolAsync(&scratch, bytes, ctx->pool, s) != cudaSuccess)
         return cuda_status(cudaErrorMemoryAllocation);
-    cudaError_t e = tc ? la::tc_noncausal(p, scratch, S_out, z_out, ctx->err_word, s)
+    cudaError_t e = tc ? la::tc_forward(p, causal != 0, scratch, S_out, z_out, ctx->err_word, s)
                        : la::noncausal(p, scratch, S_out, z_out, s);
-    cudaError_t e2 = cudaFreeAsync(scratch, s);
+    cudaError_t e2 = scratch ? cudaFreeAsync(scratch, s) : cudaSuccess;
     return cuda_status(e != cudaSuccess ? e : e2);
 }
 

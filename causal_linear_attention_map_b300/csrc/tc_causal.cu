@@ -68,6 +68,7 @@
 // library's device error word, raises a per-launch abort word that every
 // other CTA polls, and all roles run to the end without waiting.
 #include <cuda.h>
+#include <cmath>
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -130,6 +131,7 @@ struct Geo {
     int BH, N, NC;   // heads, positions, chunks per head
     int L, nseg;     // chunks per segment, segments per head
     int n_items;     // items of this launch: B*H*(nseg-1) (aggregate form) or B*H*nseg
+    int exp_rows;    // rows per head of the exported state S_out / z_out (>= DP)
 };
 
 struct Scratch {
@@ -137,7 +139,19 @@ struct Scratch {
     int *abort;      // raised by any CTA whose wait ran out
     float *preS;     // [BH, nseg, DP, DV]: segment sums, then their exclusive prefixes
     float *prez;     // [BH, nseg, DP]
+    float *num_part; // [BH, N, DV] fp32: first feature half's NUM (split feature maps)
+    float *den_part; // [BH, N]
 };
+
+// What the kernel applies to the Q and K tiles and how it finishes a chunk.
+//   kModeElu       phi = elu + 1 on the tiles; out = NUM / DEN
+//   kModeFeat      the tiles already hold phi(q), phi(k); out = NUM / DEN
+//   kModeFeatPart  phi tiles of the first half of a feature map split in two:
+//                  NUM, DEN (un-normalised) -> num_part, den_part
+//   kModeFeatComb  the second half: out = (NUM + num_part) / (DEN + den_part)
+// A feature map of Dphi = 2 x 128 thus runs as two passes whose sums over
+// features add up exactly to the single-pass ones.
+enum { kModeElu = 0, kModeFeat = 1, kModeFeatPart = 2, kModeFeatComb = 3 };
 
 struct Ctl {
     volatile int *cta;     // shared abort word of this CTA
@@ -204,7 +218,7 @@ __device__ __forceinline__ void zp_store(uint32_t zp, int r, float z)
 
 // ---------------------------------------------------------------- kernel
 
-template <int DP, int DV, bool AGG>
+template <int DP, int DV, bool AGG, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -215,6 +229,8 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     using PL = Plan<DP, DV>;
     constexpr int NS = PL::NS, NSP = PL::NSP, PR = PL::PR;
     constexpr int HALF = DV / 2;   // state / NUM columns per TMEM warp
+    constexpr bool kPhi = MODE == kModeElu;   // apply elu + 1 to the Q and K tiles in place
+    static_assert(MODE != kModeFeatComb || HALF == 32, "the split feature map takes Dv = 64");
     extern __shared__ unsigned char smem_raw[];
     const uint32_t base = align1k(smem_u32(smem_raw));
     unsigned char *gbase = smem_raw + (base - smem_u32(smem_raw));   // generic view of `base`
@@ -360,7 +376,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     const int st = nv % NS;
                     const bool ok = wait_bar(&out_ready[st], oc[st] & 1, ctl);
                     oc[st]++;
-                    if (ok) {
+                    if (ok && MODE != kModeFeatPart) {
                         const uint32_t src = base + PL::V0 + st * PL::VB;
 #pragma unroll
                         for (int b = 0; b < DV / 64; b++)
@@ -534,14 +550,16 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const int st = n % NS;
             wait_bar(&full[st], (n / NS) & 1, ctl);
             const uint32_t t = ring + st * PL::QB;
+            if constexpr (kPhi) {   // (phi tiles arrive from HBM as they are; rows past N are zero-filled)
 #pragma unroll
-            for (int h8 = 0; h8 < JR; h8 += 8) {
-                uint4 x[8];
+                for (int h8 = 0; h8 < JR; h8 += 8) {
+                    uint4 x[8];
 #pragma unroll
-                for (int j = 0; j < 8; j++) x[j] = lds128(t + tile_off(r, h8 + j));
+                    for (int j = 0; j < 8; j++) x[j] = lds128(t + tile_off(r, h8 + j));
 #pragma unroll
-                for (int j = 0; j < 8; j++)
-                    sts128(t + tile_off(r, h8 + j), zero ? make_uint4(0, 0, 0, 0) : phi_elu1_bf16x8(x[j]));
+                    for (int j = 0; j < 8; j++)
+                        sts128(t + tile_off(r, h8 + j), zero ? make_uint4(0, 0, 0, 0) : phi_elu1_bf16x8(x[j]));
+                }
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -612,12 +630,14 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const int st = nqt % NS;
             wait_bar(&q_full[st], (nqt / NS) & 1, ctl);
             const uint32_t t = base + PL::Q0 + st * PL::QB;
-            constexpr int JH = DP / 16;   // 16 B chunks per half row
-            uint4 x[JH];
+            if constexpr (kPhi) {
+                constexpr int JH = DP / 16;   // 16 B chunks per half row
+                uint4 x[JH];
 #pragma unroll
-            for (int j = 0; j < JH; j++) x[j] = lds128(t + tile_off(r, grp * JH + j));
+                for (int j = 0; j < JH; j++) x[j] = lds128(t + tile_off(r, grp * JH + j));
 #pragma unroll
-            for (int j = 0; j < JH; j++) sts128(t + tile_off(r, grp * JH + j), phi_elu1_bf16x8(x[j]));
+                for (int j = 0; j < JH; j++) sts128(t + tile_off(r, grp * JH + j), phi_elu1_bf16x8(x[j]));
+            }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&q_ready[st]);
@@ -767,32 +787,69 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (lane == 0) mbar_arrive(&num_free[k & 1]);
                 {   // out(k) = NUM / (DEN[0] + DEN[8]) -> the V slot of chunk k (bf16, swizzled)
                     const int vs = nvr % NS;
-                    const float inv = 1.f / (__uint_as_float(d[0]) + __uint_as_float(d[8]));
-                    const uint32_t vt = base + PL::V0 + vs * PL::VB + (grp * HALF / 64) * (kC * 128);
-                    auto put = [&](const uint32_t(&v)[32], int j0) {
+                    const int pos = row0 + r;                 // this thread's position in the head
+                    const long long prow = (long long)h * g.N + pos;
+                    float den = __uint_as_float(d[0]) + __uint_as_float(d[8]);
+                    if constexpr (MODE == kModeFeatPart) {
+                        // first feature half: the un-normalised sums -> scratch
+                        if (pos < g.N) {
+                            float4 *dst = reinterpret_cast<float4 *>(sc.num_part + prow * DV + grp * HALF);
 #pragma unroll
-                        for (int j = 0; j < 4; j++)
-                            sts128(vt + sw128_off(r, j0 + j),
-                                   make_uint4(pack_bf16x2(__uint_as_float(v[8 * j]) * inv,
-                                                          __uint_as_float(v[8 * j + 1]) * inv),
-                                              pack_bf16x2(__uint_as_float(v[8 * j + 2]) * inv,
-                                                          __uint_as_float(v[8 * j + 3]) * inv),
-                                              pack_bf16x2(__uint_as_float(v[8 * j + 4]) * inv,
-                                                          __uint_as_float(v[8 * j + 5]) * inv),
-                                              pack_bf16x2(__uint_as_float(v[8 * j + 6]) * inv,
-                                                          __uint_as_float(v[8 * j + 7]) * inv)));
-                    };
-                    // HALF = 64: this warp's half is one whole 64-column block;
-                    // HALF = 32: half a block, starting at chunk 4 * (grp % 2)
-                    put(n0, HALF == 64 ? 0 : 4 * grp);
-                    if constexpr (HALF == 64) put(n1, 4);
+                            for (int i = 0; i < 8; i++)
+                                __stcg(dst + i, make_float4(__uint_as_float(n0[4 * i]), __uint_as_float(n0[4 * i + 1]),
+                                                            __uint_as_float(n0[4 * i + 2]),
+                                                            __uint_as_float(n0[4 * i + 3])));
+                            if constexpr (HALF == 64) {
+#pragma unroll
+                                for (int i = 0; i < 8; i++)
+                                    __stcg(dst + 8 + i,
+                                           make_float4(__uint_as_float(n1[4 * i]), __uint_as_float(n1[4 * i + 1]),
+                                                       __uint_as_float(n1[4 * i + 2]), __uint_as_float(n1[4 * i + 3])));
+                            }
+                            if (grp == 0) __stcg(sc.den_part + prow, den);
+                        }
+                    } else {
+                        if constexpr (MODE == kModeFeatComb) {
+                            // second feature half: add the first half's sums (HALF = 32)
+                            if (pos < g.N) {
+                                const float4 *src = reinterpret_cast<const float4 *>(sc.num_part + prow * DV + grp * HALF);
+#pragma unroll
+                                for (int i = 0; i < 8; i++) {
+                                    const float4 a = __ldcg(src + i);
+                                    n0[4 * i] = __float_as_uint(__uint_as_float(n0[4 * i]) + a.x);
+                                    n0[4 * i + 1] = __float_as_uint(__uint_as_float(n0[4 * i + 1]) + a.y);
+                                    n0[4 * i + 2] = __float_as_uint(__uint_as_float(n0[4 * i + 2]) + a.z);
+                                    n0[4 * i + 3] = __float_as_uint(__uint_as_float(n0[4 * i + 3]) + a.w);
+                                }
+                                den += __ldcg(sc.den_part + prow);
+                            }
+                        }
+                        const float inv = 1.f / den;
+                        const uint32_t vt = base + PL::V0 + vs * PL::VB + (grp * HALF / 64) * (kC * 128);
+                        auto put = [&](const uint32_t(&v)[32], int j0) {
+#pragma unroll
+                            for (int j = 0; j < 4; j++)
+                                sts128(vt + sw128_off(r, j0 + j),
+                                       make_uint4(pack_bf16x2(__uint_as_float(v[8 * j]) * inv,
+                                                              __uint_as_float(v[8 * j + 1]) * inv),
+                                                  pack_bf16x2(__uint_as_float(v[8 * j + 2]) * inv,
+                                                              __uint_as_float(v[8 * j + 3]) * inv),
+                                                  pack_bf16x2(__uint_as_float(v[8 * j + 4]) * inv,
+                                                              __uint_as_float(v[8 * j + 5]) * inv),
+                                                  pack_bf16x2(__uint_as_float(v[8 * j + 6]) * inv,
+                                                              __uint_as_float(v[8 * j + 7]) * inv)));
+                        };
+                        // HALF = 64: this warp's half is one whole 64-column block;
+                        // HALF = 32: half a block, starting at chunk 4 * (grp % 2)
+                        put(n0, HALF == 64 ? 0 : 4 * grp);
+                        if constexpr (HALF == 64) put(n1, 4);
+                    }
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&out_ready[vs]);
                     nvr++;
                 }
                 (void)ok;
-                (void)row0;
                 if (!more) sd = wait_sdone();   // the last chunk's state update
                 // the head's final state after its last chunk
                 if (!more && sd && s == g.nseg - 1 && srow && (S_out || z_out)) {
@@ -803,7 +860,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         tmem_ld32_nowait(tmem + lane_base + PL::T_S + grp * HALF + cb, v);
                         tmem_ld_wait();
                         if (S_out) {
-                            float *dst = S_out + ((long long)h * DP + r) * DV + grp * HALF + cb;
+                            float *dst = S_out + ((long long)h * g.exp_rows + r) * DV + grp * HALF + cb;
 #pragma unroll
                             for (int i = 0; i < 32; i += 4)
                                 *reinterpret_cast<float4 *>(dst + i) =
@@ -815,7 +872,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         uint32_t zv[16];
                         tmem_ld16_nowait(tmem + lane_base + PL::T_Z, zv);
                         tmem_ld_wait();
-                        z_out[(long long)h * DP + r] = __uint_as_float(zv[0]);
+                        z_out[(long long)h * g.exp_rows + r] = __uint_as_float(zv[0]);
                     }
                 }
                 if (more && late) sprev_from_tmem();
@@ -876,7 +933,7 @@ struct NcPlan {
     static_assert(SMEM > 114 * 1024, "one CTA per SM: the kernel holds all 512 TMEM columns");
 };
 
-template <int DP, int DV>
+template <int DP, int DV, bool PHI>
 __global__ void __launch_bounds__(kNcThreads, 1)
 nc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o, Geo g,
               Scratch sc, int *err)
@@ -1053,12 +1110,14 @@ nc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const int st = kq % NQ;
             wait_bar(&q_full[st], (kq / NQ) & 1, ctl);
             const uint32_t t = base + PL::Q0 + st * PL::QB;
-            constexpr int JH = DP / 16;
-            uint4 x[JH];
+            if constexpr (PHI) {
+                constexpr int JH = DP / 16;
+                uint4 x[JH];
 #pragma unroll
-            for (int j = 0; j < JH; j++) x[j] = lds128(t + tile_off(r, grp * JH + j));
+                for (int j = 0; j < JH; j++) x[j] = lds128(t + tile_off(r, grp * JH + j));
 #pragma unroll
-            for (int j = 0; j < JH; j++) sts128(t + tile_off(r, grp * JH + j), phi_elu1_bf16x8(x[j]));
+                for (int j = 0; j < JH; j++) sts128(t + tile_off(r, grp * JH + j), phi_elu1_bf16x8(x[j]));
+            }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&q_ready[st]);
@@ -1072,8 +1131,8 @@ nc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const int c0 = s * g.L, nc = min(g.L, g.NC - c0);
             // S (bf16) and ZP for this head, once the last item's products are done
             if (ni > 0) wait_bar(s_free, (ni - 1) & 1, ctl);
-            if (r < DP) {
-                const float *src = sc.preS + (long long)h * g.nseg * DP * DV + (long long)r * DV + grp * HALF;
+            for (int row = r; row < DP; row += kC) {   // the head's totals (sc.preS, sc.prez: [BH, DP, DV], [BH, DP])
+                const float *src = sc.preS + (long long)h * DP * DV + (long long)row * DV + grp * HALF;
 #pragma unroll
                 for (int cb = 0; cb < HALF; cb += 32) {
                     uint32_t v[32];
@@ -1085,9 +1144,9 @@ nc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         v[i + 2] = __float_as_uint(x.z);
                         v[i + 3] = __float_as_uint(x.w);
                     }
-                    sprev_store32<DP>(s_addr, r, grp * HALF + cb, v);
+                    sprev_store32<DP>(s_addr, row, grp * HALF + cb, v);
                 }
-                if (grp == 0) zp_store(zp_addr, r, __ldcg(sc.prez + (long long)h * g.nseg * DP + r));
+                if (grp == 0) zp_store(zp_addr, row, __ldcg(sc.prez + (long long)h * DP + row));
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -1141,26 +1200,269 @@ nc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
 }
 
-// Per head: the sums over all segments into the head's first segment slot.
-__global__ void nc_total_kernel(float *__restrict__ preS, float *__restrict__ prez, int nseg, int szS,
-                                int szz)
+// Per head: the sums over all segments (preS [BH, nseg, szS], prez [BH,
+// nseg, szz]) -> totals totS [BH, tot_rows * Dv] and totz [BH, tot_rows] at
+// element offsets offS, offz (a feature map split in halves fills one half
+// of the rows per call).
+__global__ void nc_total_kernel(const float *__restrict__ preS, const float *__restrict__ prez, int nseg,
+                                int szS, int szz, float *__restrict__ totS, float *__restrict__ totz,
+                                int tot_szS, int tot_szz, int offS, int offz)
 {
     const long long head = blockIdx.y;
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
-    float *p;
+    const float *p;
+    float *dst;
     int stride;
     if (e < szS) {
         p = preS + head * nseg * (long long)szS + e;
         stride = szS;
+        dst = totS + head * tot_szS + offS + e;
     } else if (e < szS + szz) {
         p = prez + head * nseg * (long long)szz + (e - szS);
         stride = szz;
+        dst = totz + head * tot_szz + offz + (e - szS);
     } else {
         return;
     }
     float t = 0.f;
     for (int s = 0; s < nseg; s++) t += p[(long long)s * stride];
-    p[0] = t;
+    *dst = t;
+}
+
+// ------------------------------------------- random-feature map (PRF)
+//
+// phi(x) = exp(W x - |x|^2 / 2) / sqrt(m) for every row x of q and of k
+// (positive random features; review page "Rethinking Attention with
+// Performers", FAVOR+ positive random features), written to HBM as bf16
+// [rows, m] so that the chunk kernels above take them as their phi tiles.
+// U = X W^T runs on tcgen05 (M = 128 rows, N = m, K = D) with fp32
+// accumulation; W (fp32) enters as two bf16 operands W_hi = bf16(W) and
+// W_lo = bf16(W - W_hi) whose products add up in the same accumulator, so
+// that W keeps about 16 significant bits.  |x|^2 comes from the X tile in
+// shared memory; the exponent folds in the 1/sqrt(m) as -ln(m)/2.
+// Roles (10 warps): 8 epilogue warps (lane quadrant w % 4, feature half
+// w / 4), one producer warp (lane 0: X tiles; lane 1: TMA stores of the phi
+// tiles), one MMA warp.  Tiles are striped over the CTAs: tile t of the
+// 2 T tiles is q's tile t (t < T) or k's tile t - T.
+
+template <int D, int M>
+struct PrfPlan {
+    static constexpr int XB = kC * D * 2;    // one X tile
+    static constexpr int WB = M * D * 2;     // W_hi (then W_lo)
+    static constexpr int OB = kC * M * 2;    // one phi tile
+    static constexpr int kBudget = 227 * 1024 - 2048;
+    static constexpr int NO = (2 * WB + 2 * OB + 2 * XB <= kBudget) ? 2 : 1;
+    static constexpr int NX0 = (kBudget - 2 * WB - NO * OB) / XB;
+    static constexpr int NX = NX0 > 4 ? 4 : NX0;
+    static_assert(NX >= 2, "X ring too shallow");
+    static constexpr int X0 = 0;
+    static constexpr int W0 = X0 + NX * XB;
+    static constexpr int O0 = W0 + 2 * WB;
+    static constexpr int TILES = O0 + NO * OB;
+    static constexpr int SMEM = TILES + 1024 + 1024;
+    static constexpr int TMEM_COLS = 2 * M;   // two accumulators
+    static_assert(SMEM <= 227 * 1024, "shared memory plan too large");
+    static_assert(SMEM > 114 * 1024, "one CTA per SM");
+    static_assert(D % 64 == 0 && M % 64 == 0 && M <= 256, "shape");
+};
+
+template <int D, int M>
+__global__ void __launch_bounds__(kNcThreads, 1)
+prf_phi_kernel(const __grid_constant__ CUtensorMap tm_xq, const __grid_constant__ CUtensorMap tm_xk,
+               const __grid_constant__ CUtensorMap tm_pq, const __grid_constant__ CUtensorMap tm_pk,
+               const float *__restrict__ W, int T, float log_scale, int *err)
+{
+    using PL = PrfPlan<D, M>;
+    constexpr int NX = PL::NX, NO = PL::NO;
+    constexpr int MH = M / 2;   // features per epilogue warp
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t base = align1k(smem_u32(smem_raw));
+    unsigned char *gbase = smem_raw + (base - smem_u32(smem_raw));
+    uint64_t *bar = reinterpret_cast<uint64_t *>(gbase + PL::TILES);
+    uint64_t *x_full = bar, *x_empty = bar + NX;
+    uint64_t *acc_full = bar + 2 * NX, *acc_free = acc_full + 2;
+    uint64_t *o_ready = acc_free + 2, *o_free = o_ready + NO, *drain = o_free + NO;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_cta = reinterpret_cast<volatile int *>(drain + 2);
+    static_assert((2 * NX + 4 + 2 * NO + 3) * 8 <= 1024, "barrier map exceeds its 1 KB");
+    int dummy_glob = 0;   // tiles are independent: an abort stays inside this CTA
+    const Ctl ctl{abort_cta, &dummy_glob, err};
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int total = 2 * T;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NX; i++) {
+            mbar_init(&x_full[i], 1);
+            mbar_init(&x_empty[i], kNcMath + 1);   // the epilogue warps (|x|^2) and the MMA commit
+        }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_free[i], kNcMath);
+        }
+        for (int i = 0; i < NO; i++) {
+            mbar_init(&o_ready[i], kNcMath);
+            mbar_init(&o_free[i], 1);
+        }
+        mbar_init(drain, 1);
+        *abort_cta = 0;
+        fence_mbar_init();
+    }
+    if (warp < kNcMath) {
+        // W -> W_hi, W_lo: K-major [M x D] operands, 128-byte swizzle, D / 64 blocks of M rows
+        for (int row = threadIdx.x; row < M; row += kNcMath * 32) {
+#pragma unroll
+            for (int c = 0; c < D / 8; c++) {
+                const float4 a = __ldg(reinterpret_cast<const float4 *>(W + (long long)row * D + 8 * c));
+                const float4 b = __ldg(reinterpret_cast<const float4 *>(W + (long long)row * D + 8 * c + 4));
+                const float w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                float hi[8], lo[8];
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    hi[i] = __bfloat162float(__float2bfloat16_rn(w[i]));
+                    lo[i] = w[i] - hi[i];
+                }
+                const uint32_t off = (uint32_t)(c / 8) * (M * 128) + sw128_off(row, c % 8);
+                sts128(base + PL::W0 + off, make_uint4(pack_bf16x2(hi[0], hi[1]), pack_bf16x2(hi[2], hi[3]),
+                                                       pack_bf16x2(hi[4], hi[5]), pack_bf16x2(hi[6], hi[7])));
+                sts128(base + PL::W0 + PL::WB + off,
+                       make_uint4(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]), pack_bf16x2(lo[4], lo[5]),
+                                  pack_bf16x2(lo[6], lo[7])));
+            }
+        }
+        fence_proxy_async_smem();
+    }
+    if (warp == kNcMma) tmem_alloc(tslot, PL::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    if (warp == kNcProducer) {
+        if (lane == 0) {
+            // ---------------------------------------------- X tile producer
+            prefetch_tmap(&tm_xq);
+            prefetch_tmap(&tm_xk);
+            const uint64_t stream = policy_evict_first();
+            uint32_t n = 0;
+            for (int t = blockIdx.x; t < total; t += gridDim.x, n++) {
+                const int st = n % NX;
+                if (n >= NX && !wait_bar(&x_empty[st], ((n / NX) - 1) & 1, ctl)) break;
+                const CUtensorMap *tm = t < T ? &tm_xq : &tm_xk;
+                const int row = (t < T ? t : t - T) * kC;
+                mbar_arrive_expect_tx(&x_full[st], PL::XB);
+                for (int b = 0; b < D / 64; b++)
+                    tma_load_3d_hint(gbase + PL::X0 + st * PL::XB + b * kC * 128, tm, &x_full[st], b * 64, row, 0,
+                                     stream);
+            }
+            for (uint32_t m = n > NX ? n - NX : 0; m < n; m++)
+                mbar_wait(&x_full[m % NX], (m / NX) & 1, nullptr, 0);
+        } else if (lane == 1) {
+            // ------------------------------------------- phi tile stores
+            prefetch_tmap(&tm_pq);
+            prefetch_tmap(&tm_pk);
+            uint32_t n = 0;
+            for (int t = blockIdx.x; t < total; t += gridDim.x, n++) {
+                const int os = n % NO;
+                if (wait_bar(&o_ready[os], (n / NO) & 1, ctl)) {
+                    const CUtensorMap *tm = t < T ? &tm_pq : &tm_pk;
+                    const int row = (t < T ? t : t - T) * kC;
+                    const uint32_t src = base + PL::O0 + os * PL::OB;
+                    for (int b = 0; b < M / 64; b++) tma_store_3d(tm, src + b * kC * 128, b * 64, row, 0);
+                    bulk_commit_group();
+                    bulk_wait_read_all();
+                }
+                mbar_arrive(&o_free[os]);
+            }
+            bulk_wait_all();
+        }
+    } else if (warp == kNcMma) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t id = idesc_bf16(128, M, 0, 0);
+            const uint32_t w_hi = base + PL::W0, w_lo = base + PL::W0 + PL::WB;
+            uint32_t n = 0;
+            for (int t = blockIdx.x; t < total; t += gridDim.x, n++) {
+                const int st = n % NX, a = n & 1;
+                wait_bar(&x_full[st], (n / NX) & 1, ctl);
+                if (n >= 2) wait_bar(&acc_free[a], ((n >> 1) - 1) & 1, ctl);
+                tc_fence_after();
+                const uint32_t xa = base + PL::X0 + st * PL::XB;
+                if (!*abort_cta) {
+#pragma unroll
+                    for (int kk = 0; kk < D; kk += 16) {
+                        const uint32_t ko = (kk / 64) * (kC * 128) + (kk % 64) * 2;
+                        const uint32_t wo = (kk / 64) * (M * 128) + (kk % 64) * 2;
+                        const uint64_t ad = sw128_desc(xa + ko, 16, 1024);
+                        mma_bf16_ss(tmem + a * M, ad, sw128_desc(w_hi + wo, 16, 1024), id, kk > 0 ? 1u : 0u);
+                        mma_bf16_ss(tmem + a * M, ad, sw128_desc(w_lo + wo, 16, 1024), id, 1u);
+                    }
+                }
+                mma_commit(&x_empty[st]);
+                mma_commit(&acc_full[a]);
+            }
+            mma_commit(drain);
+            mbar_wait(drain, 0, nullptr, 0);
+        }
+    } else {
+        // ------------------------------------------------- epilogue warps
+        const int qd = warp & 3, grp = warp >> 2;
+        const int r = qd * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+        uint32_t n = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, n++) {
+            const int st = n % NX, a = n & 1, os = n % NO;
+            // |x|^2 of this thread's row
+            wait_bar(&x_full[st], (n / NX) & 1, ctl);
+            float ss = 0.f;
+#pragma unroll
+            for (int c = 0; c < D / 8; c++) {
+                const uint4 w = lds128(base + PL::X0 + st * PL::XB + tile_off(r, c));
+                const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const float lo = __uint_as_float(u[i] << 16), hi = __uint_as_float(u[i] & 0xffff0000u);
+                    ss = fmaf(lo, lo, ss);
+                    ss = fmaf(hi, hi, ss);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&x_empty[st]);
+            const float shift = 0.5f * ss + log_scale;
+            wait_bar(&acc_full[a], (n >> 1) & 1, ctl);
+            tc_fence_after();
+            if (n >= NO) wait_bar(&o_free[os], ((n / NO) - 1) & 1, ctl);
+            const uint32_t ot = base + PL::O0 + os * PL::OB;
+#pragma unroll
+            for (int cb = 0; cb < MH; cb += 32) {
+                uint32_t v[32];
+                tmem_ld32_nowait(tmem + lane_base + a * M + grp * MH + cb, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    const int col = grp * MH + cb + 8 * j;
+                    uint32_t w[4];
+#pragma unroll
+                    for (int i = 0; i < 4; i++)
+                        w[i] = pack_bf16x2(__expf(__uint_as_float(v[8 * j + 2 * i]) - shift),
+                                           __expf(__uint_as_float(v[8 * j + 2 * i + 1]) - shift));
+                    sts128(ot + (uint32_t)(col >> 6) * (kC * 128) + sw128_off(r, (col & 63) >> 3),
+                           make_uint4(w[0], w[1], w[2], w[3]));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_free[a]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&o_ready[os]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kNcMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, PL::TMEM_COLS);
+    }
 }
 
 // ------------------------------------------------------------ host side
@@ -1179,14 +1481,16 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode()
     return fn;
 }
 
-// 3-D map over a [BH, N, cols] bf16 tensor; box = 64 columns x 128 rows x 1 head,
-// 128-byte swizzle; rows past N read as zero.
-bool make_map(CUtensorMap *m, const void *base, long long BH, int N, int cols)
+// 3-D map over a [BH, N, cols] bf16 tensor whose rows are row_elems apart
+// (cols, the default, or wider: one column block of a wider tensor); box =
+// 64 columns x 128 rows x 1 head, 128-byte swizzle; rows past N read as zero.
+bool make_map(CUtensorMap *m, const void *base, long long BH, long long N, int cols, int row_elems = 0)
 {
     auto enc = get_encode();
     if (!enc) return false;
+    if (row_elems <= 0) row_elems = cols;
     cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)N, (cuuint64_t)BH};
-    cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)N * cols * 2};
+    cuuint64_t strides[2] = {(cuuint64_t)row_elems * 2, (cuuint64_t)N * row_elems * 2};
     cuuint32_t box[3] = {64, (cuuint32_t)kC, 1};
     cuuint32_t es[3] = {1, 1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
@@ -1223,6 +1527,7 @@ Geo plan(long long BH, int N, int sms)
     g.L = cdiv(g.NC, max(1, min(want, g.NC)));
     g.nseg = cdiv(g.NC, g.L);
     g.n_items = (int)(BH * g.nseg);
+    g.exp_rows = 0;
     return g;
 }
 
@@ -1259,43 +1564,64 @@ __global__ void seg_scan_kernel(float *__restrict__ preS, float *__restrict__ pr
     }
 }
 
+size_t up256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+// Control words (ticket, abort) and, when segmented, the segment sums.
 template <int DP, int DV>
-size_t scratch_bytes(const Geo &g)
+size_t seg_scratch_bytes(const Geo &g, bool every_segment)
 {
-    // ticket, abort word; then the segment sums / prefixes when segmented
-    return 16 + (g.nseg > 1 ? (size_t)g.BH * g.nseg * ((size_t)DP * DV + DP) * sizeof(float) : 0);
+    const bool seg = every_segment || g.nseg > 1;
+    return up256(16 + (seg ? (size_t)g.BH * g.nseg * ((size_t)DP * DV + DP) * sizeof(float) : 0));
 }
 
 template <int DP, int DV>
-cudaError_t run(const Problem &p, void *scratch, float *S_out, float *z_out, int *err,
-                cudaStream_t s)
+Scratch carve(void *scratch, const Geo &g)
 {
-    using PL = Plan<DP, DV>;
-    CUtensorMap tq, tk, tv, to;
-    if (!make_map(&tq, p.q, p.BH, p.N, p.D) || !make_map(&tk, p.k, p.BH, p.N, p.D) ||
-        !make_map(&tv, p.v, p.BH, p.N, p.Dv) || !make_map(&to, p.out, p.BH, p.N, p.Dv))
-        return cudaErrorInvalidValue;
-    const int sms = num_sms();
-    Geo g = plan(p.BH, p.N, sms);
     unsigned char *b = (unsigned char *)scratch;
     Scratch sc;
     sc.ticket = (int *)b;
     sc.abort = (int *)(b + 4);
     sc.preS = (float *)(b + 16);
     sc.prez = sc.preS + (size_t)g.BH * g.nseg * DP * DV;
+    sc.num_part = nullptr;
+    sc.den_part = nullptr;
+    return sc;
+}
+
+template <int DP, int DV, int MODE>
+cudaError_t set_smem()
+{
+    using PL = Plan<DP, DV>;
+    cudaError_t e = cudaFuncSetAttribute(tc_causal_kernel<DP, DV, true, MODE == kModeElu ? kModeElu : kModeFeat>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, PL::SMEM);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(tc_causal_kernel<DP, DV, false, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                PL::SMEM);
+}
+
+// The causal forward over prepared maps: when segmented, the segment-sum
+// pass, the scan and then the output pass; else the output pass alone.
+template <int DP, int DV, int MODE>
+cudaError_t run_causal(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &to,
+                       Geo g, void *scratch, float *num_part, float *den_part, void *out, float *S_out,
+                       float *z_out, int *err, cudaStream_t s)
+{
+    using PL = Plan<DP, DV>;
+    constexpr int AMODE = MODE == kModeElu ? kModeElu : kModeFeat;
+    const int sms = num_sms();
+    Scratch sc = carve<DP, DV>(scratch, g);
+    sc.num_part = num_part;
+    sc.den_part = den_part;
     cudaError_t e;
     int launches = 0;
+    if ((e = set_smem<DP, DV, MODE>()) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(scratch, 0, 16, s)) != cudaSuccess) return e;
     if (g.nseg > 1) {
         // pass 1: the sums of every segment but the last of each head; then the scan
         Geo ga = g;
         ga.n_items = g.BH * (g.nseg - 1);
-        if ((e = cudaFuncSetAttribute(tc_causal_kernel<DP, DV, true>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, PL::SMEM)) !=
-            cudaSuccess)
-            return e;
-        tc_causal_kernel<DP, DV, true><<<min(ga.n_items, sms), kThreads, PL::SMEM, s>>>(
-            tq, tk, tv, to, ga, sc, (__nv_bfloat16 *)p.out, nullptr, nullptr, err);
+        tc_causal_kernel<DP, DV, true, AMODE><<<min(ga.n_items, sms), kThreads, PL::SMEM, s>>>(
+            tq, tk, tv, to, ga, sc, (__nv_bfloat16 *)out, nullptr, nullptr, err);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         const int sz = DP * DV + DP;
         seg_scan_kernel<<<dim3(cdiv(sz, 256), (unsigned)g.BH), 256, 0, s>>>(sc.preS, sc.prez, g.nseg,
@@ -1305,63 +1631,185 @@ cudaError_t run(const Problem &p, void *scratch, float *S_out, float *z_out, int
         launches += 2;
     }
     // pass 2: the chunk recurrence of every segment from its prefix
-    if ((e = cudaFuncSetAttribute(tc_causal_kernel<DP, DV, false>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, PL::SMEM)) != cudaSuccess)
-        return e;
-    tc_causal_kernel<DP, DV, false><<<min(g.n_items, sms), kThreads, PL::SMEM, s>>>(
-        tq, tk, tv, to, g, sc, (__nv_bfloat16 *)p.out, S_out, z_out, err);
+    tc_causal_kernel<DP, DV, false, MODE><<<min(g.n_items, sms), kThreads, PL::SMEM, s>>>(
+        tq, tk, tv, to, g, sc, (__nv_bfloat16 *)out, S_out, z_out, err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     note_launches(launches + 1);
     return cudaSuccess;
 }
 
-template <int DP, int DV>
-cudaError_t run_nc(const Problem &p, void *scratch, float *S_out, float *z_out, int *err, cudaStream_t s)
+// Non-causal, first half: the segment-sum form over every segment, then the
+// per-head totals into rows [row_off, row_off + DP) of totS / totz, whose
+// heads hold tot_rows feature rows.
+template <int DP, int DV, int AMODE>
+cudaError_t run_totals(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &to,
+                       Geo g, void *scratch, float *totS, float *totz, int tot_rows, int row_off, int *err,
+                       cudaStream_t s)
 {
     using PL = Plan<DP, DV>;
+    const int sms = num_sms();
+    Scratch sc = carve<DP, DV>(scratch, g);
+    cudaError_t e;
+    if ((e = set_smem<DP, DV, AMODE>()) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(scratch, 0, 16, s)) != cudaSuccess) return e;
+    tc_causal_kernel<DP, DV, true, AMODE><<<min(g.n_items, sms), kThreads, PL::SMEM, s>>>(
+        tq, tk, tv, to, g, sc, nullptr, nullptr, nullptr, err);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int sz = DP * DV + DP;
+    nc_total_kernel<<<dim3(cdiv(sz, 256), (unsigned)g.BH), 256, 0, s>>>(
+        sc.preS, sc.prez, g.nseg, DP * DV, DP, totS, totz, tot_rows * DV, tot_rows, row_off * DV, row_off);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    note_launches(2);
+    return cudaSuccess;
+}
+
+// Non-causal, second half: out = phi(Q) S / phi(Q) z from the totals.
+template <int DP, int DV, bool PHI>
+cudaError_t run_readout(const CUtensorMap &tq, const CUtensorMap &to, Geo g, void *scratch, float *totS,
+                        float *totz, int *err, cudaStream_t s)
+{
     using NP = NcPlan<DP, DV>;
+    Scratch sc = carve<DP, DV>(scratch, g);
+    sc.preS = totS;
+    sc.prez = totz;
+    cudaError_t e;
+    if ((e = cudaMemsetAsync(scratch, 0, 16, s)) != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(nc_out_kernel<DP, DV, PHI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  NP::SMEM)) != cudaSuccess)
+        return e;
+    nc_out_kernel<DP, DV, PHI><<<min(g.n_items, num_sms()), kNcThreads, NP::SMEM, s>>>(tq, to, g, sc, err);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    note_launches(1);
+    return cudaSuccess;
+}
+
+cudaError_t export_totals(float *S_out, float *z_out, const float *totS, const float *totz, long long BH, int P,
+                          int Dv, cudaStream_t s)
+{
+    cudaError_t e = cudaSuccess;
+    if (S_out) e = cudaMemcpyAsync(S_out, totS, (size_t)BH * P * Dv * 4, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess && z_out) e = cudaMemcpyAsync(z_out, totz, (size_t)BH * P * 4, cudaMemcpyDeviceToDevice, s);
+    return e;
+}
+
+// ---- elu + 1 on q, k in the tile loads
+
+template <int DP, int DV>
+cudaError_t run_elu(const Problem &p, void *scratch, float *S_out, float *z_out, int *err, cudaStream_t s,
+                    bool causal)
+{
     CUtensorMap tq, tk, tv, to;
     if (!make_map(&tq, p.q, p.BH, p.N, p.D) || !make_map(&tk, p.k, p.BH, p.N, p.D) ||
         !make_map(&tv, p.v, p.BH, p.N, p.Dv) || !make_map(&to, p.out, p.BH, p.N, p.Dv))
         return cudaErrorInvalidValue;
-    const int sms = num_sms();
-    Geo g = plan(p.BH, p.N, sms);
-    unsigned char *b = (unsigned char *)scratch;
-    Scratch sc;
-    sc.ticket = (int *)b;
-    sc.abort = (int *)(b + 4);
-    sc.preS = (float *)(b + 16);
-    sc.prez = sc.preS + (size_t)g.BH * g.nseg * DP * DV;
+    Geo g = plan(p.BH, p.N, num_sms());
+    g.exp_rows = DP;
+    if (causal)
+        return run_causal<DP, DV, kModeElu>(tq, tk, tv, to, g, scratch, nullptr, nullptr, p.out, S_out, z_out,
+                                           err, s);
+    float *totS = (float *)((unsigned char *)scratch + seg_scratch_bytes<DP, DV>(g, true));
+    float *totz = totS + (size_t)g.BH * DP * DV;
+    cudaError_t e = run_totals<DP, DV, kModeElu>(tq, tk, tv, to, g, scratch, totS, totz, DP, 0, err, s);
+    if (e == cudaSuccess) e = run_readout<DP, DV, true>(tq, to, g, scratch, totS, totz, err, s);
+    if (e == cudaSuccess) e = export_totals(S_out, z_out, totS, totz, g.BH, DP, DV, s);
+    return e;
+}
+
+template <int DP, int DV>
+size_t elu_scratch_bytes(const Geo &g, bool causal)
+{
+    if (causal) return seg_scratch_bytes<DP, DV>(g, false);
+    return seg_scratch_bytes<DP, DV>(g, true) + (size_t)g.BH * ((size_t)DP * DV + DP) * sizeof(float);
+}
+
+// ---- random features: phi(q), phi(k) materialised in bf16, then the chunk
+// kernels on those tiles; m = 256 as two feature halves of 128
+
+struct PrfLayout {
+    size_t phi_q, phi_k, part, half, tot, total;
+};
+
+PrfLayout prf_layout(const Problem &p, const Geo &g, bool causal)
+{
+    const size_t R = (size_t)p.BH * p.N;
+    PrfLayout L;
+    L.phi_q = 0;
+    L.phi_k = up256(R * p.m * 2);
+    L.part = L.phi_k + up256(R * p.m * 2);
+    const size_t part = (causal && p.m == 256) ? up256(R * p.Dv * 4) + up256(R * 4) : 0;
+    L.half = L.part + part;
+    const size_t seg = p.Dv == 64 ? seg_scratch_bytes<128, 64>(g, !causal) : seg_scratch_bytes<128, 128>(g, !causal);
+    L.tot = L.half + seg;
+    L.total = L.tot + (causal ? 0 : up256((size_t)g.BH * ((size_t)p.m * p.Dv + p.m) * 4));
+    return L;
+}
+
+template <int M>
+cudaError_t run_prf_phi(const Problem &p, void *phq, void *phk, int *err, cudaStream_t s)
+{
+    using PP = PrfPlan<64, M>;
+    const long long R = p.BH * (long long)p.N;
+    CUtensorMap xq, xk, pq, pk;
+    if (!make_map(&xq, p.q, 1, R, 64) || !make_map(&xk, p.k, 1, R, 64) || !make_map(&pq, phq, 1, R, M) ||
+        !make_map(&pk, phk, 1, R, M))
+        return cudaErrorInvalidValue;
+    const int T = (int)((R + kC - 1) / kC);
     cudaError_t e;
-    if ((e = cudaMemsetAsync(scratch, 0, 16, s)) != cudaSuccess) return e;
-    // pass 1: phi(K)^T V and colsum phi(K) of every segment
-    if ((e = cudaFuncSetAttribute(tc_causal_kernel<DP, DV, true>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, PL::SMEM)) != cudaSuccess)
+    if ((e = cudaFuncSetAttribute(prf_phi_kernel<64, M>, cudaFuncAttributeMaxDynamicSharedMemorySize, PP::SMEM)) !=
+        cudaSuccess)
         return e;
-    tc_causal_kernel<DP, DV, true><<<min(g.n_items, sms), kThreads, PL::SMEM, s>>>(
-        tq, tk, tv, to, g, sc, (__nv_bfloat16 *)p.out, nullptr, nullptr, err);
+    const float log_scale = (float)(0.5 * std::log((double)M));
+    prf_phi_kernel<64, M><<<min(2 * T, num_sms()), kNcThreads, PP::SMEM, s>>>(xq, xk, pq, pk, p.W, T, log_scale,
+                                                                             err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const int sz = DP * DV + DP;
-    nc_total_kernel<<<dim3(cdiv(sz, 256), (unsigned)g.BH), 256, 0, s>>>(sc.preS, sc.prez, g.nseg, DP * DV,
-                                                                       DP);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(scratch, 0, 4, s)) != cudaSuccess) return e;   // ticket
-    // pass 2: the readout
-    if ((e = cudaFuncSetAttribute(nc_out_kernel<DP, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  NP::SMEM)) != cudaSuccess)
-        return e;
-    nc_out_kernel<DP, DV><<<min(g.n_items, sms), kNcThreads, NP::SMEM, s>>>(tq, to, g, sc, err);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    note_launches(3);
-    // the memories (the totals) for la_forward_ex
-    if (S_out &&
-        (e = cudaMemcpy2DAsync(S_out, (size_t)DP * DV * 4, sc.preS, (size_t)g.nseg * DP * DV * 4,
-                               (size_t)DP * DV * 4, g.BH, cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
-        return e;
-    if (z_out && (e = cudaMemcpy2DAsync(z_out, (size_t)DP * 4, sc.prez, (size_t)g.nseg * DP * 4, (size_t)DP * 4,
-                                        g.BH, cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
-        return e;
+    note_launches(1);
     return cudaSuccess;
+}
+
+template <int M, int DV>
+cudaError_t run_prf(const Problem &p, void *scratch, float *S_out, float *z_out, int *err, cudaStream_t s,
+                    bool causal)
+{
+    Geo g = plan(p.BH, p.N, num_sms());
+    const PrfLayout L = prf_layout(p, g, causal);
+    unsigned char *b = (unsigned char *)scratch;
+    void *phq = b + L.phi_q, *phk = b + L.phi_k;
+    cudaError_t e = run_prf_phi<M>(p, phq, phk, err, s);
+    if (e != cudaSuccess) return e;
+    // one map per 128-feature half of phi(q), phi(k)
+    CUtensorMap tq[2], tk[2], tv, to;
+    for (int f = 0; f < M / 128; f++)
+        if (!make_map(&tq[f], (const __nv_bfloat16 *)phq + 128 * f, p.BH, p.N, 128, M) ||
+            !make_map(&tk[f], (const __nv_bfloat16 *)phk + 128 * f, p.BH, p.N, 128, M))
+            return cudaErrorInvalidValue;
+    if (!make_map(&tv, p.v, p.BH, p.N, p.Dv) || !make_map(&to, p.out, p.BH, p.N, p.Dv)) return cudaErrorInvalidValue;
+    void *half = b + L.half;
+    g.exp_rows = M;
+    if (causal) {
+        if constexpr (M == 128) {
+            return run_causal<128, DV, kModeFeat>(tq[0], tk[0], tv, to, g, half, nullptr, nullptr, p.out, S_out,
+                                                  z_out, err, s);
+        } else {
+            float *num_part = (float *)(b + L.part);
+            float *den_part = (float *)(b + L.part + up256((size_t)p.BH * p.N * DV * 4));
+            e = run_causal<128, DV, kModeFeatPart>(tq[0], tk[0], tv, to, g, half, num_part, den_part, p.out, S_out,
+                                                   z_out, err, s);
+            if (e != cudaSuccess) return e;
+            return run_causal<128, DV, kModeFeatComb>(tq[1], tk[1], tv, to, g, half, num_part, den_part, p.out,
+                                                      S_out ? S_out + 128 * DV : nullptr,
+                                                      z_out ? z_out + 128 : nullptr, err, s);
+        }
+    }
+    float *totS = (float *)(b + L.tot);
+    float *totz = totS + (size_t)g.BH * M * DV;
+    for (int f = 0; f < M / 128; f++)
+        if ((e = run_totals<128, DV, kModeFeat>(tq[f], tk[f], tv, to, g, half, totS, totz, M, 128 * f, err, s)) !=
+            cudaSuccess)
+            return e;
+    CUtensorMap tqa;
+    if (!make_map(&tqa, phq, p.BH, p.N, M)) return cudaErrorInvalidValue;
+    if ((e = run_readout<M, DV, false>(tqa, to, g, half, totS, totz, err, s)) != cudaSuccess) return e;
+    return export_totals(S_out, z_out, totS, totz, g.BH, M, DV, s);
 }
 
 }  // namespace
@@ -1372,37 +1820,35 @@ bool tc_causal_supported(const Problem &p)
            (p.Dv == 64 || p.Dv == 128);
 }
 
-size_t tc_causal_scratch_bytes(const Problem &p)
+bool tc_prf_supported(const Problem &p)
+{
+    return p.dtype == DT_BF16 && p.kind == PHI_PRF && p.D == 64 &&
+           ((p.m == 128 && (p.Dv == 64 || p.Dv == 128)) || (p.m == 256 && p.Dv == 64)) &&
+           p.BH * (long long)p.N < (1LL << 31) - kC;
+}
+
+size_t tc_scratch_bytes(const Problem &p, bool causal)
 {
     Geo g = plan(p.BH, p.N, num_sms());
-    if (p.D == 64 && p.Dv == 64) return scratch_bytes<64, 64>(g);
-    if (p.D == 64 && p.Dv == 128) return scratch_bytes<64, 128>(g);
-    if (p.D == 128 && p.Dv == 64) return scratch_bytes<128, 64>(g);
-    return scratch_bytes<128, 128>(g);
+    if (p.kind == PHI_PRF) return prf_layout(p, g, causal).total;
+    if (p.D == 64 && p.Dv == 64) return elu_scratch_bytes<64, 64>(g, causal);
+    if (p.D == 64 && p.Dv == 128) return elu_scratch_bytes<64, 128>(g, causal);
+    if (p.D == 128 && p.Dv == 64) return elu_scratch_bytes<128, 64>(g, causal);
+    return elu_scratch_bytes<128, 128>(g, causal);
 }
 
-size_t tc_noncausal_scratch_bytes(const Problem &p)
+cudaError_t tc_forward(const Problem &p, bool causal, void *scratch, float *S_out, float *z_out, int *err,
+                       cudaStream_t s)
 {
-    Geo g = plan(p.BH, p.N, num_sms());
-    return 16 + (size_t)g.BH * g.nseg * ((size_t)p.P * p.Dv + p.P) * sizeof(float);
-}
-
-cudaError_t tc_noncausal(const Problem &p, void *scratch, float *S_out, float *z_out, int *err,
-                         cudaStream_t s)
-{
-    if (p.D == 64 && p.Dv == 64) return run_nc<64, 64>(p, scratch, S_out, z_out, err, s);
-    if (p.D == 64 && p.Dv == 128) return run_nc<64, 128>(p, scratch, S_out, z_out, err, s);
-    if (p.D == 128 && p.Dv == 64) return run_nc<128, 64>(p, scratch, S_out, z_out, err, s);
-    return run_nc<128, 128>(p, scratch, S_out, z_out, err, s);
-}
-
-cudaError_t tc_causal(const Problem &p, void *scratch, float *S_out, float *z_out, int *err,
-                      cudaStream_t s)
-{
-    if (p.D == 64 && p.Dv == 64) return run<64, 64>(p, scratch, S_out, z_out, err, s);
-    if (p.D == 64 && p.Dv == 128) return run<64, 128>(p, scratch, S_out, z_out, err, s);
-    if (p.D == 128 && p.Dv == 64) return run<128, 64>(p, scratch, S_out, z_out, err, s);
-    return run<128, 128>(p, scratch, S_out, z_out, err, s);
+    if (p.kind == PHI_PRF) {
+        if (p.m == 256) return run_prf<256, 64>(p, scratch, S_out, z_out, err, s, causal);
+        if (p.Dv == 64) return run_prf<128, 64>(p, scratch, S_out, z_out, err, s, causal);
+        return run_prf<128, 128>(p, scratch, S_out, z_out, err, s, causal);
+    }
+    if (p.D == 64 && p.Dv == 64) return run_elu<64, 64>(p, scratch, S_out, z_out, err, s, causal);
+    if (p.D == 64 && p.Dv == 128) return run_elu<64, 128>(p, scratch, S_out, z_out, err, s, causal);
+    if (p.D == 128 && p.Dv == 64) return run_elu<128, 64>(p, scratch, S_out, z_out, err, s, causal);
+    return run_elu<128, 128>(p, scratch, S_out, z_out, err, s, causal);
 }
 
 }  // namespace la

@@ -119,6 +119,34 @@ def test_causal_launch_plan(la):
         assert la.la_launch_count() - n0 == expect, (B, H, D)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("H,N,m,Dv", [(2, 128 * 21 + 77, 256, 64), (3, 128 * 13 + 5, 128, 128),
+                                      (1, 128 * 40, 128, 64)])
+def test_long_segment_chain_prf(la, H, N, m, Dv, causal):
+    """Random features on the tensor cores with few heads (many segments),
+    every head and position, the memories, and a ragged last chunk; m = 256
+    runs as two feature halves whose sums are added before the division."""
+    w = wl.small(B=1, H=H, N=N, D=64, Dv=Dv, causal=causal, feature="prf", m=m, seed=N + m)
+    err, _ = _forward_and_check(la, w)
+    assert err <= 2e-2
+
+
+def test_prf_launch_plan(la):
+    """m = 256, few heads: the projection, then per feature half the
+    segment-sum pass, the scan and the output pass (causal: 7 kernels), or
+    the segment-sum pass and the totals per half, then one readout
+    (non-causal: 6 kernels)."""
+    W = wl.make_W(256, 64).cuda()
+    fm = la.FeatureMap("prf", W)
+    w = wl.small(B=1, H=2, N=2048, D=64, Dv=64, feature="prf", m=256, seed=9)
+    q, k, v = (t.cuda() for t in wl.make_qkv(w))
+    for causal, expect in ((True, 7), (False, 6)):
+        n0 = la.la_launch_count()
+        la.la_forward(q, k, v, causal=causal, feature_map=fm)
+        torch.cuda.synchronize()
+        assert la.la_launch_count() - n0 == expect, causal
+
+
 def test_noncausal_launch_plan(la):
     """Non-causal bf16 elu+1 with D, Dv in {64, 128}: the segment-sum pass, the
     per-head total and the readout (three kernels); other shapes: the

@@ -52,6 +52,11 @@ SMALL = [
     (1025, 128, 128, 1, 1, "elu1", 0, "bf16", False),
     (300, 64, 64, 1, 2, "prf", 256, "bf16", False),
     (65, 32, 16, 1, 1, "prf", 32, "f32", False),
+    # random features on the tensor cores (phi materialised, m = 256 as two halves)
+    (1000, 64, 128, 1, 2, "prf", 128, "bf16", True),
+    (700, 64, 64, 2, 1, "prf", 128, "bf16", False),
+    (129, 64, 64, 1, 1, "prf", 256, "bf16", False),
+    (1, 64, 64, 1, 1, "prf", 256, "bf16", True),
 ]
 
 
