@@ -454,14 +454,17 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         const uint32_t ka = base + PL::K0 + st * PL::QB;
                         const uint32_t va = base + PL::V0 + st * PL::VB;
                         if (!*abort_cta) {
+                            // all N = Dv steps, then the narrow N = 16 ones (no shape switch per step)
 #pragma unroll
-                            for (int k = 0; k < kC; k += 16) {
-                                const uint64_t ad = sw128_desc(ka + (k / 8) * 1024, lbo_kT, 1024);
-                                const uint32_t acc = (c > 0 || k > 0) ? 1u : 0u;
-                                mma_bf16_ss(dS, ad, sw128_desc(va + (k / 8) * 1024, kC * 128, 1024), id_kv,
-                                            acc);
-                                mma_bf16_ss(dz, ad, sw32_desc(ones + (k / 8) * 256, 256, 256), id_k16, acc);
-                            }
+                            for (int k = 0; k < kC; k += 16)
+                                mma_bf16_ss(dS, sw128_desc(ka + (k / 8) * 1024, lbo_kT, 1024),
+                                            sw128_desc(va + (k / 8) * 1024, kC * 128, 1024), id_kv,
+                                            (c > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+                            for (int k = 0; k < kC; k += 16)
+                                mma_bf16_ss(dz, sw128_desc(ka + (k / 8) * 1024, lbo_kT, 1024),
+                                            sw32_desc(ones + (k / 8) * 256, 256, 256), id_k16,
+                                            (c > 0 || k > 0) ? 1u : 0u);
                         }
                         mma_commit(&k_empty[st]);
                         mma_commit(&v_empty[st]);
@@ -491,12 +494,15 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
                             for (int kk = 0; kk < PR; kk += 16) {
                                 const int kq = pc * PR + kk;
-                                const uint64_t ad =
-                                    sw128_desc(qa + (kq / 64) * (kC * 128) + (kq % 64) * 2, 16, 1024);
-                                mma_bf16_ss(rnum, ad, sw128_desc(s_addr + (kk / 8) * 1024, PR * 128, 1024),
-                                            id_qs, kq > 0 ? 1u : 0u);
-                                mma_bf16_ss(rden, ad, sw32_desc(zp_addr + (kq / 8) * 256, 256, 256), id_q16,
+                                mma_bf16_ss(rnum, sw128_desc(qa + (kq / 64) * (kC * 128) + (kq % 64) * 2, 16, 1024),
+                                            sw128_desc(s_addr + (kk / 8) * 1024, PR * 128, 1024), id_qs,
                                             kq > 0 ? 1u : 0u);
+                            }
+#pragma unroll
+                            for (int kk = 0; kk < PR; kk += 16) {
+                                const int kq = pc * PR + kk;
+                                mma_bf16_ss(rden, sw128_desc(qa + (kq / 64) * (kC * 128) + (kq % 64) * 2, 16, 1024),
+                                            sw32_desc(zp_addr + (kq / 8) * 256, 256, 256), id_q16, kq > 0 ? 1u : 0u);
                             }
                         }
                         if (pc + 1 < NSP) mma_commit(sp_free);
@@ -507,13 +513,13 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     tc_fence_after();
                     if (!*abort_cta) {
 #pragma unroll
-                        for (int kk = 0; kk < kC; kk += 16) {
-                            const uint64_t ad = sw128_desc(ka + (kk / 8) * 1024, lbo_kT, 1024);
-                            mma_bf16_ss(tmem + PL::T_S, ad, sw128_desc(va + (kk / 8) * 1024, kC * 128, 1024),
-                                        id_kv, 1u);
-                            mma_bf16_ss(tmem + PL::T_Z, ad, sw32_desc(ones + (kk / 8) * 256, 256, 256),
-                                        id_k16, 1u);
-                        }
+                        for (int kk = 0; kk < kC; kk += 16)
+                            mma_bf16_ss(tmem + PL::T_S, sw128_desc(ka + (kk / 8) * 1024, lbo_kT, 1024),
+                                        sw128_desc(va + (kk / 8) * 1024, kC * 128, 1024), id_kv, 1u);
+#pragma unroll
+                        for (int kk = 0; kk < kC; kk += 16)
+                            mma_bf16_ss(tmem + PL::T_Z, sw128_desc(ka + (kk / 8) * 1024, lbo_kT, 1024),
+                                        sw32_desc(ones + (kk / 8) * 256, 256, 256), id_k16, 1u);
                     }
                     mma_commit(s_done);
                     mma_commit(&k_empty[st]);
@@ -524,11 +530,13 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     tc_fence_after();
                     if (!*abort_cta) {
 #pragma unroll
-                        for (int kk = 0; kk < kC; kk += 16) {
-                            const uint32_t pa = tmem + PL::T_P + kk / 2;
-                            mma_bf16_ts(rnum, pa, sw128_desc(va + (kk / 8) * 1024, kC * 128, 1024), id_qs, 1u);
-                            mma_bf16_ts(rden, pa, sw32_desc(ones + (kk / 8) * 256, 256, 256), id_q16, 1u);
-                        }
+                        for (int kk = 0; kk < kC; kk += 16)
+                            mma_bf16_ts(rnum, tmem + PL::T_P + kk / 2, sw128_desc(va + (kk / 8) * 1024, kC * 128, 1024),
+                                        id_qs, 1u);
+#pragma unroll
+                        for (int kk = 0; kk < kC; kk += 16)
+                            mma_bf16_ts(rden, tmem + PL::T_P + kk / 2, sw32_desc(ones + (kk / 8) * 256, 256, 256),
+                                        id_q16, 1u);
                     }
                     mma_commit(num_full);
                     nq++;
@@ -587,8 +595,9 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const bool srow = qd * 32 < DP;   // warp-uniform: this warp's rows hold state rows
         const int piece = NSP == 1 ? 0 : qd / 2;   // S_prev piece of this warp's rows
         // Warps of the second S_prev piece write it only once MMA3 has read the
-        // first, and MMA3(c+1) also needs the epilogue of c: so they write
-        // their piece for chunk c + 1 after that epilogue.
+        // first, and MMA3(c+1) also needs their a_free(c+1): so they write their
+        // piece for chunk c + 1 after load_p(c + 1), between store_p(c + 1) and
+        // the epilogue of c.
         const bool late = NSP == 2 && piece == 1;
         const int prow = r - piece * PR;           // row inside the piece
         const uint32_t s_addr = base + PL::S0, zp_addr = base + PL::Z0;
@@ -775,6 +784,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
                 const bool ok = __all_sync(0xffffffffu, wait_bar(num_full, k & 1, ctl));
                 if (more) store_p(pk);
+                if (more && late) sprev_from_tmem();
                 tc_fence_after();
                 const uint32_t rn = tmem + lane_base + PL::T_R0 + (k & 1) * 128 + grp * HALF;
                 uint32_t d[16], n0[32], n1[32];
@@ -875,7 +885,6 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         z_out[(long long)h * g.exp_rows + r] = __uint_as_float(zv[0]);
                     }
                 }
-                if (more && late) sprev_from_tmem();
             }
             tc_fence_before();
         }
@@ -1081,14 +1090,14 @@ nc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     const uint32_t qa = base + PL::Q0 + st * PL::QB;
                     if (!*abort_cta) {
 #pragma unroll
-                        for (int kk = 0; kk < DP; kk += 16) {
-                            const uint64_t ad =
-                                sw128_desc(qa + (kk / 64) * (kC * 128) + (kk % 64) * 2, 16, 1024);
-                            mma_bf16_ss(tmem + rr * 128, ad, sw128_desc(s_addr + (kk / 8) * 1024, DP * 128, 1024),
-                                        id_qs, kk > 0 ? 1u : 0u);
-                            mma_bf16_ss(tmem + PL::T_DEN + rr * 16, ad, sw32_desc(zp_addr + (kk / 8) * 256, 256, 256),
-                                        id_q16, kk > 0 ? 1u : 0u);
-                        }
+                        for (int kk = 0; kk < DP; kk += 16)
+                            mma_bf16_ss(tmem + rr * 128, sw128_desc(qa + (kk / 64) * (kC * 128) + (kk % 64) * 2, 16, 1024),
+                                        sw128_desc(s_addr + (kk / 8) * 1024, DP * 128, 1024), id_qs, kk > 0 ? 1u : 0u);
+#pragma unroll
+                        for (int kk = 0; kk < DP; kk += 16)
+                            mma_bf16_ss(tmem + PL::T_DEN + rr * 16,
+                                        sw128_desc(qa + (kk / 64) * (kC * 128) + (kk % 64) * 2, 16, 1024),
+                                        sw32_desc(zp_addr + (kk / 8) * 256, 256, 256), id_q16, kk > 0 ? 1u : 0u);
                     }
                     mma_commit(&q_empty[st]);
                     mma_commit(&num_full[rr]);
