@@ -94,6 +94,12 @@ constexpr int kThreads = (kMmaWarp + 1) * 32;           // 512
 constexpr int kPrefetch = 1;                            // chunks of L2 prefetch ahead
 constexpr int kItemConsumers = kTmemWarps + kPhiWarps + 4;
 
+// Column-chunk split of the phi(K) work in the segment-sum form: phi warps
+// [0, kAggSplit1), TMEM warps of column half 0 [kAggSplit1, kAggSplit2),
+// of column half 1 [kAggSplit2, JR).
+template <int JR> constexpr int kAggSplit1 = JR - 2 * (JR / 3);
+template <int JR> constexpr int kAggSplit2 = JR - JR / 3;
+
 template <int DP, int DV>
 struct Plan {
     static constexpr int QB = kC * DP * 2;   // one Q or K chunk tile (bytes)
@@ -190,6 +196,24 @@ __device__ __forceinline__ uint32_t tile_off(int r, int j)
     return (uint32_t)(j >> 3) * (kC * 128) + sw128_off(r, j & 7);
 }
 
+// elu + 1 in place on 16 B chunks [J0, J1) of row r of a [kC x cols] tile;
+// rows marked `zero` (past the sequence end) become zero instead.
+template <int J0, int J1>
+__device__ __forceinline__ void phi_cols(uint32_t t, int r, bool zero)
+{
+#pragma unroll
+    for (int h = J0; h < J1; h += 8) {
+        constexpr int kMax = 8;
+        uint4 x[kMax];
+#pragma unroll
+        for (int j = 0; j < kMax; j++)
+            if (h + j < J1) x[j] = lds128(t + tile_off(r, h + j));
+#pragma unroll
+        for (int j = 0; j < kMax; j++)
+            if (h + j < J1) sts128(t + tile_off(r, h + j), zero ? make_uint4(0, 0, 0, 0) : phi_elu1_bf16x8(x[j]));
+    }
+}
+
 // One S_prev row block: 32 fp32 state values -> bf16 at row r, columns
 // [c0, c0 + 32) of an MN-major [PR x DV] piece (DV / 64 blocks of PR rows).
 template <int PR>
@@ -258,7 +282,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             mbar_init(&q_ready[i], kTmemWarps);
             mbar_init(&q_empty[i], 1);
             mbar_init(&k_full[i], 1);
-            mbar_init(&k_ready[i], kPhiWarps);
+            mbar_init(&k_ready[i], AGG && kPhi ? kPhiWarps + kTmemWarps : kPhiWarps);
             mbar_init(&k_empty[i], 1);
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
@@ -559,15 +583,8 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             wait_bar(&full[st], (n / NS) & 1, ctl);
             const uint32_t t = ring + st * PL::QB;
             if constexpr (kPhi) {   // (phi tiles arrive from HBM as they are; rows past N are zero-filled)
-#pragma unroll
-                for (int h8 = 0; h8 < JR; h8 += 8) {
-                    uint4 x[8];
-#pragma unroll
-                    for (int j = 0; j < 8; j++) x[j] = lds128(t + tile_off(r, h8 + j));
-#pragma unroll
-                    for (int j = 0; j < 8; j++)
-                        sts128(t + tile_off(r, h8 + j), zero ? make_uint4(0, 0, 0, 0) : phi_elu1_bf16x8(x[j]));
-                }
+                // segment-sum form: the idle TMEM warps take the other two thirds of the columns
+                phi_cols<0, AGG ? kAggSplit1<JR> : JR>(t, r, zero);
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -602,6 +619,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const int prow = r - piece * PR;           // row inside the piece
         const uint32_t s_addr = base + PL::S0, zp_addr = base + PL::Z0;
         uint32_t kg = 0;      // global index of the next chunk whose A is read
+        uint32_t nkt = 0;     // K ring position (segment-sum form: this warp's share of phi(K))
         uint32_t nvr = 0;     // V ring position (phase A and C tiles)
         uint32_t nsp = 0;     // S_prev copies made (one per chunk)
         uint32_t nsd = 0;     // s_done phases consumed
@@ -700,6 +718,24 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const int c0 = s * g.L, nc = min(g.L, g.NC - c0);
             const long long slot_id = (long long)h * g.nseg + s;   // this (head, segment) in scratch
             if constexpr (AGG) {
+                if constexpr (kPhi) {
+                    // their share of phi(K) on the segment's K tiles (the phi warps do the rest)
+                    constexpr int JR = DP / 8;
+                    for (int c = 0; c < nc; c++) {
+                        const int st = nkt % NS;
+                        wait_bar(&k_full[st], (nkt / NS) & 1, ctl);
+                        const uint32_t t = base + PL::K0 + st * PL::QB;
+                        const bool zero = r >= g.N - (c0 + c) * kC;
+                        if (grp == 0)
+                            phi_cols<kAggSplit1<JR>, kAggSplit2<JR>>(t, r, zero);
+                        else
+                            phi_cols<kAggSplit2<JR>, JR>(t, r, zero);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&k_ready[st]);
+                        nkt++;
+                    }
+                }
                 // the segment's sums (region it % 2 and its denominator slot) -> scratch
                 const int rr = it & 1;
                 wait_bar(sloc_done, it & 1, ctl);
@@ -776,6 +812,14 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const int row0 = (c0 + c) * kC;
                 const bool more = c + 1 < nc;
                 bool sd = true;
+                if constexpr (MODE == kModeFeatComb) {
+                    // the first half's sums for this chunk's rows: into L2 now, read at the epilogue
+                    if (row0 + r < g.N) {
+                        const long long pr = (long long)h * g.N + row0 + r;
+                        prefetch_l2(sc.num_part + pr * DV + grp * HALF);
+                        if (grp == 0 && lane == 0) prefetch_l2(sc.den_part + pr);
+                    }
+                }
                 if (more) {
                     phi_q();
                     wait_sdone();
