@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace la {
 
 // Input/output element types.
@@ -31,5 +33,21 @@ __device__ __forceinline__ float phi_elu1(float x) { return x > 0.f ? x + 1.f : 
 __device__ __forceinline__ float phi_elu1_fast(float x) { return x > 0.f ? x + 1.f : __expf(x); }
 
 __host__ __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per kernel and
+// device (bit d of the mask: device d < 64; others set it on every call),
+// so that a forward call does not pay for it again.
+template <auto Kernel>
+cudaError_t set_max_smem_once(int bytes)
+{
+    static std::atomic<unsigned long long> done{0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
 
 }  // namespace la

@@ -147,12 +147,10 @@ cudaError_t launch(const Problem &p, float *KV, float *ks, cudaStream_t s)
     size_t sm1 = ((size_t)p.P * p.Dv + p.P + (size_t)kC * p.P + (size_t)kC * p.Dv + kC) * 4;
     size_t sm2 = ((size_t)p.P * p.Dv + p.P + (size_t)kC * p.P + 2 * kC) * 4;
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(nc_kv_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)sm1)) != cudaSuccess)
-        return e;
-    if ((e = cudaFuncSetAttribute(nc_out_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)sm2)) != cudaSuccess)
-        return e;
+    // the opt-in limit once, at the largest size any launch of these kernels asks for
+    if ((e = set_max_smem_once<nc_kv_kernel<T>>(227 * 1024)) != cudaSuccess) return e;
+    if ((e = set_max_smem_once<nc_out_kernel<T>>(227 * 1024)) != cudaSuccess) return e;
+    if (sm1 > 227 * 1024 || sm2 > 227 * 1024) return cudaErrorInvalidValue;
     nc_kv_kernel<T><<<dim3((unsigned)p.BH, splits), kThreads, sm1, s>>>(
         (const T *)p.k, (const T *)p.v, p.N, p.D, p.Dv, p.P, p.kind, p.W, rows_per, KV, ks);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

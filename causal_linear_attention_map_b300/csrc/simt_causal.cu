@@ -175,8 +175,8 @@ cudaError_t launch(const Problem &p, float *S_out, float *z_out, cudaStream_t s)
         L = simt_layout(p.P, p.Dv, C);
     }
     auto kern = simt_causal_kernel<T>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)L.total);
+    if (L.total > 227 * 1024) return cudaErrorInvalidValue;
+    cudaError_t e = set_max_smem_once<simt_causal_kernel<T>>(227 * 1024);
     if (e != cudaSuccess) return e;
     kern<<<(unsigned)p.BH, kThreads, L.total, s>>>(
         (const T *)p.q, (const T *)p.k, (const T *)p.v, (T *)p.out, p.N, p.D, p.Dv, p.P, C,

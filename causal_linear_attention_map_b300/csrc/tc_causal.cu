@@ -1645,11 +1645,9 @@ template <int DP, int DV, int MODE>
 cudaError_t set_smem()
 {
     using PL = Plan<DP, DV>;
-    cudaError_t e = cudaFuncSetAttribute(tc_causal_kernel<DP, DV, true, MODE == kModeElu ? kModeElu : kModeFeat>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, PL::SMEM);
+    cudaError_t e = set_max_smem_once<tc_causal_kernel<DP, DV, true, MODE == kModeElu ? kModeElu : kModeFeat>>(PL::SMEM);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(tc_causal_kernel<DP, DV, false, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                PL::SMEM);
+    return set_max_smem_once<tc_causal_kernel<DP, DV, false, MODE>>(PL::SMEM);
 }
 
 // The causal forward over prepared maps: when segmented, the segment-sum
@@ -1727,8 +1725,7 @@ cudaError_t run_readout(const CUtensorMap &tq, const CUtensorMap &to, Geo g, voi
     sc.prez = totz;
     cudaError_t e;
     if ((e = cudaMemsetAsync(scratch, 0, 16, s)) != cudaSuccess) return e;
-    if ((e = cudaFuncSetAttribute(nc_out_kernel<DP, DV, PHI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  NP::SMEM)) != cudaSuccess)
+    if ((e = set_max_smem_once<nc_out_kernel<DP, DV, PHI>>(NP::SMEM)) != cudaSuccess)
         return e;
     nc_out_kernel<DP, DV, PHI><<<min(g.n_items, num_sms()), kNcThreads, NP::SMEM, s>>>(tq, to, g, sc, err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -1808,8 +1805,7 @@ cudaError_t run_prf_phi(const Problem &p, void *phq, void *phk, int *err, cudaSt
         return cudaErrorInvalidValue;
     const int T = (int)((R + kC - 1) / kC);
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(prf_phi_kernel<64, M>, cudaFuncAttributeMaxDynamicSharedMemorySize, PP::SMEM)) !=
-        cudaSuccess)
+    if ((e = set_max_smem_once<prf_phi_kernel<64, M>>(PP::SMEM)) != cudaSuccess)
         return e;
     const float log_scale = (float)(0.5 * std::log((double)M));
     prf_phi_kernel<64, M><<<min(2 * T, num_sms()), kNcThreads, PP::SMEM, s>>>(xq, xk, pq, pk, p.W, T, log_scale,
