@@ -103,19 +103,34 @@ template <int JR> constexpr int kAggSplit2 = JR - JR / 3;
 template <int DP, int DV>
 struct Plan {
     static constexpr int QB = kC * DP * 2;   // one Q or K chunk tile (bytes)
-    static constexpr int VB = kC * DV * 2;   // one V chunk tile
-    static constexpr int ZB = DP * 32;       // ZP [DP x 16] bf16, 32-byte swizzle
-    static constexpr int OB = kC * 32;       // ONES [C x 16]
     static constexpr int kBudget = 227 * 1024 - 2048;
+    // Fused side products: every V slot carries a constant ONES block after
+    // its DV / 64 blocks and the S_prev buffer a z block after its own, so
+    // that z, rowsum(P) and phi(Q).z_prev ride on the N = DV products as
+    // N = DV + 16 (DV + 16 <= 128 so that NUM | DEN fits one TMEM region).
+    // Taken when the larger slots still leave two-deep rings.
+    static constexpr int VB_F = kC * (DV + 64) * 2;
+    static constexpr int SB_F = DP * (DV + 64) * 2;
+    static constexpr int NS_F = (SB_F + 4 * (2 * QB + VB_F) <= kBudget)   ? 4
+                                : (SB_F + 3 * (2 * QB + VB_F) <= kBudget) ? 3
+                                : (SB_F + 2 * (2 * QB + VB_F) <= kBudget) ? 2
+                                                                           : 0;
+    static constexpr bool FUSED = DV + 16 <= 128 && NS_F >= 2;
+    static constexpr int VB = FUSED ? VB_F : kC * DV * 2;   // one V chunk slot
+    static constexpr int ZB = FUSED ? 0 : DP * 32;          // ZP [DP x 16] bf16, 32-byte swizzle
+    static constexpr int OB = FUSED ? 0 : kC * 32;          // ONES [C x 16]
     // S_prev pieces along Dphi: one, or two 64-row halves when that is what
     // lets two-deep rings fit
-    static constexpr int NSP = (2 * (2 * QB + VB) + DP * DV * 2 + ZB + OB <= kBudget) ? 1 : 2;
+    static constexpr int NSP =
+        FUSED ? 1 : (2 * (2 * QB + VB) + DP * DV * 2 + ZB + OB <= kBudget) ? 1 : 2;
     static constexpr int PR = DP / NSP;      // S_prev rows per piece
-    static constexpr int SB = PR * DV * 2;
+    static constexpr int SB = FUSED ? SB_F : PR * DV * 2;
     static constexpr int kFixed = SB + ZB + OB;
-    static constexpr int NS = (kFixed + 4 * (2 * QB + VB) <= kBudget)   ? 4
+    static constexpr int NS = FUSED ? NS_F
+                              : (kFixed + 4 * (2 * QB + VB) <= kBudget)   ? 4
                               : (kFixed + 3 * (2 * QB + VB) <= kBudget) ? 3
                                                                          : 2;
+    static constexpr int NQ16 = FUSED ? DV + 16 : DV;   // N of the products that carry the side sums
     static constexpr int Q0 = 0;
     static constexpr int K0 = Q0 + NS * QB;
     static constexpr int V0 = K0 + NS * QB;
@@ -240,6 +255,16 @@ __device__ __forceinline__ void zp_store(uint32_t zp, int r, float z)
     sts128(zp + sw32_off(r, 1), make_uint4(l, l, l, l));
 }
 
+// z (fp32) -> row r of the z block that follows S_prev in the fused layout
+// (128-byte swizzle): columns 0-7 bf16(z), 8-15 bf16(z - bf16(z)).
+__device__ __forceinline__ void zblk_store(uint32_t zb, int r, float z)
+{
+    const float hi = __bfloat162float(__float2bfloat16_rn(z));
+    const uint32_t h = pack_bf16x2(hi, hi), l = pack_bf16x2(z - hi, z - hi);
+    sts128(zb + sw128_off(r, 0), make_uint4(h, h, h, h));
+    sts128(zb + sw128_off(r, 1), make_uint4(l, l, l, l));
+}
+
 // ---------------------------------------------------------------- kernel
 
 template <int DP, int DV, bool AGG, int MODE>
@@ -308,12 +333,21 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         *abort_cta = 0;
         fence_mbar_init();
     }
-    if (warp < kTmemWarps) {   // the constant ONES tile (bar + 47 .. 48: sloc_read)
+    if (warp < kTmemWarps) {   // the constant ONES tile(s): columns 0-7 one, 8-15 zero
         const uint32_t one = pack_bf16x2(1.f, 1.f);
-        const uint32_t ones = base + PL::O0;
-        for (int r = threadIdx.x; r < kC; r += kTmemWarps * 32) {
-            sts128(ones + sw32_off(r, 0), make_uint4(one, one, one, one));
-            sts128(ones + sw32_off(r, 1), make_uint4(0, 0, 0, 0));
+        if constexpr (PL::FUSED) {   // a block after every V slot's DV / 64 blocks (never loaded over)
+            for (int i = threadIdx.x; i < NS * kC; i += kTmemWarps * 32) {
+                const int st = i / kC, r = i % kC;
+                const uint32_t blk = base + PL::V0 + st * PL::VB + (DV / 64) * (kC * 128);
+                sts128(blk + sw128_off(r, 0), make_uint4(one, one, one, one));
+                sts128(blk + sw128_off(r, 1), make_uint4(0, 0, 0, 0));
+            }
+        } else {
+            const uint32_t ones = base + PL::O0;
+            for (int r = threadIdx.x; r < kC; r += kTmemWarps * 32) {
+                sts128(ones + sw32_off(r, 0), make_uint4(one, one, one, one));
+                sts128(ones + sw32_off(r, 1), make_uint4(0, 0, 0, 0));
+            }
         }
         fence_proxy_async_smem();
     }
@@ -332,7 +366,9 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const int role = warp - kProducerWarp;   // 0 Q, 1 K, 2 V
             const CUtensorMap *tm = role == 0 ? &tm_q : role == 1 ? &tm_k : &tm_v;
             const int nb = role == 2 ? DV / 64 : DP / 64;   // 64-column boxes per tile
-            const int tb = role == 2 ? PL::VB : PL::QB;     // tile bytes
+            const int tb = role == 2 ? PL::VB : PL::QB;     // slot stride in the ring
+            const int tx = role == 2 ? kC * DV * 2 : PL::QB;  // bytes one tile load brings (a fused V
+                                                            // slot also holds the constant ONES block)
             unsigned char *ring = gbase + (role == 0 ? PL::Q0 : role == 1 ? PL::K0 : PL::V0);
             uint64_t *full = role == 0 ? q_full : role == 1 ? k_full : v_full;
             uint64_t *empty = role == 0 ? q_empty : role == 1 ? k_empty : v_empty;
@@ -346,7 +382,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             auto load = [&](int head, int chunk, uint64_t pol) {
                 const int st = n % NS;
                 if (n >= NS && !wait_bar(&empty[st], ((n / NS) - 1) & 1, ctl)) return false;
-                mbar_arrive_expect_tx(&full[st], tb);
+                mbar_arrive_expect_tx(&full[st], tx);
                 for (int b = 0; b < nb; b++)
                     tma_load_3d_hint(ring + st * tb + b * kC * 128, tm, &full[st], b * 64, chunk * kC,
                                      head, pol);
@@ -417,10 +453,12 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t id_qk = idesc_bf16(128, kC, 0, 0);
-            constexpr uint32_t id_qs = idesc_bf16(128, DV, 0, 1);
+            // (fused layout: N = DV + 16 carries the z / denominator columns)
+            constexpr uint32_t id_qs = idesc_bf16(128, PL::NQ16, 0, 1);
             constexpr uint32_t id_q16 = idesc_bf16(128, 16, 0, 1);
-            constexpr uint32_t id_kv = idesc_bf16(128, DV, 1, 1);
+            constexpr uint32_t id_kv = idesc_bf16(128, PL::NQ16, 1, 1);
             constexpr uint32_t id_k16 = idesc_bf16(128, 16, 1, 1);
+            constexpr bool kSide = !PL::FUSED;   // separate N = 16 side products
             constexpr uint32_t lbo_kT = DP == 128 ? kC * 128 : 0;   // DP = 64: rows 64-127 repeat 0-63
             const uint32_t s_addr = base + PL::S0, zp_addr = base + PL::Z0, ones = base + PL::O0;
             uint32_t nkv = 0;    // K / V ring loads consumed (phase A and C)
@@ -484,11 +522,13 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                 mma_bf16_ss(dS, sw128_desc(ka + (k / 8) * 1024, lbo_kT, 1024),
                                             sw128_desc(va + (k / 8) * 1024, kC * 128, 1024), id_kv,
                                             (c > 0 || k > 0) ? 1u : 0u);
+                            if constexpr (kSide) {
 #pragma unroll
-                            for (int k = 0; k < kC; k += 16)
-                                mma_bf16_ss(dz, sw128_desc(ka + (k / 8) * 1024, lbo_kT, 1024),
-                                            sw32_desc(ones + (k / 8) * 256, 256, 256), id_k16,
-                                            (c > 0 || k > 0) ? 1u : 0u);
+                                for (int k = 0; k < kC; k += 16)
+                                    mma_bf16_ss(dz, sw128_desc(ka + (k / 8) * 1024, lbo_kT, 1024),
+                                                sw32_desc(ones + (k / 8) * 256, 256, 256), id_k16,
+                                                (c > 0 || k > 0) ? 1u : 0u);
+                            }
                         }
                         mma_commit(&k_empty[st]);
                         mma_commit(&v_empty[st]);
@@ -522,11 +562,15 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                             sw128_desc(s_addr + (kk / 8) * 1024, PR * 128, 1024), id_qs,
                                             kq > 0 ? 1u : 0u);
                             }
+                            if constexpr (kSide) {
 #pragma unroll
-                            for (int kk = 0; kk < PR; kk += 16) {
-                                const int kq = pc * PR + kk;
-                                mma_bf16_ss(rden, sw128_desc(qa + (kq / 64) * (kC * 128) + (kq % 64) * 2, 16, 1024),
-                                            sw32_desc(zp_addr + (kq / 8) * 256, 256, 256), id_q16, kq > 0 ? 1u : 0u);
+                                for (int kk = 0; kk < PR; kk += 16) {
+                                    const int kq = pc * PR + kk;
+                                    mma_bf16_ss(rden,
+                                                sw128_desc(qa + (kq / 64) * (kC * 128) + (kq % 64) * 2, 16, 1024),
+                                                sw32_desc(zp_addr + (kq / 8) * 256, 256, 256), id_q16,
+                                                kq > 0 ? 1u : 0u);
+                                }
                             }
                         }
                         if (pc + 1 < NSP) mma_commit(sp_free);
@@ -540,10 +584,12 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         for (int kk = 0; kk < kC; kk += 16)
                             mma_bf16_ss(tmem + PL::T_S, sw128_desc(ka + (kk / 8) * 1024, lbo_kT, 1024),
                                         sw128_desc(va + (kk / 8) * 1024, kC * 128, 1024), id_kv, 1u);
+                        if constexpr (kSide) {
 #pragma unroll
-                        for (int kk = 0; kk < kC; kk += 16)
-                            mma_bf16_ss(tmem + PL::T_Z, sw128_desc(ka + (kk / 8) * 1024, lbo_kT, 1024),
-                                        sw32_desc(ones + (kk / 8) * 256, 256, 256), id_k16, 1u);
+                            for (int kk = 0; kk < kC; kk += 16)
+                                mma_bf16_ss(tmem + PL::T_Z, sw128_desc(ka + (kk / 8) * 1024, lbo_kT, 1024),
+                                            sw32_desc(ones + (kk / 8) * 256, 256, 256), id_k16, 1u);
+                        }
                     }
                     mma_commit(s_done);
                     mma_commit(&k_empty[st]);
@@ -557,10 +603,12 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         for (int kk = 0; kk < kC; kk += 16)
                             mma_bf16_ts(rnum, tmem + PL::T_P + kk / 2, sw128_desc(va + (kk / 8) * 1024, kC * 128, 1024),
                                         id_qs, 1u);
+                        if constexpr (kSide) {
 #pragma unroll
-                        for (int kk = 0; kk < kC; kk += 16)
-                            mma_bf16_ts(rden, tmem + PL::T_P + kk / 2, sw32_desc(ones + (kk / 8) * 256, 256, 256),
-                                        id_q16, 1u);
+                            for (int kk = 0; kk < kC; kk += 16)
+                                mma_bf16_ts(rden, tmem + PL::T_P + kk / 2, sw32_desc(ones + (kk / 8) * 256, 256, 256),
+                                            id_q16, 1u);
+                        }
                     }
                     mma_commit(num_full);
                     nq++;
@@ -642,7 +690,10 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     uint32_t zv[16];
                     tmem_ld16_nowait(tmem + lane_base + PL::T_Z, zv);
                     tmem_ld_wait();
-                    zp_store(zp_addr, r, __uint_as_float(zv[0]));
+                    if constexpr (PL::FUSED)
+                        zblk_store(s_addr + (DV / 64) * (PR * 128), r, __uint_as_float(zv[0]));
+                    else
+                        zp_store(zp_addr, r, __uint_as_float(zv[0]));
                 }
             }
             fence_proxy_async_smem();
@@ -756,7 +807,8 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     }
                     if (grp == 0) {
                         uint32_t d[16];
-                        tmem_ld16_nowait(tmem + lane_base + PL::T_DEN0 + rr * 16, d);
+                        // z of the segment: the DEN slot, or (fused) the columns after S in the region
+                        tmem_ld16_nowait(tmem + lane_base + (PL::FUSED ? PL::T_R0 + rr * 128 + DV : PL::T_DEN0 + rr * 16), d);
                         tmem_ld_wait();
                         __stcg(sc.prez + slot_id * DP + r, __uint_as_float(d[0]));
                     }
@@ -832,7 +884,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 tc_fence_after();
                 const uint32_t rn = tmem + lane_base + PL::T_R0 + (k & 1) * 128 + grp * HALF;
                 uint32_t d[16], n0[32], n1[32];
-                tmem_ld16_nowait(tmem + lane_base + PL::T_DEN0 + (k & 1) * 16, d);
+                tmem_ld16_nowait(tmem + lane_base + (PL::FUSED ? PL::T_R0 + (k & 1) * 128 + DV : PL::T_DEN0 + (k & 1) * 16), d);
                 tmem_ld32_nowait(rn, n0);
                 if constexpr (HALF == 64) tmem_ld32_nowait(rn + 32, n1);
                 tmem_ld_wait();
