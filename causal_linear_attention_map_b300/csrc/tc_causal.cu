@@ -104,33 +104,26 @@ template <int DP, int DV>
 struct Plan {
     static constexpr int QB = kC * DP * 2;   // one Q or K chunk tile (bytes)
     static constexpr int kBudget = 227 * 1024 - 2048;
-    // Fused side products: every V slot carries a constant ONES block after
-    // its DV / 64 blocks and the S_prev buffer a z block after its own, so
-    // that z, rowsum(P) and phi(Q).z_prev ride on the N = DV products as
-    // N = DV + 16 (DV + 16 <= 128 so that NUM | DEN fits one TMEM region).
-    // Taken when the larger slots still leave two-deep rings.
-    static constexpr int VB_F = kC * (DV + 64) * 2;
-    static constexpr int SB_F = DP * (DV + 64) * 2;
-    static constexpr int NS_F = (SB_F + 4 * (2 * QB + VB_F) <= kBudget)   ? 4
-                                : (SB_F + 3 * (2 * QB + VB_F) <= kBudget) ? 3
-                                : (SB_F + 2 * (2 * QB + VB_F) <= kBudget) ? 2
-                                                                           : 0;
-    static constexpr bool FUSED = DV + 16 <= 128 && NS_F >= 2;
-    static constexpr int VB = FUSED ? VB_F : kC * DV * 2;   // one V chunk slot
-    static constexpr int ZB = FUSED ? 0 : DP * 32;          // ZP [DP x 16] bf16, 32-byte swizzle
-    static constexpr int OB = FUSED ? 0 : kC * 32;          // ONES [C x 16]
+    // V tiles and S_prev are stored in 32-byte swizzle, as blocks of 16
+    // columns: a V slot is followed by a constant ONES block [C x 16]
+    // (columns 0-7 one, 8-15 zero) and S_prev by a z block [rows x 16]
+    // (bf16 z | z - bf16(z)).  The MMAs that read V or S_prev then run with
+    // N = DV + 16 and leave z, rowsum(P) and phiQ . z_prev in the 16 columns
+    // after S or NUM: no separate narrow products (one tcgen05.mma costs
+    // about the same for N = 16 as for N = 144 with these operands).
+    static constexpr int NQ16 = DV + 16;
+    static constexpr int VB = kC * NQ16 * 2;   // one V slot: DV / 16 blocks + ONES
     // S_prev pieces along Dphi: one, or two 64-row halves when that is what
-    // lets two-deep rings fit
-    static constexpr int NSP =
-        FUSED ? 1 : (2 * (2 * QB + VB) + DP * DV * 2 + ZB + OB <= kBudget) ? 1 : 2;
+    // lets two-deep rings fit (each piece with its own z block)
+    static constexpr int NSP = (2 * (2 * QB + VB) + DP * NQ16 * 2 <= kBudget) ? 1 : 2;
     static constexpr int PR = DP / NSP;      // S_prev rows per piece
-    static constexpr int SB = FUSED ? SB_F : PR * DV * 2;
-    static constexpr int kFixed = SB + ZB + OB;
-    static constexpr int NS = FUSED ? NS_F
-                              : (kFixed + 4 * (2 * QB + VB) <= kBudget)   ? 4
+    static constexpr int SB = PR * NQ16 * 2;
+    static constexpr int ZB = 0, OB = 0;     // (inside the V slots and the S_prev buffer)
+    static constexpr int kFixed = SB;
+    static constexpr int NS = (kFixed + 4 * (2 * QB + VB) <= kBudget)   ? 4
                               : (kFixed + 3 * (2 * QB + VB) <= kBudget) ? 3
                                                                          : 2;
-    static constexpr int NQ16 = FUSED ? DV + 16 : DV;   // N of the products that carry the side sums
+    static_assert(kFixed + 2 * (2 * QB + VB) <= kBudget, "no two-deep rings");
     static constexpr int Q0 = 0;
     static constexpr int K0 = Q0 + NS * QB;
     static constexpr int V0 = K0 + NS * QB;
@@ -139,9 +132,15 @@ struct Plan {
     static constexpr int O0 = Z0 + ZB;
     static constexpr int TILES = O0 + OB;
     static constexpr int SMEM = TILES + 1024 /* alignment */ + 1024 /* barriers */;
-    // TMEM columns: state S, z; the denominators of the two regions; the
-    // regions R0, R1 (A then NUM of alternate chunks); the bf16 P
-    static constexpr int T_S = 0, T_Z = DV, T_DEN0 = DV + 16, T_R0 = DV + 64, T_P = DV + 320;
+    // TMEM columns: state S | z; the regions R0, R1 (A, then NUM | DEN of
+    // alternate chunks); the bf16 P.  Region stride: A (128 columns), then
+    // NUM | DEN (DV + 16)
+    static constexpr int RS = NQ16 > kC ? NQ16 : kC;
+    static constexpr int T_S = 0, T_Z = DV;                // S | z
+    static constexpr int T_R0 = DV == 128 ? 144 : DV + 64;  // regions R0, R1
+    static constexpr int T_P = T_R0 + 2 * RS;               // the bf16 P
+    // 32-column TMEM accesses at multiples of 32 use one x32 op, else two x16
+    static constexpr bool ALN32 = T_R0 % 32 == 0 && RS % 32 == 0 && T_P % 32 == 0;
     static constexpr int TMEM_COLS = 512;
     static_assert(T_P + kC / 2 <= TMEM_COLS, "TMEM plan too large");
     static_assert(SMEM <= 227 * 1024, "shared memory plan too large");
@@ -246,6 +245,41 @@ __device__ __forceinline__ void sprev_store32(uint32_t st, int r, int c0, const 
     }
 }
 
+// The same in 32-byte swizzle: blocks of 16 columns, PR * 32 bytes apart.
+template <int PR>
+__device__ __forceinline__ void sprev_store32_sw32(uint32_t st, int r, int c0, const uint32_t (&v)[32])
+{
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        const int col = c0 + 8 * j;
+        const uint32_t a = st + (uint32_t)(col >> 4) * (PR * 32) + sw32_off(r, (col >> 3) & 1);
+        sts128(a, make_uint4(
+                      pack_bf16x2(__uint_as_float(v[8 * j]), __uint_as_float(v[8 * j + 1])),
+                      pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+                      pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+                      pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]))));
+    }
+}
+
+// 32 TMEM columns from a 16-aligned column address (one x32 access when the
+// plan keeps it 32-aligned, else two x16).
+template <bool A32>
+__device__ __forceinline__ void tmem_ld32c(uint32_t taddr, uint32_t (&r)[32])
+{
+    if constexpr (A32)
+        tmem_ld32_nowait(taddr, r);
+    else
+        tmem_ld32x2_nowait(taddr, r);
+}
+template <bool A32>
+__device__ __forceinline__ void tmem_st32c(uint32_t taddr, const uint32_t (&r)[32])
+{
+    if constexpr (A32)
+        tmem_st32_nowait(taddr, r);
+    else
+        tmem_st32x2_nowait(taddr, r);
+}
+
 // z (fp32) -> one row of ZP: columns 0-7 bf16(z), 8-15 bf16(z - bf16(z)).
 __device__ __forceinline__ void zp_store(uint32_t zp, int r, float z)
 {
@@ -253,16 +287,6 @@ __device__ __forceinline__ void zp_store(uint32_t zp, int r, float z)
     const uint32_t h = pack_bf16x2(hi, hi), l = pack_bf16x2(z - hi, z - hi);
     sts128(zp + sw32_off(r, 0), make_uint4(h, h, h, h));
     sts128(zp + sw32_off(r, 1), make_uint4(l, l, l, l));
-}
-
-// z (fp32) -> row r of the z block that follows S_prev in the fused layout
-// (128-byte swizzle): columns 0-7 bf16(z), 8-15 bf16(z - bf16(z)).
-__device__ __forceinline__ void zblk_store(uint32_t zb, int r, float z)
-{
-    const float hi = __bfloat162float(__float2bfloat16_rn(z));
-    const uint32_t h = pack_bf16x2(hi, hi), l = pack_bf16x2(z - hi, z - hi);
-    sts128(zb + sw128_off(r, 0), make_uint4(h, h, h, h));
-    sts128(zb + sw128_off(r, 1), make_uint4(l, l, l, l));
 }
 
 // ---------------------------------------------------------------- kernel
@@ -333,21 +357,13 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         *abort_cta = 0;
         fence_mbar_init();
     }
-    if (warp < kTmemWarps) {   // the constant ONES tile(s): columns 0-7 one, 8-15 zero
+    if (warp < kTmemWarps) {   // the ONES block after every V slot's DV / 16 blocks (never loaded over)
         const uint32_t one = pack_bf16x2(1.f, 1.f);
-        if constexpr (PL::FUSED) {   // a block after every V slot's DV / 64 blocks (never loaded over)
-            for (int i = threadIdx.x; i < NS * kC; i += kTmemWarps * 32) {
-                const int st = i / kC, r = i % kC;
-                const uint32_t blk = base + PL::V0 + st * PL::VB + (DV / 64) * (kC * 128);
-                sts128(blk + sw128_off(r, 0), make_uint4(one, one, one, one));
-                sts128(blk + sw128_off(r, 1), make_uint4(0, 0, 0, 0));
-            }
-        } else {
-            const uint32_t ones = base + PL::O0;
-            for (int r = threadIdx.x; r < kC; r += kTmemWarps * 32) {
-                sts128(ones + sw32_off(r, 0), make_uint4(one, one, one, one));
-                sts128(ones + sw32_off(r, 1), make_uint4(0, 0, 0, 0));
-            }
+        for (int i = threadIdx.x; i < NS * kC; i += kTmemWarps * 32) {
+            const int st = i / kC, r = i % kC;
+            const uint32_t blk = base + PL::V0 + st * PL::VB + (DV / 16) * (kC * 32);
+            sts128(blk + sw32_off(r, 0), make_uint4(one, one, one, one));
+            sts128(blk + sw32_off(r, 1), make_uint4(0, 0, 0, 0));
         }
         fence_proxy_async_smem();
     }
@@ -365,7 +381,9 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (lane == 0) {
             const int role = warp - kProducerWarp;   // 0 Q, 1 K, 2 V
             const CUtensorMap *tm = role == 0 ? &tm_q : role == 1 ? &tm_k : &tm_v;
-            const int nb = role == 2 ? DV / 64 : DP / 64;   // 64-column boxes per tile
+            const int nb = role == 2 ? DV / 16 : DP / 64;   // boxes per tile (V: 16-column boxes,
+            const int bw = role == 2 ? 16 : 64;             //  32-byte swizzle; Q, K: 64 columns,
+            const int bs = role == 2 ? kC * 32 : kC * 128;  //  128-byte swizzle) and their stride
             const int tb = role == 2 ? PL::VB : PL::QB;     // slot stride in the ring
             const int tx = role == 2 ? kC * DV * 2 : PL::QB;  // bytes one tile load brings (a fused V
                                                             // slot also holds the constant ONES block)
@@ -377,15 +395,14 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             uint32_t n = 0;
             bool ok = true;
             auto prefetch = [&](int head, int chunk) {
-                for (int b = 0; b < nb; b++) tma_prefetch_3d(tm, b * 64, chunk * kC, head);
+                for (int b = 0; b < nb; b++) tma_prefetch_3d(tm, b * bw, chunk * kC, head);
             };
             auto load = [&](int head, int chunk, uint64_t pol) {
                 const int st = n % NS;
                 if (n >= NS && !wait_bar(&empty[st], ((n / NS) - 1) & 1, ctl)) return false;
                 mbar_arrive_expect_tx(&full[st], tx);
                 for (int b = 0; b < nb; b++)
-                    tma_load_3d_hint(ring + st * tb + b * kC * 128, tm, &full[st], b * 64, chunk * kC,
-                                     head, pol);
+                    tma_load_3d_hint(ring + st * tb + b * bs, tm, &full[st], b * bw, chunk * kC, head, pol);
                 n++;
                 return true;
             };
@@ -453,14 +470,12 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t id_qk = idesc_bf16(128, kC, 0, 0);
-            // (fused layout: N = DV + 16 carries the z / denominator columns)
+            // N = DV + 16: the z / denominator columns ride on every product with V or S_prev
             constexpr uint32_t id_qs = idesc_bf16(128, PL::NQ16, 0, 1);
-            constexpr uint32_t id_q16 = idesc_bf16(128, 16, 0, 1);
             constexpr uint32_t id_kv = idesc_bf16(128, PL::NQ16, 1, 1);
-            constexpr uint32_t id_k16 = idesc_bf16(128, 16, 1, 1);
-            constexpr bool kSide = !PL::FUSED;   // separate N = 16 side products
+            constexpr uint32_t lbo_v = kC * 32, lbo_s = PR * 32;   // 16-column block strides (32B swizzle)
             constexpr uint32_t lbo_kT = DP == 128 ? kC * 128 : 0;   // DP = 64: rows 64-127 repeat 0-63
-            const uint32_t s_addr = base + PL::S0, zp_addr = base + PL::Z0, ones = base + PL::O0;
+            const uint32_t s_addr = base + PL::S0;
             uint32_t nkv = 0;    // K / V ring loads consumed (phase A and C)
             uint32_t nq = 0;     // Q ring loads consumed
             uint32_t ndone = 0;  // phase-C chunks whose MMA2 has been issued (global chunk index)
@@ -482,7 +497,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 tc_fence_after();
                 const uint32_t qa = base + PL::Q0 + (qn % NS) * PL::QB;
                 const uint32_t ka = base + PL::K0 + (kn % NS) * PL::QB;
-                const uint32_t dst = tmem + PL::T_R0 + (k & 1) * 128;
+                const uint32_t dst = tmem + PL::T_R0 + (k & 1) * PL::RS;
                 if (!*abort_cta) {
 #pragma unroll
                     for (int kk = 0; kk < DP; kk += 16) {
@@ -506,8 +521,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     // denominator slot, once the TMEM warps have read item it - 2's
                     const int rr = it & 1;
                     if (it >= 2) wait_bar(&sloc_read[rr], ((it >> 1) - 1) & 1, ctl);
-                    const uint32_t dS = tmem + PL::T_R0 + rr * 128;
-                    const uint32_t dz = tmem + PL::T_DEN0 + rr * 16;
+                    const uint32_t dS = tmem + PL::T_R0 + rr * PL::RS;   // S | z of the segment
                     for (int c = 0; c < nc; c++) {
                         const int st = nkv % NS;
                         wait_bar(&k_ready[st], (nkv / NS) & 1, ctl);
@@ -516,19 +530,11 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         const uint32_t ka = base + PL::K0 + st * PL::QB;
                         const uint32_t va = base + PL::V0 + st * PL::VB;
                         if (!*abort_cta) {
-                            // all N = Dv steps, then the narrow N = 16 ones (no shape switch per step)
 #pragma unroll
                             for (int k = 0; k < kC; k += 16)
                                 mma_bf16_ss(dS, sw128_desc(ka + (k / 8) * 1024, lbo_kT, 1024),
-                                            sw128_desc(va + (k / 8) * 1024, kC * 128, 1024), id_kv,
+                                            sw32_desc(va + (k / 8) * 256, lbo_v, 256), id_kv,
                                             (c > 0 || k > 0) ? 1u : 0u);
-                            if constexpr (kSide) {
-#pragma unroll
-                                for (int k = 0; k < kC; k += 16)
-                                    mma_bf16_ss(dz, sw128_desc(ka + (k / 8) * 1024, lbo_kT, 1024),
-                                                sw32_desc(ones + (k / 8) * 256, 256, 256), id_k16,
-                                                (c > 0 || k > 0) ? 1u : 0u);
-                            }
                         }
                         mma_commit(&k_empty[st]);
                         mma_commit(&v_empty[st]);
@@ -546,9 +552,8 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     const uint32_t qa = base + PL::Q0 + qs * PL::QB;
                     const uint32_t ka = base + PL::K0 + st * PL::QB;
                     const uint32_t va = base + PL::V0 + st * PL::VB;
-                    const uint32_t rnum = tmem + PL::T_R0 + (k & 1) * 128;
-                    const uint32_t rden = tmem + PL::T_DEN0 + (k & 1) * 16;
-                    // MMA3 / MMA3b: NUM = phiQ S_prev, DEN = phiQ ZP (A(k) has been read)
+                    const uint32_t rnum = tmem + PL::T_R0 + (k & 1) * PL::RS;   // NUM | DEN
+                    // MMA3: NUM | DEN = phiQ [S_prev | z_prev] (A(k) has been read)
                     wait_bar(a_free, k & 1, ctl);
 #pragma unroll
                     for (int pc = 0; pc < NSP; pc++) {
@@ -559,56 +564,34 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             for (int kk = 0; kk < PR; kk += 16) {
                                 const int kq = pc * PR + kk;
                                 mma_bf16_ss(rnum, sw128_desc(qa + (kq / 64) * (kC * 128) + (kq % 64) * 2, 16, 1024),
-                                            sw128_desc(s_addr + (kk / 8) * 1024, PR * 128, 1024), id_qs,
+                                            sw32_desc(s_addr + (kk / 8) * 256, lbo_s, 256), id_qs,
                                             kq > 0 ? 1u : 0u);
-                            }
-                            if constexpr (kSide) {
-#pragma unroll
-                                for (int kk = 0; kk < PR; kk += 16) {
-                                    const int kq = pc * PR + kk;
-                                    mma_bf16_ss(rden,
-                                                sw128_desc(qa + (kq / 64) * (kC * 128) + (kq % 64) * 2, 16, 1024),
-                                                sw32_desc(zp_addr + (kq / 8) * 256, 256, 256), id_q16,
-                                                kq > 0 ? 1u : 0u);
-                                }
                             }
                         }
                         if (pc + 1 < NSP) mma_commit(sp_free);
                     }
                     mma_commit(&q_empty[qs]);
-                    // MMA4 / MMA4b: S += phiK^T V, Z += phiK^T ONES
+                    // MMA4: S | z += phiK^T [V | ONES]
                     wait_bar(&v_full[st], (nkv / NS) & 1, ctl);
                     tc_fence_after();
                     if (!*abort_cta) {
 #pragma unroll
                         for (int kk = 0; kk < kC; kk += 16)
                             mma_bf16_ss(tmem + PL::T_S, sw128_desc(ka + (kk / 8) * 1024, lbo_kT, 1024),
-                                        sw128_desc(va + (kk / 8) * 1024, kC * 128, 1024), id_kv, 1u);
-                        if constexpr (kSide) {
-#pragma unroll
-                            for (int kk = 0; kk < kC; kk += 16)
-                                mma_bf16_ss(tmem + PL::T_Z, sw128_desc(ka + (kk / 8) * 1024, lbo_kT, 1024),
-                                            sw32_desc(ones + (kk / 8) * 256, 256, 256), id_k16, 1u);
-                        }
+                                        sw32_desc(va + (kk / 8) * 256, lbo_v, 256), id_kv, 1u);
                     }
                     mma_commit(s_done);
                     mma_commit(&k_empty[st]);
                     // MMA1(k+1) into the other region
                     if (c + 1 < nc) mma1(k + 1, nq + 1, nkv + 1);
-                    // MMA2 / MMA2b: NUM += P V, DEN += P ONES  (P in TMEM)
+                    // MMA2: NUM | DEN += P [V | ONES]  (P in TMEM)
                     wait_bar(p_ready, k & 1, ctl);
                     tc_fence_after();
                     if (!*abort_cta) {
 #pragma unroll
                         for (int kk = 0; kk < kC; kk += 16)
-                            mma_bf16_ts(rnum, tmem + PL::T_P + kk / 2, sw128_desc(va + (kk / 8) * 1024, kC * 128, 1024),
+                            mma_bf16_ts(rnum, tmem + PL::T_P + kk / 2, sw32_desc(va + (kk / 8) * 256, lbo_v, 256),
                                         id_qs, 1u);
-                        if constexpr (kSide) {
-#pragma unroll
-                            for (int kk = 0; kk < kC; kk += 16)
-                                mma_bf16_ts(rden, tmem + PL::T_P + kk / 2, sw32_desc(ones + (kk / 8) * 256, 256, 256),
-                                            id_q16, 1u);
-                        }
                     }
                     mma_commit(num_full);
                     nq++;
@@ -665,7 +648,8 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // the epilogue of c.
         const bool late = NSP == 2 && piece == 1;
         const int prow = r - piece * PR;           // row inside the piece
-        const uint32_t s_addr = base + PL::S0, zp_addr = base + PL::Z0;
+        const uint32_t s_addr = base + PL::S0;
+        const uint32_t z_addr = s_addr + (DV / 16) * (PR * 32);   // the z block after S_prev's blocks
         uint32_t kg = 0;      // global index of the next chunk whose A is read
         uint32_t nkt = 0;     // K ring position (segment-sum form: this warp's share of phi(K))
         uint32_t nvr = 0;     // V ring position (phase A and C tiles)
@@ -684,16 +668,13 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     uint32_t v[32];
                     tmem_ld32_nowait(tmem + lane_base + PL::T_S + grp * HALF + cb, v);
                     tmem_ld_wait();
-                    sprev_store32<PR>(s_addr, prow, grp * HALF + cb, v);
+                    sprev_store32_sw32<PR>(s_addr, prow, grp * HALF + cb, v);
                 }
                 if (grp == 0) {
                     uint32_t zv[16];
                     tmem_ld16_nowait(tmem + lane_base + PL::T_Z, zv);
                     tmem_ld_wait();
-                    if constexpr (PL::FUSED)
-                        zblk_store(s_addr + (DV / 64) * (PR * 128), r, __uint_as_float(zv[0]));
-                    else
-                        zp_store(zp_addr, r, __uint_as_float(zv[0]));
+                    zp_store(z_addr, prow, __uint_as_float(zv[0]));
                 }
             }
             fence_proxy_async_smem();
@@ -725,10 +706,10 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         auto load_p = [&](uint32_t (&pk)[32]) {
             wait_bar(a_full, kg & 1, ctl);
             tc_fence_after();
-            const uint32_t ra = tmem + lane_base + PL::T_R0 + (kg & 1) * 128 + grp * 64;
+            const uint32_t ra = tmem + lane_base + PL::T_R0 + (kg & 1) * PL::RS + grp * 64;
             uint32_t a0[32], a1[32];
-            tmem_ld32_nowait(ra, a0);
-            tmem_ld32_nowait(ra + 32, a1);
+            tmem_ld32c<PL::ALN32>(ra, a0);
+            tmem_ld32c<PL::ALN32>(ra + 32, a1);
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
@@ -746,7 +727,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         };
         // P -> its TMEM slot (keys [64 grp, 64 grp + 64) -> columns [32 grp, 32 grp + 32))
         auto store_p = [&](const uint32_t (&pk)[32]) {
-            tmem_st32_nowait(tmem + lane_base + PL::T_P + grp * 32, pk);
+            tmem_st32c<PL::ALN32>(tmem + lane_base + PL::T_P + grp * 32, pk);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -797,7 +778,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
                     for (int cb = 0; cb < HALF; cb += 32) {
                         uint32_t l[32];
-                        tmem_ld32_nowait(tmem + lane_base + PL::T_R0 + rr * 128 + grp * HALF + cb, l);
+                        tmem_ld32c<PL::ALN32>(tmem + lane_base + PL::T_R0 + rr * PL::RS + grp * HALF + cb, l);
                         tmem_ld_wait();
 #pragma unroll
                         for (int i = 0; i < 8; i++)
@@ -807,8 +788,8 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     }
                     if (grp == 0) {
                         uint32_t d[16];
-                        // z of the segment: the DEN slot, or (fused) the columns after S in the region
-                        tmem_ld16_nowait(tmem + lane_base + (PL::FUSED ? PL::T_R0 + rr * 128 + DV : PL::T_DEN0 + rr * 16), d);
+                        // z of the segment: the columns after S in the region
+                        tmem_ld16_nowait(tmem + lane_base + PL::T_R0 + rr * PL::RS + DV, d);
                         tmem_ld_wait();
                         __stcg(sc.prez + slot_id * DP + r, __uint_as_float(d[0]));
                     }
@@ -882,11 +863,11 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (more) store_p(pk);
                 if (more && late) sprev_from_tmem();
                 tc_fence_after();
-                const uint32_t rn = tmem + lane_base + PL::T_R0 + (k & 1) * 128 + grp * HALF;
+                const uint32_t rn = tmem + lane_base + PL::T_R0 + (k & 1) * PL::RS + grp * HALF;
                 uint32_t d[16], n0[32], n1[32];
-                tmem_ld16_nowait(tmem + lane_base + (PL::FUSED ? PL::T_R0 + (k & 1) * 128 + DV : PL::T_DEN0 + (k & 1) * 16), d);
-                tmem_ld32_nowait(rn, n0);
-                if constexpr (HALF == 64) tmem_ld32_nowait(rn + 32, n1);
+                tmem_ld16_nowait(tmem + lane_base + PL::T_R0 + (k & 1) * PL::RS + DV, d);   // DEN
+                tmem_ld32c<PL::ALN32>(rn, n0);
+                if constexpr (HALF == 64) tmem_ld32c<PL::ALN32>(rn + 32, n1);
                 tmem_ld_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -1588,18 +1569,20 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode()
 
 // 3-D map over a [BH, N, cols] bf16 tensor whose rows are row_elems apart
 // (cols, the default, or wider: one column block of a wider tensor); box =
-// 64 columns x 128 rows x 1 head, 128-byte swizzle; rows past N read as zero.
-bool make_map(CUtensorMap *m, const void *base, long long BH, long long N, int cols, int row_elems = 0)
+// 64 columns x 128 rows x 1 head with 128-byte swizzle, or (sw = 32) 16
+// columns x 128 rows with 32-byte swizzle; rows past N read as zero.
+bool make_map(CUtensorMap *m, const void *base, long long BH, long long N, int cols, int row_elems = 0,
+              int sw = 128)
 {
     auto enc = get_encode();
     if (!enc) return false;
     if (row_elems <= 0) row_elems = cols;
     cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)N, (cuuint64_t)BH};
     cuuint64_t strides[2] = {(cuuint64_t)row_elems * 2, (cuuint64_t)N * row_elems * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)kC, 1};
+    cuuint32_t box[3] = {sw == 32 ? 16u : 64u, (cuuint32_t)kC, 1};
     cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
-                     strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, sw == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -1801,8 +1784,9 @@ cudaError_t run_elu(const Problem &p, void *scratch, float *S_out, float *z_out,
                     bool causal)
 {
     CUtensorMap tq, tk, tv, to;
+    // V tiles in 32-byte swizzle (16-column blocks, each V slot followed by its ONES block)
     if (!make_map(&tq, p.q, p.BH, p.N, p.D) || !make_map(&tk, p.k, p.BH, p.N, p.D) ||
-        !make_map(&tv, p.v, p.BH, p.N, p.Dv) || !make_map(&to, p.out, p.BH, p.N, p.Dv))
+        !make_map(&tv, p.v, p.BH, p.N, p.Dv, 0, 32) || !make_map(&to, p.out, p.BH, p.N, p.Dv))
         return cudaErrorInvalidValue;
     Geo g = plan(p.BH, p.N, num_sms());
     g.exp_rows = DP;
@@ -1883,7 +1867,8 @@ cudaError_t run_prf(const Problem &p, void *scratch, float *S_out, float *z_out,
         if (!make_map(&tq[f], (const __nv_bfloat16 *)phq + 128 * f, p.BH, p.N, 128, M) ||
             !make_map(&tk[f], (const __nv_bfloat16 *)phk + 128 * f, p.BH, p.N, 128, M))
             return cudaErrorInvalidValue;
-    if (!make_map(&tv, p.v, p.BH, p.N, p.Dv) || !make_map(&to, p.out, p.BH, p.N, p.Dv)) return cudaErrorInvalidValue;
+    if (!make_map(&tv, p.v, p.BH, p.N, p.Dv, 0, 32) || !make_map(&to, p.out, p.BH, p.N, p.Dv))
+        return cudaErrorInvalidValue;
     void *half = b + L.half;
     g.exp_rows = M;
     if (causal) {
