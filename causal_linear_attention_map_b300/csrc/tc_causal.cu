@@ -381,9 +381,13 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (lane == 0) {
             const int role = warp - kProducerWarp;   // 0 Q, 1 K, 2 V
             const CUtensorMap *tm = role == 0 ? &tm_q : role == 1 ? &tm_k : &tm_v;
-            const int nb = role == 2 ? DV / 16 : DP / 64;   // boxes per tile (V: 16-column boxes,
-            const int bw = role == 2 ? 16 : 64;             //  32-byte swizzle; Q, K: 64 columns,
-            const int bs = role == 2 ? kC * 32 : kC * 128;  //  128-byte swizzle) and their stride
+            // boxes per tile, their width and stride: V of the output form in 16-column
+            // boxes (32-byte swizzle); Q, K and the segment-sum form's V in 64-column
+            // boxes (128-byte swizzle: fewer, longer rows per TMA request)
+            constexpr bool kV32 = !AGG;
+            const int nb = role == 2 ? (kV32 ? DV / 16 : DV / 64) : DP / 64;
+            const int bw = role == 2 && kV32 ? 16 : 64;
+            const int bs = role == 2 && kV32 ? kC * 32 : kC * 128;
             const int tb = role == 2 ? PL::VB : PL::QB;     // slot stride in the ring
             const int tx = role == 2 ? kC * DV * 2 : PL::QB;  // bytes one tile load brings (a fused V
                                                             // slot also holds the constant ONES block)
@@ -530,10 +534,19 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         const uint32_t ka = base + PL::K0 + st * PL::QB;
                         const uint32_t va = base + PL::V0 + st * PL::VB;
                         if (!*abort_cta) {
+                            // (V in 128-byte swizzle here; z from the slot's ONES block)
+                            constexpr uint32_t id_s = idesc_bf16(128, DV, 1, 1);
+                            constexpr uint32_t id_z = idesc_bf16(128, 16, 1, 1);
+                            const uint32_t ones = va + DV * kC * 2;
 #pragma unroll
                             for (int k = 0; k < kC; k += 16)
                                 mma_bf16_ss(dS, sw128_desc(ka + (k / 8) * 1024, lbo_kT, 1024),
-                                            sw32_desc(va + (k / 8) * 256, lbo_v, 256), id_kv,
+                                            sw128_desc(va + (k / 8) * 1024, kC * 128, 1024), id_s,
+                                            (c > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+                            for (int k = 0; k < kC; k += 16)
+                                mma_bf16_ss(dS + DV, sw128_desc(ka + (k / 8) * 1024, lbo_kT, 1024),
+                                            sw32_desc(ones + (k / 8) * 256, 256, 256), id_z,
                                             (c > 0 || k > 0) ? 1u : 0u);
                         }
                         mma_commit(&k_empty[st]);
@@ -1688,9 +1701,9 @@ cudaError_t set_smem()
 // The causal forward over prepared maps: when segmented, the segment-sum
 // pass, the scan and then the output pass; else the output pass alone.
 template <int DP, int DV, int MODE>
-cudaError_t run_causal(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &to,
-                       Geo g, void *scratch, float *num_part, float *den_part, void *out, float *S_out,
-                       float *z_out, int *err, cudaStream_t s)
+cudaError_t run_causal(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                       const CUtensorMap &tv_agg, const CUtensorMap &to, Geo g, void *scratch, float *num_part,
+                       float *den_part, void *out, float *S_out, float *z_out, int *err, cudaStream_t s)
 {
     using PL = Plan<DP, DV>;
     constexpr int AMODE = MODE == kModeElu ? kModeElu : kModeFeat;
@@ -1707,7 +1720,7 @@ cudaError_t run_causal(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
         Geo ga = g;
         ga.n_items = g.BH * (g.nseg - 1);
         tc_causal_kernel<DP, DV, true, AMODE><<<min(ga.n_items, sms), kThreads, PL::SMEM, s>>>(
-            tq, tk, tv, to, ga, sc, (__nv_bfloat16 *)out, nullptr, nullptr, err);
+            tq, tk, tv_agg, to, ga, sc, (__nv_bfloat16 *)out, nullptr, nullptr, err);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         const int sz = DP * DV + DP;
         seg_scan_kernel<<<dim3(cdiv(sz, 256), (unsigned)g.BH), 256, 0, s>>>(sc.preS, sc.prez, g.nseg,
@@ -1728,7 +1741,7 @@ cudaError_t run_causal(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
 // per-head totals into rows [row_off, row_off + DP) of totS / totz, whose
 // heads hold tot_rows feature rows.
 template <int DP, int DV, int AMODE>
-cudaError_t run_totals(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &to,
+cudaError_t run_totals(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv_agg, const CUtensorMap &to,
                        Geo g, void *scratch, float *totS, float *totz, int tot_rows, int row_off, int *err,
                        cudaStream_t s)
 {
@@ -1739,7 +1752,7 @@ cudaError_t run_totals(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
     if ((e = set_smem<DP, DV, AMODE>()) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(scratch, 0, 16, s)) != cudaSuccess) return e;
     tc_causal_kernel<DP, DV, true, AMODE><<<min(g.n_items, sms), kThreads, PL::SMEM, s>>>(
-        tq, tk, tv, to, g, sc, nullptr, nullptr, nullptr, err);
+        tq, tk, tv_agg, to, g, sc, nullptr, nullptr, nullptr, err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int sz = DP * DV + DP;
     nc_total_kernel<<<dim3(cdiv(sz, 256), (unsigned)g.BH), 256, 0, s>>>(
@@ -1783,19 +1796,21 @@ template <int DP, int DV>
 cudaError_t run_elu(const Problem &p, void *scratch, float *S_out, float *z_out, int *err, cudaStream_t s,
                     bool causal)
 {
-    CUtensorMap tq, tk, tv, to;
-    // V tiles in 32-byte swizzle (16-column blocks, each V slot followed by its ONES block)
+    // V: 32-byte swizzle for the output form (16-column blocks, each V slot followed
+    // by its ONES block), 128-byte swizzle for the segment-sum form
+    CUtensorMap tq, tk, tv, tva, to;
     if (!make_map(&tq, p.q, p.BH, p.N, p.D) || !make_map(&tk, p.k, p.BH, p.N, p.D) ||
-        !make_map(&tv, p.v, p.BH, p.N, p.Dv, 0, 32) || !make_map(&to, p.out, p.BH, p.N, p.Dv))
+        !make_map(&tv, p.v, p.BH, p.N, p.Dv, 0, 32) || !make_map(&tva, p.v, p.BH, p.N, p.Dv) ||
+        !make_map(&to, p.out, p.BH, p.N, p.Dv))
         return cudaErrorInvalidValue;
     Geo g = plan(p.BH, p.N, num_sms());
     g.exp_rows = DP;
     if (causal)
-        return run_causal<DP, DV, kModeElu>(tq, tk, tv, to, g, scratch, nullptr, nullptr, p.out, S_out, z_out,
-                                           err, s);
+        return run_causal<DP, DV, kModeElu>(tq, tk, tv, tva, to, g, scratch, nullptr, nullptr, p.out, S_out,
+                                           z_out, err, s);
     float *totS = (float *)((unsigned char *)scratch + seg_scratch_bytes<DP, DV>(g, true));
     float *totz = totS + (size_t)g.BH * DP * DV;
-    cudaError_t e = run_totals<DP, DV, kModeElu>(tq, tk, tv, to, g, scratch, totS, totz, DP, 0, err, s);
+    cudaError_t e = run_totals<DP, DV, kModeElu>(tq, tk, tva, to, g, scratch, totS, totz, DP, 0, err, s);
     if (e == cudaSuccess) e = run_readout<DP, DV, true>(tq, to, g, scratch, totS, totz, err, s);
     if (e == cudaSuccess) e = export_totals(S_out, z_out, totS, totz, g.BH, DP, DV, s);
     return e;
@@ -1867,21 +1882,23 @@ cudaError_t run_prf(const Problem &p, void *scratch, float *S_out, float *z_out,
         if (!make_map(&tq[f], (const __nv_bfloat16 *)phq + 128 * f, p.BH, p.N, 128, M) ||
             !make_map(&tk[f], (const __nv_bfloat16 *)phk + 128 * f, p.BH, p.N, 128, M))
             return cudaErrorInvalidValue;
-    if (!make_map(&tv, p.v, p.BH, p.N, p.Dv, 0, 32) || !make_map(&to, p.out, p.BH, p.N, p.Dv))
+    CUtensorMap tva;
+    if (!make_map(&tv, p.v, p.BH, p.N, p.Dv, 0, 32) || !make_map(&tva, p.v, p.BH, p.N, p.Dv) ||
+        !make_map(&to, p.out, p.BH, p.N, p.Dv))
         return cudaErrorInvalidValue;
     void *half = b + L.half;
     g.exp_rows = M;
     if (causal) {
         if constexpr (M == 128) {
-            return run_causal<128, DV, kModeFeat>(tq[0], tk[0], tv, to, g, half, nullptr, nullptr, p.out, S_out,
-                                                  z_out, err, s);
+            return run_causal<128, DV, kModeFeat>(tq[0], tk[0], tv, tva, to, g, half, nullptr, nullptr, p.out,
+                                                  S_out, z_out, err, s);
         } else {
             float *num_part = (float *)(b + L.part);
             float *den_part = (float *)(b + L.part + up256((size_t)p.BH * p.N * DV * 4));
-            e = run_causal<128, DV, kModeFeatPart>(tq[0], tk[0], tv, to, g, half, num_part, den_part, p.out, S_out,
-                                                   z_out, err, s);
+            e = run_causal<128, DV, kModeFeatPart>(tq[0], tk[0], tv, tva, to, g, half, num_part, den_part, p.out,
+                                                   S_out, z_out, err, s);
             if (e != cudaSuccess) return e;
-            return run_causal<128, DV, kModeFeatComb>(tq[1], tk[1], tv, to, g, half, num_part, den_part, p.out,
+            return run_causal<128, DV, kModeFeatComb>(tq[1], tk[1], tv, tva, to, g, half, num_part, den_part, p.out,
                                                       S_out ? S_out + 128 * DV : nullptr,
                                                       z_out ? z_out + 128 : nullptr, err, s);
         }
@@ -1889,7 +1906,7 @@ cudaError_t run_prf(const Problem &p, void *scratch, float *S_out, float *z_out,
     float *totS = (float *)(b + L.tot);
     float *totz = totS + (size_t)g.BH * M * DV;
     for (int f = 0; f < M / 128; f++)
-        if ((e = run_totals<128, DV, kModeFeat>(tq[f], tk[f], tv, to, g, half, totS, totz, M, 128 * f, err, s)) !=
+        if ((e = run_totals<128, DV, kModeFeat>(tq[f], tk[f], tva, to, g, half, totS, totz, M, 128 * f, err, s)) !=
             cudaSuccess)
             return e;
     CUtensorMap tqa;
