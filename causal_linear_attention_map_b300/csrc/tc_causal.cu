@@ -229,23 +229,8 @@ __device__ __forceinline__ void phi_cols(uint32_t t, int r, bool zero)
 }
 
 // One S_prev row block: 32 fp32 state values -> bf16 at row r, columns
-// [c0, c0 + 32) of an MN-major [PR x DV] piece (DV / 64 blocks of PR rows).
-template <int PR>
-__device__ __forceinline__ void sprev_store32(uint32_t st, int r, int c0, const uint32_t (&v)[32])
-{
-#pragma unroll
-    for (int j = 0; j < 4; j++) {
-        const int col = c0 + 8 * j;
-        const uint32_t a = st + (uint32_t)(col >> 6) * (PR * 128) + sw128_off(r, (col & 63) >> 3);
-        sts128(a, make_uint4(
-                      pack_bf16x2(__uint_as_float(v[8 * j]), __uint_as_float(v[8 * j + 1])),
-                      pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
-                      pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
-                      pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]))));
-    }
-}
-
-// The same in 32-byte swizzle: blocks of 16 columns, PR * 32 bytes apart.
+// [c0, c0 + 32) of an MN-major [PR x DV] piece in 32-byte swizzle (blocks of
+// 16 columns, PR * 32 bytes apart).
 template <int PR>
 __device__ __forceinline__ void sprev_store32_sw32(uint32_t st, int r, int c0, const uint32_t (&v)[32])
 {
@@ -1011,8 +996,11 @@ template <int DP, int DV>
 struct NcPlan {
     static constexpr int QB = kC * DP * 2;
     static constexpr int OB = kC * DV * 2;
-    static constexpr int SB = DP * DV * 2;
-    static constexpr int ZB = DP * 32;
+    // S in 32-byte swizzle (16-column blocks, DP * 32 bytes apart) followed by
+    // the z block (bf16 z | z - bf16(z)): one N = DV + 16 product gives NUM | DEN
+    static constexpr int NQ16 = DV + 16;
+    static constexpr int SB = DP * NQ16 * 2;
+    static constexpr int ZB = 0;
     static constexpr int NO = 2;
     static constexpr int kBudget = 227 * 1024 - 2048;
     static constexpr int NQ0 = (kBudget - NO * OB - SB - ZB) / QB;
@@ -1024,9 +1012,9 @@ struct NcPlan {
     static constexpr int Z0 = S0 + SB;
     static constexpr int TILES = Z0 + ZB;
     static constexpr int SMEM = TILES + 1024 + 1024;
-    // TMEM: NUM of region r at column 128 r (DV columns), its DEN (16
-    // columns) at T_DEN + 16 r
-    static constexpr int T_DEN = 256;
+    // TMEM: region r at column RS r holds NUM | DEN (DV + 16 columns)
+    static constexpr int RS = NQ16 > kC ? NQ16 : kC;
+    static constexpr bool ALN32 = RS % 32 == 0;
     static constexpr int TMEM_COLS = 512;
     static_assert(SMEM <= 227 * 1024, "shared memory plan too large");
     static_assert(SMEM > 114 * 1024, "one CTA per SM: the kernel holds all 512 TMEM columns");
@@ -1161,9 +1149,8 @@ nc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     } else if (warp == kNcMma) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t id_qs = idesc_bf16(128, DV, 0, 1);
-            constexpr uint32_t id_q16 = idesc_bf16(128, 16, 0, 1);
-            const uint32_t s_addr = base + PL::S0, zp_addr = base + PL::Z0;
+            constexpr uint32_t id_qs = idesc_bf16(128, PL::NQ16, 0, 1);
+            const uint32_t s_addr = base + PL::S0;
             uint32_t k = 0, ni = 0;
             for (int it = 0;; it++) {
                 const int item = next_item(it, false);
@@ -1181,13 +1168,9 @@ nc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     if (!*abort_cta) {
 #pragma unroll
                         for (int kk = 0; kk < DP; kk += 16)
-                            mma_bf16_ss(tmem + rr * 128, sw128_desc(qa + (kk / 64) * (kC * 128) + (kk % 64) * 2, 16, 1024),
-                                        sw128_desc(s_addr + (kk / 8) * 1024, DP * 128, 1024), id_qs, kk > 0 ? 1u : 0u);
-#pragma unroll
-                        for (int kk = 0; kk < DP; kk += 16)
-                            mma_bf16_ss(tmem + PL::T_DEN + rr * 16,
+                            mma_bf16_ss(tmem + rr * PL::RS,
                                         sw128_desc(qa + (kk / 64) * (kC * 128) + (kk % 64) * 2, 16, 1024),
-                                        sw32_desc(zp_addr + (kk / 8) * 256, 256, 256), id_q16, kk > 0 ? 1u : 0u);
+                                        sw32_desc(s_addr + (kk / 8) * 256, DP * 32, 256), id_qs, kk > 0 ? 1u : 0u);
                     }
                     mma_commit(&q_empty[st]);
                     mma_commit(&num_full[rr]);
@@ -1203,7 +1186,8 @@ nc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int qd = warp & 3, grp = warp >> 2;
         const int r = qd * 32 + lane;
         const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
-        const uint32_t s_addr = base + PL::S0, zp_addr = base + PL::Z0;
+        const uint32_t s_addr = base + PL::S0;
+        const uint32_t z_addr = s_addr + (DV / 16) * (DP * 32);   // the z block after S's blocks
         uint32_t k = 0, kq = 0, ni = 0;
         auto phi_q = [&]() {
             const int st = kq % NQ;
@@ -1243,9 +1227,9 @@ nc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         v[i + 2] = __float_as_uint(x.z);
                         v[i + 3] = __float_as_uint(x.w);
                     }
-                    sprev_store32<DP>(s_addr, row, grp * HALF + cb, v);
+                    sprev_store32_sw32<DP>(s_addr, row, grp * HALF + cb, v);
                 }
-                if (grp == 0) zp_store(zp_addr, row, __ldcg(sc.prez + (long long)h * DP + row));
+                if (grp == 0) zp_store(z_addr, row, __ldcg(sc.prez + (long long)h * DP + row));
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -1259,10 +1243,10 @@ nc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 wait_bar(&num_full[rr], (k >> 1) & 1, ctl);
                 tc_fence_after();
                 uint32_t d[16], n0[32], n1[32];
-                const uint32_t rn = tmem + lane_base + rr * 128 + grp * HALF;
-                tmem_ld16_nowait(tmem + lane_base + PL::T_DEN + rr * 16, d);
-                tmem_ld32_nowait(rn, n0);
-                if constexpr (HALF == 64) tmem_ld32_nowait(rn + 32, n1);
+                const uint32_t rn = tmem + lane_base + rr * PL::RS + grp * HALF;
+                tmem_ld16_nowait(tmem + lane_base + rr * PL::RS + DV, d);   // DEN
+                tmem_ld32c<PL::ALN32>(rn, n0);
+                if constexpr (HALF == 64) tmem_ld32c<PL::ALN32>(rn + 32, n1);
                 tmem_ld_wait();
                 tc_fence_before();
                 __syncwarp();
