@@ -168,16 +168,21 @@ class ClockSampler:
 # ------------------------------------------------------------------ our arm
 
 def dist_setup():
+    """One process per GPU (torchrun env).  Ranks use NCCL on GPUs; without a
+    GPU (host-side tests of the multi-rank logic) they use gloo."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    gpu = torch.cuda.is_available()
+    if gpu:
+        torch.cuda.set_device(local)
     if ws > 1:
         import torch.distributed as dist
 
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
-        torch.cuda.set_device(local)
+        if gpu:
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")
     return ws, rank, local
 
 
@@ -186,17 +191,26 @@ def barrier(ws):
         import torch.distributed as dist
 
         dist.barrier()
-    torch.cuda.synchronize()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
 
 
 def max_over_ranks(x: float, ws: int) -> float:
+    """The slowest rank's time (every rank gets it)."""
     if ws == 1:
         return x
     import torch.distributed as dist
 
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_rate(units_per_rank_step: float, steps: int, ws: int, max_ms: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest
+    rank's time (replicas: every rank does the same work)."""
+    return units_per_rank_step * steps * ws / (max_ms / 1e3)
 
 
 def cpu_baseline(w: wl.Workload, q, k, v, W, budget_s=12.0):
@@ -308,7 +322,7 @@ def run_ours(args):
     total_ms = max_over_ranks(total_ms, ws)
     ms_step = total_ms / args.steps
     tokens = w.B * w.N
-    value = tokens * args.steps * ws / (total_ms / 1e3)
+    value = job_rate(tokens, args.steps, ws, total_ms)
 
     pk, pk_kind = peaks()
     fwd_s = ms_step / 1e3
@@ -347,7 +361,7 @@ def run_ours(args):
     e1.record(stream)
     e1.synchronize()
     e_ms = max_over_ranks(e0.elapsed_time(e1), ws)
-    e2e = {"value": tokens * e_steps * ws / (e_ms / 1e3), "unit": "tokens/s",
+    e2e = {"value": job_rate(tokens, e_steps, ws, e_ms), "unit": "tokens/s",
            "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out.numel() * out.element_size(),
            "steps": e_steps, "path": "pinned host -> device copies, la_forward_ex, device -> host"}
     del hq, hk, hv, hout
@@ -445,7 +459,7 @@ def run_decode(la, args, S_fwd, z_fwd, dev, stream, ws):
     pk, pk_kind = peaks()
     bps = decode_bytes_per_step(B * H, D, D, D)
     ach = bps * T / (ms / 1e3) / 1e9
-    res = {"steps_per_s": T * ws / (ms / 1e3), "tokens_per_s": T * B * ws / (ms / 1e3),
+    res = {"steps_per_s": job_rate(T, 1, ws, ms), "tokens_per_s": job_rate(T * B, 1, ws, ms),
            "ms_total": ms, "us_per_step": ms * 1e3 / T, "decode_steps": T, "B": B, "H": H,
            "D": D, "launches": launches,
            "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"],
@@ -454,7 +468,7 @@ def run_decode(la, args, S_fwd, z_fwd, dev, stream, ws):
                         "note": "the 64 MB fp32 state fits in L2 (126 MB), so steps may run "
                                 "from L2; frac can exceed 1"}}
     if graph_ms is not None:
-        res["graph"] = {"steps_per_s": T * ws / (graph_ms / 1e3), "ms_total": graph_ms,
+        res["graph"] = {"steps_per_s": job_rate(T, 1, ws, graph_ms), "ms_total": graph_ms,
                         "launches_per_graph": G,
                         "note": "steps replayed with the state reset; same 4096 inputs"}
     return res

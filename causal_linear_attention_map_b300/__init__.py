@@ -30,7 +30,8 @@ STATUS_NAMES = {0: "LA_OK", -1: "LA_ERR_NULL", -2: "LA_ERR_DIM", -3: "LA_ERR_DTY
                 -4: "LA_ERR_FEATURE", -5: "LA_ERR_CUDA", -6: "LA_ERR_TIMEOUT",
                 -7: "LA_ERR_ALIGN"}
 EXPORTED = ("la_forward", "la_forward_ex", "la_step", "la_status_string", "la_check",
-            "la_shutdown", "la_version", "la_launch_count", "la_forward_noncausal_noalloc")
+            "la_shutdown", "la_version", "la_launch_count", "la_forward_noncausal_noalloc",
+            "la_selftest_timeout")
 
 _DT = {torch.float32: LA_F32, torch.bfloat16: LA_BF16}
 
@@ -96,6 +97,8 @@ def load(path: str | None = None):
     lib.la_status_string.restype = ctypes.c_char_p
     lib.la_check.argtypes = [vp]
     lib.la_check.restype = i
+    lib.la_selftest_timeout.argtypes = [i, vp]
+    lib.la_selftest_timeout.restype = i
     lib.la_shutdown.argtypes = []
     lib.la_shutdown.restype = None
     lib.la_version.argtypes = []
@@ -210,6 +213,13 @@ def la_step(S, z, q, k, v, feature_map: FeatureMap | None = None, out=None, stre
 def la_check(stream=None) -> int:
     """Synchronise the stream and return deferred device errors as a status."""
     return load().la_check(_stream(stream))
+
+
+def la_selftest_timeout(budget_ms: int = 50, stream=None) -> int:
+    """Launch the failure-detection self-test: a bounded wait that nothing
+    completes gives up after ~budget_ms; the next la_check returns
+    LA_ERR_TIMEOUT.  Returns the launch status."""
+    return load().la_selftest_timeout(int(budget_ms), _stream(stream))
 
 
 def la_shutdown() -> None:

@@ -45,6 +45,10 @@ size_t tc_scratch_bytes(const Problem &p, bool causal);
 cudaError_t tc_forward(const Problem &p, bool causal, void *scratch, float *S_out, float *z_out, int *err,
                        cudaStream_t s);
 
+// Failure-detection self-test: one bounded wait that runs out after about
+// budget_ms of SM clock and sets *err (see la_selftest_timeout).
+cudaError_t wait_selftest(int budget_ms, int *err, cudaStream_t s);
+
 // Non-causal: KV = phi(K)^T V and ksum = sum phi(k) reduced over N into
 // fp32 scratch (KV [BH, P, Dv], ksum [BH, P]; zeroed here), then the readout.
 size_t noncausal_scratch_bytes(const Problem &p);

@@ -224,6 +224,14 @@ int la_check(void *stream)
     return LA_OK;
 }
 
+int la_selftest_timeout(int budget_ms, void *stream)
+{
+    DeviceCtx *ctx = nullptr;
+    int st = get_ctx(&ctx);
+    if (st != LA_OK) return st;
+    return cuda_status(la::wait_selftest(budget_ms, ctx->err_word, (cudaStream_t)stream));
+}
+
 void la_shutdown(void)
 {
     std::lock_guard<std::mutex> lock(g_mu);

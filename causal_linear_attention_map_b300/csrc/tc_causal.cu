@@ -1548,6 +1548,34 @@ prf_phi_kernel(const __grid_constant__ CUtensorMap tm_xq, const __grid_constant_
     }
 }
 
+// ------------------------------------------------ failure-detection self-test
+//
+// One thread waits, with the kernels' own bounded wait, for phase 0 of an
+// mbarrier that expects one arrival which never comes; when the budget runs
+// out the wait raises the error word (as in a real stall) and returns.
+__global__ void wait_selftest_kernel(int *err, long long budget_cycles)
+{
+    __shared__ uint64_t bar;
+    __shared__ int cta_abort;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        cta_abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int glob = 0;
+        const Ctl ctl{&cta_abort, &glob, err};
+        const long long t0 = clock64();
+        while (!mbar_try_wait(&bar, 0)) {
+            if (clock64() - t0 > budget_cycles) {
+                raise_abort(ctl);
+                break;
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------ host side
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode()
@@ -1900,6 +1928,18 @@ cudaError_t run_prf(const Problem &p, void *scratch, float *S_out, float *z_out,
 }
 
 }  // namespace
+
+cudaError_t wait_selftest(int budget_ms, int *err, cudaStream_t s)
+{
+    budget_ms = budget_ms < 1 ? 1 : budget_ms > 2000 ? 2000 : budget_ms;
+    int dev = 0, khz = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev) != cudaSuccess || khz <= 0) khz = 2000000;
+    wait_selftest_kernel<<<1, 32, 0, s>>>(err, (long long)budget_ms * khz);
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) note_launches(1);
+    return e;
+}
 
 bool tc_causal_supported(const Problem &p)
 {

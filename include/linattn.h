@@ -136,6 +136,18 @@ const char *la_status_string(int status);
  */
 int la_check(void *stream);
 
+/*
+ * la_selftest_timeout -- exercise the library's failure detection without
+ * faulting the GPU: launches one small kernel on `stream` whose bounded
+ * mbarrier wait (the same wait every tensor-core kernel uses) waits for a
+ * phase that nothing completes.  After `budget_ms` milliseconds of SM clock
+ * (clamped to 1..2000) the wait gives up, sets this device's error word and
+ * the kernel returns normally, so the next la_check on the device returns
+ * LA_ERR_TIMEOUT (and clears it) while the context stays usable.
+ * Returns LA_OK once launched, LA_ERR_CUDA if the launch fails.
+ */
+int la_selftest_timeout(int budget_ms, void *stream);
+
 /* Release the library's memory pools on every device it used.  Must not be
  * called while work from this library is still running. */
 void la_shutdown(void);

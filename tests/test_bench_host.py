@@ -1,0 +1,80 @@
+"""Host-side logic of bench.py: the algorithmic byte and flop counts of the
+roofline against their closed forms, the shortened-workload option, the
+reference arm on non-zero ranks, and the multi-rank path (barrier, the
+slowest rank's time, the whole-job rate) as two gloo ranks on the CPU."""
+import argparse
+import os
+import socket
+
+import torch.multiprocessing as mp
+
+import bench
+import workloads as wl
+
+
+def test_algorithmic_counts_of_the_five_workloads():
+    # bytes: read q, k, v and write out once, (2 D + 2 Dv) elements per token-head
+    assert bench.alg_bytes(wl.LONG_65536) == 16 * 65536 * (2 * 128 + 2 * 128) * 2
+    assert bench.alg_bytes(wl.TINY_F32) == 64 * (2 * 16 + 2 * 16) * 4
+    # flops per token-head: 4 P Dv (S update, readout) + 3 P (z, denominator) + Dv (divide)
+    assert bench.alg_flops(wl.LONG_65536) == 16 * 65536 * (4 * 128 * 128 + 3 * 128 + 128)
+    # random features add the projection and the exponent arguments: 4 m D + 2 D + 2 m
+    p = wl.PRF_16384
+    per = 4 * 256 * 64 + 3 * 256 + 64 + 4 * 256 * 64 + 2 * 64 + 2 * 256
+    assert bench.alg_flops(p) == 2 * 8 * 16384 * per
+    # the long workload is HBM-bound against any B300-class ridge point
+    assert bench.alg_flops(wl.LONG_65536) / bench.alg_bytes(wl.LONG_65536) < 100
+
+
+def test_seq_len_option_shortens_the_named_workload():
+    a = argparse.Namespace(workload=wl.LONG_65536.name, seq_len=16384)
+    w = bench.workload_of(a)
+    assert (w.B, w.H, w.N, w.D, w.Dv) == (1, 16, 16384, 128, 128)
+    assert w.name == "causal_B1_H16_N16384_D128_bf16"
+    a.seq_len = 0
+    assert bench.workload_of(a) == wl.LONG_65536
+
+
+def test_reference_arm_is_silent_on_other_ranks(monkeypatch, capsys):
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "1")
+    a = argparse.Namespace(workload=wl.LONG_65536.name, seq_len=0, steps=1, warmup=3)
+    assert bench.run_reference(a) is None
+    assert capsys.readouterr().out == ""
+
+
+def _rank(rank, ws, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(ws), LOCAL_RANK=str(rank))
+    import torch.distributed as dist
+
+    import bench as b
+
+    w, r, _ = b.dist_setup()
+    b.barrier(w)
+    t_ms = 10.0 + 5.0 * r                # rank 1 is the slower one
+    slowest = b.max_over_ranks(t_ms, w)
+    q.put((r, w, slowest, b.job_rate(1000.0, 4, w, slowest)))
+    b.barrier(w)
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_agree_on_the_slowest_time_and_the_job_rate():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [g[0] for g in got] == [0, 1]
+    for _, ws, slowest, rate in got:
+        assert ws == 2
+        assert slowest == 15.0
+        # both ranks' units over the slowest rank's time
+        assert abs(rate - 1000.0 * 4 * 2 / 0.015) < 1e-6 * rate

@@ -141,3 +141,18 @@ def test_library_is_the_loaded_native_code(la):
     la.load()
     maps = open("/proc/self/maps").read()
     assert "liblinattn.so" in maps
+
+
+def test_bounded_wait_timeout_is_reported_and_the_context_survives(la):
+    """Failure detection without a GPU fault: a bounded wait that nothing
+    completes gives up, the next la_check reports LA_ERR_TIMEOUT (once), and
+    the library keeps working afterwards."""
+    torch.cuda.synchronize()
+    assert la.la_check() == la.LA_OK
+    assert la.la_selftest_timeout(20) == la.LA_OK
+    assert la.la_check() == -6
+    assert la.la_check() == la.LA_OK
+    w = wl.small(B=1, H=2, N=300, D=64, Dv=64, seed=77)
+    out, _, _, ref = _run(la, w)
+    assert_close(np64(out), ref, "bf16", what="after the self-test")
+    assert la.la_check() == la.LA_OK
