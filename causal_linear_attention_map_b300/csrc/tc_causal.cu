@@ -1679,7 +1679,10 @@ __global__ void seg_scan_kernel(float *__restrict__ preS, float *__restrict__ pr
 
 size_t up256(size_t b) { return (b + 255) & ~(size_t)255; }
 
-// Control words (ticket, abort) and, when segmented, the segment sums.
+// Control words and, when segmented, the segment sums.  The 16-byte header
+// holds the segment-sum pass's ticket (+0), the abort word (+4) and the
+// output or readout pass's ticket (+8): one memset clears all three, so no
+// stream operation sits between the passes.
 template <int DP, int DV>
 size_t seg_scratch_bytes(const Geo &g, bool every_segment)
 {
@@ -1692,7 +1695,7 @@ Scratch carve(void *scratch, const Geo &g)
 {
     unsigned char *b = (unsigned char *)scratch;
     Scratch sc;
-    sc.ticket = (int *)b;
+    sc.ticket = (int *)b;   // (the second pass's ticket is at b + 8)
     sc.abort = (int *)(b + 4);
     sc.preS = (float *)(b + 16);
     sc.prez = sc.preS + (size_t)g.BH * g.nseg * DP * DV;
@@ -1738,9 +1741,9 @@ cudaError_t run_causal(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
         seg_scan_kernel<<<dim3(cdiv(sz, 256), (unsigned)g.BH), 256, 0, s>>>(sc.preS, sc.prez, g.nseg,
                                                                            DP * DV, DP);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        if ((e = cudaMemsetAsync(scratch, 0, 4, s)) != cudaSuccess) return e;   // ticket
         launches += 2;
     }
+    sc.ticket = (int *)((unsigned char *)scratch + 8);   // the output pass's own ticket
     // pass 2: the chunk recurrence of every segment from its prefix
     tc_causal_kernel<DP, DV, false, MODE><<<min(g.n_items, sms), kThreads, PL::SMEM, s>>>(
         tq, tk, tv, to, g, sc, (__nv_bfloat16 *)out, S_out, z_out, err);
@@ -1783,8 +1786,8 @@ cudaError_t run_readout(const CUtensorMap &tq, const CUtensorMap &to, Geo g, voi
     Scratch sc = carve<DP, DV>(scratch, g);
     sc.preS = totS;
     sc.prez = totz;
+    sc.ticket = (int *)((unsigned char *)scratch + 8);   // cleared with the header by run_totals
     cudaError_t e;
-    if ((e = cudaMemsetAsync(scratch, 0, 16, s)) != cudaSuccess) return e;
     if ((e = set_max_smem_once<nc_out_kernel<DP, DV, PHI>>(NP::SMEM)) != cudaSuccess)
         return e;
     nc_out_kernel<DP, DV, PHI><<<min(g.n_items, num_sms()), kNcThreads, NP::SMEM, s>>>(tq, to, g, sc, err);
