@@ -1,6 +1,7 @@
-// tc_causal.cu -- chunked causal linear attention on the sm_103a tensor
-// cores (tcgen05, TMEM accumulators, TMA loads), bf16 inputs, fp32 state,
-// in ONE persistent kernel that reads q, k, v from HBM once.
+// tc_causal.cu -- linear attention on the sm_103a tensor cores (tcgen05,
+// TMEM accumulators, TMA loads and stores), bf16 inputs, fp32 state: the
+// chunked causal kernel, the non-causal readout, and the random-feature
+// projection.
 //
 // The method (review page "Transformers are RNNs", proposed method b2-b3,
 // b5): with phi applied to q and k, out_i = phi(q_i)^T S_i / phi(q_i)^T z_i
@@ -27,7 +28,8 @@
 //   warps 0-7   TMEM warps: phi(Q) in place on the Q tile, masked scores P,
 //               the state copy S_prev / ZP for the next chunk, the epilogue,
 //               phase B.  Warp w owns TMEM lane quadrant w % 4 (rows 32 (w%4)
-//               ..) and column half w / 4.
+//               ..) and column half w / 4.  (Aggregate form: two thirds of
+//               each K tile's phi, then the segment's sums to scratch.)
 //   warps 8-11  phi warps, one per lane quadrant (one tile row per thread):
 //               phi(K) in place on the K tile in shared memory.
 //   warp 12     TMA producer of Q tiles and item scheduler.
@@ -36,33 +38,34 @@
 //               tiles (lane 1).
 //   warp 15     MMA issuer (one thread).
 // The epilogue writes each output tile into the shared-memory slot of that
-// chunk's V tile (V is dead once MMA2 has read it; the two tiles have the
-// same shape and swizzle), and one thread stores it with a TMA tile store,
-// releasing the V slot once the store has read it.
+// chunk's V tile (V is dead once MMA2 has read it), and one thread stores it
+// with a TMA tile store, releasing the V slot once the store has read it.
 // The producers prefetch a tile ahead into L2.  Q, K and V have their own
 // rings because they free up at different points: Q after MMA3, K after
-// MMA4, V after MMA2.
+// MMA4, V after the output store.
 //
-// Per chunk c, all tcgen05.mma with fp32 accumulation in TMEM:
-//   MMA1   A    = phiQ . phiK^T        M=C, N=C,  K=Dphi
-//   MMA3   NUM  = phiQ . S_prev        M=C, N=Dv, K=Dphi   (S_prev bf16 in smem)
-//   MMA3b  DEN  = phiQ . ZP            M=C, N=16, K=Dphi
-//   MMA4   S   += phiK^T . V           M=Dphi, N=Dv, K=C
-//   MMA4b  Z   += phiK^T . ONES        M=Dphi, N=16, K=C   (Z[:,0] = z)
-//   MMA2   NUM += P . V                M=C, N=Dv, K=C      (P bf16 in TMEM)
-//   MMA2b  DEN += P . ONES             M=C, N=16, K=C
-// ONES is a constant [C x 16] tile (columns 0-7 = 1, 8-15 = 0) and ZP holds
-// z_prev split into bf16 hi (columns 0-7) and lo (columns 8-15), so that
-// out = NUM / (DEN[:,0] + DEN[:,8]).  phi never goes back to HBM.
-// TMEM holds two 128-column regions R0, R1 that chunks use alternately:
-// chunk k's scores A(k) land in R[k % 2], and once the TMEM warps have read
-// them into registers (as the masked bf16 P, which gets its own slot) the
-// same region takes NUM(k).  So MMA3(k) never waits for the epilogue of
-// k - 1; only MMA1(k + 2) needs R[k % 2] back.  The issue order per chunk is
+// Per chunk, four groups of tcgen05.mma (kind::f16, M = 128, K = 16 per
+// instruction) with fp32 accumulation in TMEM:
+//   MMA1   A         = phiQ . phiK^T              N = C,       K = Dphi
+//   MMA3   NUM | DEN = phiQ . [S_prev | ZP]       N = Dv + 16, K = Dphi
+//   MMA4   S   | z  += phiK^T . [V | ONES]        N = Dv + 16, K = C  (M = Dphi)
+//   MMA2   NUM | DEN += P . [V | ONES]            N = Dv + 16, K = C  (P bf16 in TMEM)
+// ONES is a constant [C x 16] block (columns 0-7 = 1, 8-15 = 0) after each V
+// slot, and ZP holds z_prev split into bf16 hi (columns 0-7) and lo (8-15)
+// after S_prev: V and S_prev are kept in 32-byte swizzle (16-column blocks)
+// so that these blocks are simply the next block of the operand, and
+// out = NUM / (DEN[:,0] + DEN[:,8]).  (A separate N = 16 product per K step
+// would cost about as much as the full one.)  phi never goes back to HBM.
+// TMEM holds two regions R0, R1 that chunks use alternately: chunk k's
+// scores A(k) land in R[k % 2], and once the TMEM warps have read them into
+// registers (as the masked bf16 P, which gets its own slot) the same region
+// takes NUM(k) | DEN(k).  So MMA3(k) never waits for the epilogue of k - 1;
+// only MMA1(k + 2) needs R[k % 2] back.  The issue order per chunk is
 // MMA3(k), MMA4(k), MMA1(k+1), MMA2(k), which keeps independent work in the
-// tensor pipe while the TMEM warps convert A(k + 1) and drain NUM(k).  At D = Dv = 128 S_prev is staged in
-// two 64-row halves (the second written once MMA3 has read the first), which
-// leaves shared memory for two-deep Q, K and V rings.
+// tensor pipe while the TMEM warps convert A(k + 1) and drain NUM(k).  At
+// D = Dv = 128 S_prev is staged in two 64-row halves (the second written
+// once MMA3 has read the first), which leaves shared memory for two-deep Q,
+// K and V rings.
 //
 // Every wait is bounded (clock64 budget).  On expiry the kernel sets the
 // library's device error word, raises a per-launch abort word that every
@@ -118,7 +121,6 @@ struct Plan {
     static constexpr int NSP = (2 * (2 * QB + VB) + DP * NQ16 * 2 <= kBudget) ? 1 : 2;
     static constexpr int PR = DP / NSP;      // S_prev rows per piece
     static constexpr int SB = PR * NQ16 * 2;
-    static constexpr int ZB = 0, OB = 0;     // (inside the V slots and the S_prev buffer)
     static constexpr int kFixed = SB;
     static constexpr int NS = (kFixed + 4 * (2 * QB + VB) <= kBudget)   ? 4
                               : (kFixed + 3 * (2 * QB + VB) <= kBudget) ? 3
@@ -127,10 +129,8 @@ struct Plan {
     static constexpr int Q0 = 0;
     static constexpr int K0 = Q0 + NS * QB;
     static constexpr int V0 = K0 + NS * QB;
-    static constexpr int S0 = V0 + NS * VB;
-    static constexpr int Z0 = S0 + SB;
-    static constexpr int O0 = Z0 + ZB;
-    static constexpr int TILES = O0 + OB;
+    static constexpr int S0 = V0 + NS * VB;   // S_prev (and its z block)
+    static constexpr int TILES = S0 + SB;
     static constexpr int SMEM = TILES + 1024 /* alignment */ + 1024 /* barriers */;
     // TMEM columns: state S | z; the regions R0, R1 (A, then NUM | DEN of
     // alternate chunks); the bf16 P.  Region stride: A (128 columns), then

@@ -42,11 +42,16 @@
  *  - Supported sizes: B, H, N >= 0 (a zero size is a no-op that returns
  *    LA_OK; la_forward_ex then writes zero states); D and Dv in
  *    {16, 32, 64, 128}; PRF m in {16, 32, 64, 128, 256} (else LA_ERR_FEATURE).
+ *  - Execution: bf16 inputs with elu+1 and D, Dv in {64, 128}, or with PRF,
+ *    D = 64 and (m = 128, Dv in {64, 128}) or (m = 256, Dv = 64), run on the
+ *    tensor cores (tcgen05); every other supported case (fp32, other sizes)
+ *    runs on the CUDA cores.  Both compute the same sums; rounding differs.
  *  - Scratch: la_forward may take stream-ordered scratch memory from a
  *    library-owned CUDA memory pool on the current device (per-segment
- *    states of the causal scan, partial sums of the non-causal pass); it is
- *    returned to the pool, in stream order, before the call returns.
- *    la_shutdown() releases the pools.
+ *    states of the causal scan, partial sums of the non-causal pass, the
+ *    phi(q), phi(k) tiles of random features); it is returned to the pool,
+ *    in stream order, before the call returns.  la_shutdown() releases the
+ *    pools.
  */
 #ifndef LINATTN_H
 #define LINATTN_H
