@@ -202,6 +202,24 @@ __device__ __forceinline__ bool wait_bar(uint64_t *b, uint32_t parity, const Ctl
     return true;
 }
 
+// wait_bar for a lane that shares its warp with another waiting role: naps
+// between polls so that the other lane keeps the warp's issue slots.
+__device__ __forceinline__ bool wait_bar_nap(uint64_t *b, uint32_t parity, const Ctl &c)
+{
+    if (*c.cta) return false;
+    if (mbar_try_wait(b, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(b, parity)) {
+        if (*c.cta) return false;
+        if (clock64() - t0 > kWaitBudget) {
+            raise_abort(c);
+            return false;
+        }
+        __nanosleep(128);
+    }
+    return true;
+}
+
 __device__ __forceinline__ uint32_t align1k(uint32_t a) { return (a + 1023u) & ~1023u; }
 
 // Element (row r, 16 B chunk j) of a [kC x cols] 128B-swizzled tile.
@@ -440,7 +458,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const int c0 = s * g.L, nc = min(g.L, g.NC - c0);
                 for (int c = 0; c < nc; c++, nv++) {
                     const int st = nv % NS;
-                    const bool ok = wait_bar(&out_ready[st], oc[st] & 1, ctl);
+                    const bool ok = wait_bar_nap(&out_ready[st], oc[st] & 1, ctl);
                     oc[st]++;
                     if (ok && MODE != kModeFeatPart) {
                         const uint32_t src = base + PL::V0 + st * PL::VB;
