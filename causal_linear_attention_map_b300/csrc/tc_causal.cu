@@ -68,8 +68,9 @@
 // K and V rings.
 //
 // Every wait is bounded (clock64 budget).  On expiry the kernel sets the
-// library's device error word, raises a per-launch abort word that every
-// other CTA polls, and all roles run to the end without waiting.
+// library's device error word and a per-launch abort word (the other CTAs
+// take no further item once they see it; their own waits are bounded too),
+// and all roles of the CTA run to the end without waiting.
 #include <cuda.h>
 #include <cmath>
 #include <cudaTypedefs.h>
@@ -421,7 +422,8 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 int item = -1;
                 if (role == 0) {
                     ok = it < 2 || wait_bar(&item_empty[slot], ((it >> 1) - 1) & 1, ctl);
-                    if (ok && !*abort_cta) {
+                    // no new item once any CTA of this launch has given up a wait
+                    if (ok && !*abort_cta && !*ctl.glob) {
                         item = atomicAdd(sc.ticket, 1);
                         if (item >= g.n_items) item = -1;
                     }
@@ -1104,7 +1106,7 @@ nc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (producer) {
             const bool ok = it < 2 || wait_bar(&item_empty[slot], ((it >> 1) - 1) & 1, ctl);
             int item = -1;
-            if (ok && !*abort_cta) {
+            if (ok && !*abort_cta && !*ctl.glob) {   // (not after another CTA gave up a wait)
                 item = atomicAdd(sc.ticket, 1);
                 if (item >= g.n_items) item = -1;
             }
