@@ -684,7 +684,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             tc_fence_after();
             if (srow) {
-#pragma unroll
+#pragma unroll 1
                 for (int cb = 0; cb < HALF; cb += 32) {
                     uint32_t v[32];
                     tmem_ld32_nowait(tmem + lane_base + PL::T_S + grp * HALF + cb, v);
