@@ -50,4 +50,26 @@ cudaError_t set_max_smem_once(int bytes)
     return e;
 }
 
+// Launch a kernel that depends on the previous launch in the stream as a
+// programmatic dependent launch: it may start once every block of that
+// launch has signalled (griddepcontrol.launch_dependents) or exited, and it
+// must execute griddepcontrol.wait before it reads anything that launch
+// wrote.  Its prologue then overlaps the previous kernel's tail.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args &&...args)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 }  // namespace la

@@ -331,6 +331,9 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const Ctl ctl{abort_cta, sc.abort, err};
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    // the segment-sum form is followed by the scan or the totals, launched as
+    // its dependents (every block of this grid is resident by now)
+    if constexpr (AGG) griddep_launch();
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; i++) {
@@ -829,7 +832,10 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             phi_q();   // phi(Q) of chunk 0 first: MMA1 of chunk 0 does not wait for phase B
 
             // ---- phase B: the state before this segment (the exclusive prefix of
-            // the head's earlier segments; zero for the first) -> T_S, T_Z
+            // the head's earlier segments; zero for the first) -> T_S, T_Z.  The
+            // scan that writes the prefixes may still be running (this pass is its
+            // dependent launch): wait for it here, after this warp's first phi(Q).
+            griddep_wait();
             if (srow) {
                 const float4 *src = reinterpret_cast<const float4 *>(sc.preS + slot_id * DP * DV +
                                                                      (long long)r * DV + grp * HALF);
@@ -1241,6 +1247,7 @@ nc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const int c0 = s * g.L, nc = min(g.L, g.NC - c0);
             // S (bf16) and ZP for this head, once the last item's products are done
             if (ni > 0) wait_bar(s_free, (ni - 1) & 1, ctl);
+            griddep_wait();   // the totals kernel (this grid's prerequisite) has completed
             for (int row = r; row < DP; row += kC) {   // the head's totals (sc.preS, sc.prez: [BH, DP, DV], [BH, DP])
                 const float *src = sc.preS + (long long)h * DP * DV + (long long)row * DV + grp * HALF;
 #pragma unroll
@@ -1318,6 +1325,8 @@ __global__ void nc_total_kernel(const float *__restrict__ preS, const float *__r
                                 int szS, int szz, float *__restrict__ totS, float *__restrict__ totz,
                                 int tot_szS, int tot_szz, int offS, int offz)
 {
+    griddep_launch();
+    griddep_wait();   // the segment sums are complete
     const long long head = blockIdx.y;
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
     const float *p;
@@ -1677,6 +1686,8 @@ Geo plan(long long BH, int N, int sms)
 __global__ void seg_scan_kernel(float *__restrict__ preS, float *__restrict__ prez, int nseg, int szS,
                                 int szz)
 {
+    griddep_launch();
+    griddep_wait();   // the segment sums are complete
     const long long head = blockIdx.y;
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
     float *p;
@@ -1765,16 +1776,23 @@ cudaError_t run_causal(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
             tq, tk, tv_agg, to, ga, sc, (__nv_bfloat16 *)out, nullptr, nullptr, err);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         const int sz = DP * DV + DP;
-        seg_scan_kernel<<<dim3(cdiv(sz, 256), (unsigned)g.BH), 256, 0, s>>>(sc.preS, sc.prez, g.nseg,
-                                                                           DP * DV, DP);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = launch_dependent(seg_scan_kernel, dim3(cdiv(sz, 256), (unsigned)g.BH), dim3(256), 0, s, sc.preS,
+                                  sc.prez, g.nseg, DP * DV, DP)) != cudaSuccess)
+            return e;
         launches += 2;
     }
     sc.ticket = (int *)((unsigned char *)scratch + 8);   // the output pass's own ticket
     // pass 2: the chunk recurrence of every segment from its prefix
-    tc_causal_kernel<DP, DV, false, MODE><<<min(g.n_items, sms), kThreads, PL::SMEM, s>>>(
-        tq, tk, tv, to, g, sc, (__nv_bfloat16 *)out, S_out, z_out, err);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // (after the scan: a dependent launch, whose phase B waits for the scan)
+    if (g.nseg > 1) {
+        e = launch_dependent(tc_causal_kernel<DP, DV, false, MODE>, dim3(min(g.n_items, sms)), dim3(kThreads),
+                             PL::SMEM, s, tq, tk, tv, to, g, sc, (__nv_bfloat16 *)out, S_out, z_out, err);
+    } else {
+        tc_causal_kernel<DP, DV, false, MODE><<<min(g.n_items, sms), kThreads, PL::SMEM, s>>>(
+            tq, tk, tv, to, g, sc, (__nv_bfloat16 *)out, S_out, z_out, err);
+        e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) return e;
     note_launches(launches + 1);
     return cudaSuccess;
 }
@@ -1797,9 +1815,10 @@ cudaError_t run_totals(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
         tq, tk, tv_agg, to, g, sc, nullptr, nullptr, nullptr, err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int sz = DP * DV + DP;
-    nc_total_kernel<<<dim3(cdiv(sz, 256), (unsigned)g.BH), 256, 0, s>>>(
-        sc.preS, sc.prez, g.nseg, DP * DV, DP, totS, totz, tot_rows * DV, tot_rows, row_off * DV, row_off);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_dependent(nc_total_kernel, dim3(cdiv(sz, 256), (unsigned)g.BH), dim3(256), 0, s,
+                              (const float *)sc.preS, (const float *)sc.prez, g.nseg, DP * DV, DP, totS, totz,
+                              tot_rows * DV, tot_rows, row_off * DV, row_off)) != cudaSuccess)
+        return e;
     note_launches(2);
     return cudaSuccess;
 }
@@ -1817,8 +1836,10 @@ cudaError_t run_readout(const CUtensorMap &tq, const CUtensorMap &to, Geo g, voi
     cudaError_t e;
     if ((e = set_max_smem_once<nc_out_kernel<DP, DV, PHI>>(NP::SMEM)) != cudaSuccess)
         return e;
-    nc_out_kernel<DP, DV, PHI><<<min(g.n_items, num_sms()), kNcThreads, NP::SMEM, s>>>(tq, to, g, sc, err);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // (after the totals kernel: a dependent launch that waits for it before reading S, z)
+    if ((e = launch_dependent(nc_out_kernel<DP, DV, PHI>, dim3(min(g.n_items, num_sms())), dim3(kNcThreads),
+                              NP::SMEM, s, tq, to, g, sc, err)) != cudaSuccess)
+        return e;
     note_launches(1);
     return cudaSuccess;
 }
