@@ -29,9 +29,9 @@ LA_OK = 0
 STATUS_NAMES = {0: "LA_OK", -1: "LA_ERR_NULL", -2: "LA_ERR_DIM", -3: "LA_ERR_DTYPE",
                 -4: "LA_ERR_FEATURE", -5: "LA_ERR_CUDA", -6: "LA_ERR_TIMEOUT",
                 -7: "LA_ERR_ALIGN"}
-EXPORTED = ("la_forward", "la_forward_ex", "la_step", "la_status_string", "la_check",
-            "la_shutdown", "la_version", "la_launch_count", "la_forward_noncausal_noalloc",
-            "la_selftest_timeout")
+EXPORTED = ("la_forward", "la_forward_ex", "la_forward_host", "la_step", "la_status_string",
+            "la_check", "la_shutdown", "la_version", "la_launch_count",
+            "la_forward_noncausal_noalloc", "la_selftest_timeout")
 
 _DT = {torch.float32: LA_F32, torch.bfloat16: LA_BF16}
 
@@ -91,6 +91,8 @@ def load(path: str | None = None):
     lib.la_forward.restype = i
     lib.la_forward_ex.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, fm, i, vp, vp, vp]
     lib.la_forward_ex.restype = i
+    lib.la_forward_host.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, fm, i, vp]
+    lib.la_forward_host.restype = i
     lib.la_step.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, fm, i, vp]
     lib.la_step.restype = i
     lib.la_status_string.argtypes = [i]
@@ -134,6 +136,20 @@ def _check_tensors(*ts):
     for t in ts:
         if not t.is_cuda:
             raise ValueError("tensors must be CUDA tensors")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+        if t.dtype != dt:
+            raise ValueError("q, k, v, out must share one dtype")
+    if dt not in _DT:
+        raise ValueError(f"unsupported dtype {dt}")
+    return _DT[dt]
+
+
+def _check_host_tensors(*ts):
+    dt = ts[0].dtype
+    for t in ts:
+        if t.is_cuda:
+            raise ValueError("la_forward_host takes host (CPU) tensors")
         if not t.is_contiguous():
             raise ValueError("tensors must be contiguous")
         if t.dtype != dt:
@@ -189,6 +205,25 @@ def la_forward(q, k, v, causal=True, feature_map: FeatureMap | None = None, out=
     _, fmp = _fm(feature_map)
     st = load().la_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                            B, H, N, D, Dv, int(bool(causal)), fmp, dt, _stream(stream))
+    _raise(st)
+    return out
+
+
+def la_forward_host(q, k, v, causal=True, feature_map: FeatureMap | None = None, out=None,
+                    stream=None):
+    """la_forward_host: q, k, v and out in host memory (pinned for overlapped
+    copies; ``out`` is allocated pinned when not given).  ``out`` holds the
+    result once ``stream`` has been synchronised."""
+    B, H, N, D = q.shape
+    Dv = v.shape[-1]
+    if k.shape != q.shape or tuple(v.shape[:3]) != (B, H, N):
+        raise ValueError("shape mismatch between q, k, v")
+    if out is None:
+        out = torch.empty((B, H, N, Dv), dtype=q.dtype, pin_memory=True)
+    dt = _check_host_tensors(q, k, v, out)
+    _, fmp = _fm(feature_map)
+    st = load().la_forward_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                B, H, N, D, Dv, int(bool(causal)), fmp, dt, _stream(stream))
     _raise(st)
     return out
 

@@ -23,6 +23,7 @@ struct DeviceCtx {
     bool pool_ready = false;
     cudaMemPool_t pool = nullptr;
     int *err_word = nullptr;   // device int: set by kernels whose bounded waits ran out
+    cudaStream_t h2d = nullptr, d2h = nullptr;   // la_forward_host copy streams (created on first use)
 };
 
 std::mutex g_mu;
@@ -156,6 +157,103 @@ int forward_impl(const void *q, const void *k, const void *v, void *out, int B, 
     return cuda_status(e != cudaSuccess ? e : e2);
 }
 
+// la_forward_host: at most kHostGroups head groups, each with at least
+// kHostGroupBytes of inputs (a group's forward has a fixed cost of a few
+// launches, so small problems take few groups)
+constexpr int kHostGroups = 16;
+constexpr size_t kHostGroupBytes = 16u << 20;
+
+// The copy streams of la_forward_host on this device (created once).
+int host_streams(DeviceCtx *c)
+{
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (c->h2d && c->d2h) return LA_OK;
+    if (!c->h2d && cudaStreamCreateWithFlags(&c->h2d, cudaStreamNonBlocking) != cudaSuccess)
+        return cuda_status(cudaErrorUnknown);
+    if (!c->d2h && cudaStreamCreateWithFlags(&c->d2h, cudaStreamNonBlocking) != cudaSuccess)
+        return cuda_status(cudaErrorUnknown);
+    return LA_OK;
+}
+
+size_t round256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+int forward_host_impl(const void *q, const void *k, const void *v, void *out, int B, int H, int N, int D,
+                      int Dv, int causal, const la_feature_map *fm, int dtype, void *stream)
+{
+    int kind, m, P;
+    const float *W;
+    int st = check_common(B, H, D, Dv, fm, dtype, &kind, &m, &W, &P);
+    if (st != LA_OK) return st;
+    if (N < 0) return LA_ERR_DIM;
+    const long long BH = (long long)B * H;
+    if (BH > 0x7fffffffLL) return LA_ERR_DIM;
+    if (BH == 0 || N == 0) return LA_OK;   // nothing to copy or compute
+    if (!q || !k || !v || !out) return LA_ERR_NULL;
+    DeviceCtx *ctx = nullptr;
+    if ((st = get_ctx(&ctx)) != LA_OK) return st;
+    if ((st = host_streams(ctx)) != LA_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+
+    const size_t es = dtype == LA_F32 ? 4 : 2;
+    const size_t qh = (size_t)N * D * es, vh = (size_t)N * Dv * es;   // bytes per head
+    const size_t oq = 0, ok = round256(BH * qh), ov = ok + round256(BH * qh), oo = ov + round256(BH * vh);
+    const size_t total = oo + round256(BH * vh);
+    const size_t in_bytes = BH * (2 * qh + vh);
+    long long want = (long long)(in_bytes / kHostGroupBytes);
+    want = want < 1 ? 1 : want > kHostGroups ? kHostGroups : want;
+    const long long hg = (BH + want - 1) / want;   // heads per group
+    const int G = (int)((BH + hg - 1) / hg);
+
+    // events: the buffer is allocated; per group its inputs are in, its outputs are out
+    cudaEvent_t ev[2 * kHostGroups + 2] = {};
+    const int nev = 2 * G + 2;
+    for (int i = 0; i < nev; i++)
+        if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) {
+            for (int j = 0; j < i; j++) cudaEventDestroy(ev[j]);
+            return cuda_status(cudaErrorUnknown);
+        }
+    cudaEvent_t ev_alloc = ev[0], ev_done = ev[1], *ev_in = ev + 2, *ev_fw = ev + 2 + G;
+
+    unsigned char *d = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync((void **)&d, total, ctx->pool, s);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_alloc, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->h2d, ev_alloc, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->d2h, ev_alloc, 0);
+    for (int g = 0; g < G && e == cudaSuccess && st == LA_OK; g++) {
+        const long long h0 = g * hg, nh = BH - h0 < hg ? BH - h0 : hg;
+        const size_t bq = h0 * qh, bv = h0 * vh;
+        e = cudaMemcpyAsync(d + oq + bq, (const unsigned char *)q + bq, nh * qh, cudaMemcpyHostToDevice, ctx->h2d);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(d + ok + bq, (const unsigned char *)k + bq, nh * qh, cudaMemcpyHostToDevice,
+                                ctx->h2d);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(d + ov + bv, (const unsigned char *)v + bv, nh * vh, cudaMemcpyHostToDevice,
+                                ctx->h2d);
+        if (e == cudaSuccess) e = cudaEventRecord(ev_in[g], ctx->h2d);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev_in[g], 0);
+        if (e != cudaSuccess) break;
+        // the group's heads as B = 1, H = nh (heads are contiguous in [B, H, N, .])
+        st = forward_impl(d + oq + bq, d + ok + bq, d + ov + bv, d + oo + bv, 1, (int)nh, N, D, Dv, causal, fm,
+                          dtype, stream, nullptr, nullptr);
+        if (st != LA_OK) break;
+        e = cudaEventRecord(ev_fw[g], s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->d2h, ev_fw[g], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync((unsigned char *)out + bv, d + oo + bv, nh * vh, cudaMemcpyDeviceToHost, ctx->d2h);
+    }
+    // join both copy streams back into `stream` (also after a failure, so that
+    // the buffer is released only once nothing uses it), then release it
+    cudaError_t e2 = cudaEventRecord(ev_done, ctx->d2h);
+    if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(s, ev_done, 0);
+    cudaEvent_t ev_in_done = ev_alloc;   // reused: the last host-to-device copy
+    if (e2 == cudaSuccess) e2 = cudaEventRecord(ev_in_done, ctx->h2d);
+    if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(s, ev_in_done, 0);
+    if (d && e2 == cudaSuccess) e2 = cudaFreeAsync(d, s);
+    for (int i = 0; i < nev; i++) cudaEventDestroy(ev[i]);   // released once they have completed
+    if (st != LA_OK) return st;
+    return cuda_status(e != cudaSuccess ? e : e2);
+}
+
 }  // namespace
 
 extern "C" {
@@ -172,6 +270,12 @@ int la_forward_ex(const void *q, const void *k, const void *v, void *out, int B,
                   float *S_out, float *z_out)
 {
     return forward_impl(q, k, v, out, B, H, N, D, Dv, causal, fm, dtype, stream, S_out, z_out);
+}
+
+int la_forward_host(const void *q, const void *k, const void *v, void *out, int B, int H, int N, int D,
+                    int Dv, int causal, const la_feature_map *fm, int dtype, void *stream)
+{
+    return forward_host_impl(q, k, v, out, B, H, N, D, Dv, causal, fm, dtype, stream);
 }
 
 int la_step(float *S, float *z, const void *q, const void *k, const void *v, void *out, int B,
@@ -244,6 +348,8 @@ void la_shutdown(void)
         cudaDeviceSynchronize();
         cudaMemPoolDestroy(c.pool);
         cudaFree(c.err_word);
+        if (c.h2d) cudaStreamDestroy(c.h2d);
+        if (c.d2h) cudaStreamDestroy(c.d2h);
         c = DeviceCtx();
     }
     if (have_cur) cudaSetDevice(cur);

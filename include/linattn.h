@@ -117,6 +117,30 @@ int la_forward_ex(const void *q, const void *k, const void *v, void *out,
                   float *S_out, float *z_out);
 
 /*
+ * la_forward_host -- la_forward with q, k, v (inputs) and out (output) in
+ * host memory, same layouts; the feature map's W stays in device memory.
+ * The B*H heads are split into up to 16 groups of consecutive heads, which
+ * flow through three stages on three streams: the host-to-device copy of
+ * a group's q, k, v (a library stream), its forward (on `stream`) and the
+ * device-to-host copy of its out (a second library stream).  So the copies
+ * in both directions and the compute overlap, and a step costs about its
+ * larger copy direction.  Device buffers for the whole problem come from
+ * the library's stream-ordered pool and go back to it at the end.
+ * Ordering: the first copy starts after the work queued on `stream` before
+ * the call, and work queued on `stream` after the call starts after the last
+ * copy has completed.  The host buffers must stay valid, and unmodified, until
+ * then (synchronise `stream`).  Page-locked host buffers (cudaHostAlloc,
+ * cudaHostRegister) give overlapped asynchronous copies; pageable ones give
+ * the same results with the copies staged by the driver.  Each group's
+ * segments are planned for that group alone, so outputs equal la_forward's
+ * within the parity tolerances (not bit for bit).  Status codes as
+ * la_forward; a host pointer the driver rejects gives LA_ERR_CUDA.
+ */
+int la_forward_host(const void *q, const void *k, const void *v, void *out,
+                    int B, int H, int N, int D, int Dv, int causal,
+                    const la_feature_map *fm, int dtype, void *stream);
+
+/*
  * la_step -- one recurrent decode step for B*H independent heads ("proposed
  * method", bullet 5; "main results", bullet 3: the state is updated
  * incrementally).  In place on the fp32 memories:

@@ -121,6 +121,45 @@ def test_step_matches_oracle_and_forward(la, feature, m, dtype):
     assert_state_close(np64(z), zref, 1e-5, what="z after steps")
 
 
+HOST_CASES = [
+    # (N, D, Dv, B, H, feature, m, dtype, causal).  Groups take >= 16 MB of
+    # inputs: 19 heads of 6.3 MB -> 7 groups of 3, 3, ..., 1 heads; 32 heads
+    # of 1.6 MB -> 3 groups of 11, 11, 10; then single-group problems with
+    # random features and on the CUDA-core path
+    (8192 + 5, 128, 128, 1, 19, "elu1", 0, "bf16", True),
+    (4096, 64, 64, 4, 8, "elu1", 0, "bf16", False),
+    (1000, 64, 64, 1, 2, "prf", 256, "bf16", True),
+    (300, 32, 32, 1, 3, "elu1", 0, "f32", True),
+]
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("case", HOST_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_forward_host_buffers(la, case, pinned):
+    """la_forward_host: host q, k, v in and out, head groups pipelined
+    through the copies and the forward; element-wise parity with the oracle
+    (pageable buffers too, where the driver stages the copies)."""
+    N, D, Dv, B, H, feature, m, dtype, causal = case
+    w = wl.small(B=B, H=H, N=N, D=D, Dv=Dv, causal=causal, feature=feature, m=m, dtype=dtype,
+                 scaled=dtype == "bf16", seed=N * 3 + D)
+    q, k, v = wl.make_qkv(w)
+    W = wl.make_W(m, D) if feature == "prf" else None
+    fm = la.FeatureMap("prf", W.cuda()) if W is not None else None
+    if pinned:
+        hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+        hout = None
+    else:
+        hq, hk, hv = q, k, v
+        hout = torch.full((B, H, N, Dv), float("nan"), dtype=q.dtype)
+    out = la.la_forward_host(hq, hk, hv, causal=causal, feature_map=fm, out=hout)
+    torch.cuda.synchronize()
+    assert not out.is_cuda
+    ref = oracle.forward(np64(q), np64(k), np64(v), causal=causal, feature=feature,
+                         W=W.double().numpy() if W is not None else None)
+    ref = ref[0] if isinstance(ref, tuple) else ref
+    assert_close(np64(out), ref, dtype, what=f"host {case} pinned={pinned}")
+
+
 def test_resume_forward_then_step(la):
     """forward_ex over N1 positions exports (S, z); steps continue from it."""
     B, H, N, N1, D, Dv = 1, 2, 300, 257, 64, 64
