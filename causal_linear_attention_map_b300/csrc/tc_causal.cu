@@ -385,9 +385,10 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
     if (warp == kProducerWarp || warp == kKWarp || warp == kVWarp) {
         // ---------------------------------------- Q / K / V tile producers
-        // The Q producer also hands out the items.  Phase A streams the
-        // segment's K, V from HBM (kept in L2 for phase C); phase C reads Q
-        // from HBM and K, V again (from L2 when phase A ran).
+        // The Q producer also hands out the items.  The segment-sum form
+        // streams a segment's K, V; the output form streams its Q, K, V (K
+        // and V a second time: the two passes are too far apart for L2 to
+        // keep them).
         if (lane == 0) {
             const int role = warp - kProducerWarp;   // 0 Q, 1 K, 2 V
             const CUtensorMap *tm = role == 0 ? &tm_q : role == 1 ? &tm_k : &tm_v;
@@ -491,7 +492,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             constexpr uint32_t lbo_v = kC * 32, lbo_s = PR * 32;   // 16-column block strides (32B swizzle)
             constexpr uint32_t lbo_kT = DP == 128 ? kC * 128 : 0;   // DP = 64: rows 64-127 repeat 0-63
             const uint32_t s_addr = base + PL::S0;
-            uint32_t nkv = 0;    // K / V ring loads consumed (phase A and C)
+            uint32_t nkv = 0;    // K / V ring loads consumed
             uint32_t nq = 0;     // Q ring loads consumed
             uint32_t ndone = 0;  // phase-C chunks whose MMA2 has been issued (global chunk index)
             uint32_t nfree[2] = {0, 0};   // num_free phases seen per region
@@ -676,7 +677,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const uint32_t z_addr = s_addr + (DV / 16) * (PR * 32);   // the z block after S_prev's blocks
         uint32_t kg = 0;      // global index of the next chunk whose A is read
         uint32_t nkt = 0;     // K ring position (segment-sum form: this warp's share of phi(K))
-        uint32_t nvr = 0;     // V ring position (phase A and C tiles)
+        uint32_t nvr = 0;     // V ring position
         uint32_t nsp = 0;     // S_prev copies made (one per chunk)
         uint32_t nsd = 0;     // s_done phases consumed
 
@@ -1661,11 +1662,10 @@ int num_sms()
     return g_num_sms;
 }
 
-// Segment length L (chunks): the estimated makespan, in chunk-times, is
-// waves * (L + [segmented] (L / 2 + 1)): phase C costs one chunk-time per
-// chunk, phase A half of that (k, v only), and the chain about one more.
-// Segments per head: enough items to give every SM one (one wave), and no
-// segmentation once B*H alone fills the GPU.
+// Segments per head: enough (head, segment) items to give every SM one (one
+// wave of the persistent grid), and no segmentation once B*H alone fills
+// the GPU.  The output pass's time is about L chunk-times, the segment-sum
+// pass adds about a third of that, so the forward scales with L.
 Geo plan(long long BH, int N, int sms)
 {
     Geo g;
