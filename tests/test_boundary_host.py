@@ -107,3 +107,25 @@ def test_step_validation_codes(lib):
     assert st(ptrs=p[:5] + [0]) == -1
     assert st(ptrs=[FAKE + 8] + p[1:]) == -7
     assert st(B=0) == 0
+
+
+def test_host_forward_validation_codes(lib):
+    """la_forward_host validates like la_forward before anything is enqueued
+    (host pointers are not dereferenced on these paths)."""
+    import causal_linear_attention_map_b300 as la
+
+    p = (FAKE, FAKE + 4096, FAKE + 8192, FAKE + 12288)
+
+    def hf(*, B=1, H=1, N=8, D=64, Dv=64, fm=None, dtype=1, ptrs=p):
+        fmp = ctypes.byref(fm) if fm is not None else None
+        return lib.la_forward_host(*ptrs, B, H, N, D, Dv, 1, fmp, dtype, None)
+
+    assert hf(dtype=3) == -3
+    assert hf(D=48) == -2
+    assert hf(N=-1) == -2
+    assert hf(fm=la.la_feature_map(1, 64, None)) == -4
+    assert hf(ptrs=(FAKE, 0, FAKE, FAKE)) == -1
+    assert hf(ptrs=(FAKE, FAKE, FAKE, 0)) == -1
+    # nothing to copy or compute: succeeds without touching the device
+    assert hf(B=0) == 0
+    assert hf(N=0, ptrs=(0, 0, 0, 0)) == 0
