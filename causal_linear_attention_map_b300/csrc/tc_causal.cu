@@ -117,18 +117,22 @@ struct Plan {
     // about the same for N = 16 as for N = 144 with these operands).
     static constexpr int NQ16 = DV + 16;
     static constexpr int VB = kC * NQ16 * 2;   // one V slot: DV / 16 blocks + ONES
+    // DP = 256 (both halves of a 256-feature map at once) runs only in the
+    // segment-sum form: no Q ring and no S_prev buffer
+    static constexpr bool kSumOnly = DP > 128;
     // S_prev pieces along Dphi: one, or two 64-row halves when that is what
     // lets two-deep rings fit (each piece with its own z block)
-    static constexpr int NSP = (2 * (2 * QB + VB) + DP * NQ16 * 2 <= kBudget) ? 1 : 2;
+    static constexpr int NSP = kSumOnly || (2 * (2 * QB + VB) + DP * NQ16 * 2 <= kBudget) ? 1 : 2;
     static constexpr int PR = DP / NSP;      // S_prev rows per piece
-    static constexpr int SB = PR * NQ16 * 2;
+    static constexpr int SB = kSumOnly ? 0 : PR * NQ16 * 2;
     static constexpr int kFixed = SB;
-    static constexpr int NS = (kFixed + 4 * (2 * QB + VB) <= kBudget)   ? 4
-                              : (kFixed + 3 * (2 * QB + VB) <= kBudget) ? 3
-                                                                         : 2;
-    static_assert(kFixed + 2 * (2 * QB + VB) <= kBudget, "no two-deep rings");
+    static constexpr int STAGE = (kSumOnly ? 1 : 2) * QB + VB;   // ring bytes per stage
+    static constexpr int NS = (kFixed + 4 * STAGE <= kBudget)   ? 4
+                              : (kFixed + 3 * STAGE <= kBudget) ? 3
+                                                                : 2;
+    static_assert(kFixed + 2 * STAGE <= kBudget, "no two-deep rings");
     static constexpr int Q0 = 0;
-    static constexpr int K0 = Q0 + NS * QB;
+    static constexpr int K0 = Q0 + (kSumOnly ? 0 : NS * QB);
     static constexpr int V0 = K0 + NS * QB;
     static constexpr int S0 = V0 + NS * VB;   // S_prev (and its z block)
     static constexpr int TILES = S0 + SB;
@@ -142,8 +146,15 @@ struct Plan {
     static constexpr int T_P = T_R0 + 2 * RS;               // the bf16 P
     // 32-column TMEM accesses at multiples of 32 use one x32 op, else two x16
     static constexpr bool ALN32 = T_R0 % 32 == 0 && RS % 32 == 0 && T_P % 32 == 0;
+    // segment-sum form: the segment's S | z (one block of DV + 16 columns per
+    // 128 feature rows) in one of two regions that alternate between items
+    static constexpr int NRB = DP > 128 ? DP / 128 : 1;
+    static constexpr int SUM_COL0 = kSumOnly ? 0 : T_R0;
+    static constexpr int SUM_STRIDE = kSumOnly ? NRB * NQ16 : RS;
+    static constexpr bool SUM_ALN32 = kSumOnly ? false : ALN32;
     static constexpr int TMEM_COLS = 512;
     static_assert(T_P + kC / 2 <= TMEM_COLS, "TMEM plan too large");
+    static_assert(SUM_COL0 + 2 * SUM_STRIDE <= TMEM_COLS, "TMEM plan too large");
     static_assert(SMEM <= 227 * 1024, "shared memory plan too large");
     static_assert(SMEM > 114 * 1024, "one CTA per SM: the kernel holds all 512 TMEM columns");
 };
@@ -162,6 +173,8 @@ struct Scratch {
     float *prez;     // [BH, nseg, DP]
     float *num_part; // [BH, N, DV] fp32: first feature half's NUM (split feature maps)
     float *den_part; // [BH, N]
+    int pre_rows;    // feature rows per prefix slot (split feature maps: both halves' rows,
+    int pre_off;     // this pass's from row pre_off); else DP and 0
 };
 
 // What the kernel applies to the Q and K tiles and how it finishes a chunk.
@@ -490,7 +503,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             constexpr uint32_t id_qs = idesc_bf16(128, PL::NQ16, 0, 1);
             constexpr uint32_t id_kv = idesc_bf16(128, PL::NQ16, 1, 1);
             constexpr uint32_t lbo_v = kC * 32, lbo_s = PR * 32;   // 16-column block strides (32B swizzle)
-            constexpr uint32_t lbo_kT = DP == 128 ? kC * 128 : 0;   // DP = 64: rows 64-127 repeat 0-63
+            constexpr uint32_t lbo_kT = DP >= 128 ? kC * 128 : 0;   // DP = 64: rows 64-127 repeat 0-63
             const uint32_t s_addr = base + PL::S0;
             uint32_t nkv = 0;    // K / V ring loads consumed
             uint32_t nq = 0;     // Q ring loads consumed
@@ -537,7 +550,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     // denominator slot, once the TMEM warps have read item it - 2's
                     const int rr = it & 1;
                     if (it >= 2) wait_bar(&sloc_read[rr], ((it >> 1) - 1) & 1, ctl);
-                    const uint32_t dS = tmem + PL::T_R0 + rr * PL::RS;   // S | z of the segment
+                    const uint32_t dS = tmem + PL::SUM_COL0 + rr * PL::SUM_STRIDE;   // S | z of the segment
                     for (int c = 0; c < nc; c++) {
                         const int st = nkv % NS;
                         wait_bar(&k_ready[st], (nkv / NS) & 1, ctl);
@@ -551,15 +564,19 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             constexpr uint32_t id_z = idesc_bf16(128, 16, 1, 1);
                             const uint32_t ones = va + DV * kC * 2;
 #pragma unroll
-                            for (int k = 0; k < kC; k += 16)
-                                mma_bf16_ss(dS, sw128_desc(ka + (k / 8) * 1024, lbo_kT, 1024),
-                                            sw128_desc(va + (k / 8) * 1024, kC * 128, 1024), id_s,
-                                            (c > 0 || k > 0) ? 1u : 0u);
+                            for (int rb = 0; rb < PL::NRB; rb++) {   // 128 feature rows (two K boxes) each
+                                const uint32_t kb = ka + rb * 2 * (kC * 128), d = dS + rb * PL::NQ16;
 #pragma unroll
-                            for (int k = 0; k < kC; k += 16)
-                                mma_bf16_ss(dS + DV, sw128_desc(ka + (k / 8) * 1024, lbo_kT, 1024),
-                                            sw32_desc(ones + (k / 8) * 256, 256, 256), id_z,
-                                            (c > 0 || k > 0) ? 1u : 0u);
+                                for (int k = 0; k < kC; k += 16)
+                                    mma_bf16_ss(d, sw128_desc(kb + (k / 8) * 1024, lbo_kT, 1024),
+                                                sw128_desc(va + (k / 8) * 1024, kC * 128, 1024), id_s,
+                                                (c > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+                                for (int k = 0; k < kC; k += 16)
+                                    mma_bf16_ss(d + DV, sw128_desc(kb + (k / 8) * 1024, lbo_kT, 1024),
+                                                sw32_desc(ones + (k / 8) * 256, 256, 256), id_z,
+                                                (c > 0 || k > 0) ? 1u : 0u);
+                            }
                         }
                         mma_commit(&k_empty[st]);
                         mma_commit(&v_empty[st]);
@@ -802,25 +819,30 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 wait_bar(sloc_done, it & 1, ctl);
                 tc_fence_after();
                 if (srow) {
-                    float4 *dst = reinterpret_cast<float4 *>(sc.preS + slot_id * DP * DV + (long long)r * DV +
-                                                             grp * HALF);
 #pragma unroll
-                    for (int cb = 0; cb < HALF; cb += 32) {
-                        uint32_t l[32];
-                        tmem_ld32c<PL::ALN32>(tmem + lane_base + PL::T_R0 + rr * PL::RS + grp * HALF + cb, l);
-                        tmem_ld_wait();
+                    for (int rb = 0; rb < PL::NRB; rb++) {   // feature rows r + 128 rb
+                        const int row = r + 128 * rb;
+                        const uint32_t src = tmem + lane_base + PL::SUM_COL0 + rr * PL::SUM_STRIDE + rb * PL::NQ16;
+                        float4 *dst = reinterpret_cast<float4 *>(sc.preS + slot_id * DP * DV + (long long)row * DV +
+                                                                 grp * HALF);
 #pragma unroll
-                        for (int i = 0; i < 8; i++)
-                            __stcg(dst + cb / 4 + i,
-                                   make_float4(__uint_as_float(l[4 * i]), __uint_as_float(l[4 * i + 1]),
-                                               __uint_as_float(l[4 * i + 2]), __uint_as_float(l[4 * i + 3])));
-                    }
-                    if (grp == 0) {
-                        uint32_t d[16];
-                        // z of the segment: the columns after S in the region
-                        tmem_ld16_nowait(tmem + lane_base + PL::T_R0 + rr * PL::RS + DV, d);
-                        tmem_ld_wait();
-                        __stcg(sc.prez + slot_id * DP + r, __uint_as_float(d[0]));
+                        for (int cb = 0; cb < HALF; cb += 32) {
+                            uint32_t l[32];
+                            tmem_ld32c<PL::SUM_ALN32>(src + grp * HALF + cb, l);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int i = 0; i < 8; i++)
+                                __stcg(dst + cb / 4 + i,
+                                       make_float4(__uint_as_float(l[4 * i]), __uint_as_float(l[4 * i + 1]),
+                                                   __uint_as_float(l[4 * i + 2]), __uint_as_float(l[4 * i + 3])));
+                        }
+                        if (grp == 0) {
+                            uint32_t d[16];
+                            // z of the segment: the columns after S in the block
+                            tmem_ld16_nowait(src + DV, d);
+                            tmem_ld_wait();
+                            __stcg(sc.prez + slot_id * DP + row, __uint_as_float(d[0]));
+                        }
                     }
                 }
                 tc_fence_before();
@@ -837,9 +859,11 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // scan that writes the prefixes may still be running (this pass is its
             // dependent launch): wait for it here, after this warp's first phi(Q).
             griddep_wait();
+            // (split feature maps: the prefix slots hold both halves' feature rows)
+            const int prs = MODE >= kModeFeatPart ? sc.pre_rows : DP, pro = MODE >= kModeFeatPart ? sc.pre_off : 0;
             if (srow) {
-                const float4 *src = reinterpret_cast<const float4 *>(sc.preS + slot_id * DP * DV +
-                                                                     (long long)r * DV + grp * HALF);
+                const float4 *src = reinterpret_cast<const float4 *>(sc.preS + slot_id * prs * DV +
+                                                                     (long long)(pro + r) * DV + grp * HALF);
 #pragma unroll
                 for (int cb = 0; cb < HALF; cb += 32) {
                     uint32_t v[32];
@@ -854,7 +878,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     tmem_st32_nowait(tmem + lane_base + PL::T_S + grp * HALF + cb, v);
                 }
                 if (grp == 0) {
-                    const float zprev = s > 0 ? __ldcg(sc.prez + slot_id * DP + r) : 0.f;
+                    const float zprev = s > 0 ? __ldcg(sc.prez + slot_id * prs + pro + r) : 0.f;
                     uint32_t zw[16];
 #pragma unroll
                     for (int i = 0; i < 16; i++) zw[i] = i < 8 ? __float_as_uint(zprev) : 0u;
@@ -1739,6 +1763,8 @@ Scratch carve(void *scratch, const Geo &g)
     sc.prez = sc.preS + (size_t)g.BH * g.nseg * DP * DV;
     sc.num_part = nullptr;
     sc.den_part = nullptr;
+    sc.pre_rows = DP;
+    sc.pre_off = 0;
     return sc;
 }
 
@@ -1902,7 +1928,10 @@ PrfLayout prf_layout(const Problem &p, const Geo &g, bool causal)
     L.part = L.phi_k + up256(R * p.m * 2);
     const size_t part = (causal && p.m == 256) ? up256(R * p.Dv * 4) + up256(R * 4) : 0;
     L.half = L.part + part;
-    const size_t seg = p.Dv == 64 ? seg_scratch_bytes<128, 64>(g, !causal) : seg_scratch_bytes<128, 128>(g, !causal);
+    // (causal m = 256: one prefix slot holds both feature halves' rows)
+    const size_t seg = causal && p.m == 256 ? seg_scratch_bytes<256, 64>(g, false)
+                       : p.Dv == 64         ? seg_scratch_bytes<128, 64>(g, !causal)
+                                            : seg_scratch_bytes<128, 128>(g, !causal);
     L.tot = L.half + seg;
     L.total = L.tot + (causal ? 0 : up256((size_t)g.BH * ((size_t)p.m * p.Dv + p.m) * 4));
     return L;
@@ -1926,6 +1955,67 @@ cudaError_t run_prf_phi(const Problem &p, void *phq, void *phk, int *err, cudaSt
                                                                              err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     note_launches(1);
+    return cudaSuccess;
+}
+
+// Causal m = 256 over materialised phi tiles: one segment-sum pass over all
+// 256 features (S as two 128-row blocks; V read once), one scan, then the
+// output pass of the first 128-feature half (un-normalised sums to
+// num_part, den_part) and that of the second (adds them and divides).  The
+// prefix slots hold 256 feature rows; each output pass reads its half.
+template <int DV>
+cudaError_t run_causal_split(const CUtensorMap (&tq)[2], const CUtensorMap (&tk)[2], const CUtensorMap &tk_all,
+                             const CUtensorMap &tv, const CUtensorMap &tv_agg, const CUtensorMap &to, Geo g,
+                             void *scratch, float *num_part, float *den_part, void *out, float *S_out,
+                             float *z_out, int *err, cudaStream_t s)
+{
+    using PA = Plan<256, DV>;
+    using PL = Plan<128, DV>;
+    const int sms = num_sms();
+    Scratch sc = carve<256, DV>(scratch, g);
+    sc.num_part = num_part;
+    sc.den_part = den_part;
+    cudaError_t e;
+    int launches = 0;
+    if ((e = set_max_smem_once<tc_causal_kernel<256, DV, true, kModeFeat>>(PA::SMEM)) != cudaSuccess ||
+        (e = set_max_smem_once<tc_causal_kernel<128, DV, false, kModeFeatPart>>(PL::SMEM)) != cudaSuccess ||
+        (e = set_max_smem_once<tc_causal_kernel<128, DV, false, kModeFeatComb>>(PL::SMEM)) != cudaSuccess)
+        return e;
+    // the 16-byte header: segment-sum ticket (+0), abort word (+4), the two
+    // output passes' tickets (+8, +12)
+    if ((e = cudaMemsetAsync(scratch, 0, 16, s)) != cudaSuccess) return e;
+    if (g.nseg > 1) {
+        Geo ga = g;
+        ga.n_items = g.BH * (g.nseg - 1);
+        tc_causal_kernel<256, DV, true, kModeFeat><<<min(ga.n_items, sms), kThreads, PA::SMEM, s>>>(
+            tq[0], tk_all, tv_agg, to, ga, sc, (__nv_bfloat16 *)out, nullptr, nullptr, err);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        const int sz = 256 * DV + 256;
+        if ((e = launch_dependent(seg_scan_kernel, dim3(cdiv(sz, 256), (unsigned)g.BH), dim3(256), 0, s, sc.preS,
+                                  sc.prez, g.nseg, 256 * DV, 256)) != cudaSuccess)
+            return e;
+        launches += 2;
+    }
+    sc.pre_rows = 256;
+    sc.pre_off = 0;
+    sc.ticket = (int *)((unsigned char *)scratch + 8);
+    if (g.nseg > 1) {
+        e = launch_dependent(tc_causal_kernel<128, DV, false, kModeFeatPart>, dim3(min(g.n_items, sms)),
+                             dim3(kThreads), PL::SMEM, s, tq[0], tk[0], tv, to, g, sc, (__nv_bfloat16 *)out, S_out,
+                             z_out, err);
+    } else {
+        tc_causal_kernel<128, DV, false, kModeFeatPart><<<min(g.n_items, sms), kThreads, PL::SMEM, s>>>(
+            tq[0], tk[0], tv, to, g, sc, (__nv_bfloat16 *)out, S_out, z_out, err);
+        e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) return e;
+    sc.pre_off = 128;
+    sc.ticket = (int *)((unsigned char *)scratch + 12);
+    tc_causal_kernel<128, DV, false, kModeFeatComb><<<min(g.n_items, sms), kThreads, PL::SMEM, s>>>(
+        tq[1], tk[1], tv, to, g, sc, (__nv_bfloat16 *)out, S_out ? S_out + 128 * DV : nullptr,
+        z_out ? z_out + 128 : nullptr, err);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    note_launches(launches + 2);
     return cudaSuccess;
 }
 
@@ -1958,12 +2048,10 @@ cudaError_t run_prf(const Problem &p, void *scratch, float *S_out, float *z_out,
         } else {
             float *num_part = (float *)(b + L.part);
             float *den_part = (float *)(b + L.part + up256((size_t)p.BH * p.N * DV * 4));
-            e = run_causal<128, DV, kModeFeatPart>(tq[0], tk[0], tv, tva, to, g, half, num_part, den_part, p.out,
-                                                   S_out, z_out, err, s);
-            if (e != cudaSuccess) return e;
-            return run_causal<128, DV, kModeFeatComb>(tq[1], tk[1], tv, tva, to, g, half, num_part, den_part, p.out,
-                                                      S_out ? S_out + 128 * DV : nullptr,
-                                                      z_out ? z_out + 128 : nullptr, err, s);
+            CUtensorMap tk_all;
+            if (!make_map(&tk_all, phk, p.BH, p.N, M, M)) return cudaErrorInvalidValue;
+            return run_causal_split<DV>(tq, tk, tk_all, tv, tva, to, g, half, num_part, den_part, p.out, S_out,
+                                        z_out, err, s);
         }
     }
     float *totS = (float *)(b + L.tot);

@@ -132,15 +132,15 @@ def test_long_segment_chain_prf(la, H, N, m, Dv, causal):
 
 
 def test_prf_launch_plan(la):
-    """m = 256, few heads: the projection, then per feature half the
-    segment-sum pass, the scan and the output pass (causal: 7 kernels), or
-    the segment-sum pass and the totals per half, then one readout
-    (non-causal: 6 kernels)."""
+    """m = 256, few heads: the projection, then (causal: 5 kernels) one
+    segment-sum pass over all 256 features, the scan, and the output pass of
+    each 128-feature half, or (non-causal: 6 kernels) the segment-sum pass
+    and the totals per half, then one readout."""
     W = wl.make_W(256, 64).cuda()
     fm = la.FeatureMap("prf", W)
     w = wl.small(B=1, H=2, N=2048, D=64, Dv=64, feature="prf", m=256, seed=9)
     q, k, v = (t.cuda() for t in wl.make_qkv(w))
-    for causal, expect in ((True, 7), (False, 6)):
+    for causal, expect in ((True, 5), (False, 6)):
         n0 = la.la_launch_count()
         la.la_forward(q, k, v, causal=causal, feature_map=fm)
         torch.cuda.synchronize()
