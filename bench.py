@@ -322,6 +322,9 @@ def run_ours(args):
         total_ms = e0.elapsed_time(e1)
     barrier(ws)
     sampler.mark(t_wall0, time.time())
+    # stop polling nvidia-smi once the timed region is over: its driver queries
+    # would otherwise slow the host-bound e2e steps of the small workloads
+    clocks = sampler.stop() if rank == 0 else None
     launches = la.la_launch_count() - n0
     total_ms = max_over_ranks(total_ms, ws)
     ms_step = total_ms / args.steps
@@ -393,7 +396,6 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu_baseline and ws == 1:
         log("timing the oracle on host cores ...")
         result["cpu_baseline"] = cpu_baseline(w, q, k, v, W)
-    clocks = sampler.stop() if rank == 0 else None
     if clocks:
         result["clocks"] = clocks
     if rank == 0:
