@@ -57,6 +57,10 @@ SMALL = [
     (700, 64, 64, 2, 1, "prf", 128, "bf16", False),
     (129, 64, 64, 1, 1, "prf", 256, "bf16", False),
     (1, 64, 64, 1, 1, "prf", 256, "bf16", True),
+    # many heads (B*H >= the SM count): one segment per head, so no segment-sum
+    # pass or scan, for both feature-map layouts of the causal random features
+    (200, 64, 64, 2, 80, "prf", 256, "bf16", True),
+    (150, 64, 128, 1, 160, "prf", 128, "bf16", True),
 ]
 
 
