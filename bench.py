@@ -388,7 +388,9 @@ def run_ours(args):
                                "before the start event)" if flush else
                          f"inputs ({in_bytes / 1e6:.0f} MB) larger than L2",
                          "parallelism": "replicas" if ws > 1 else "single GPU"},
-              "roofline": roofline, "e2e": e2e, "gpu_launches": launches}
+              "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
+              # the same rate counted per (position, head): tokens/s x H
+              "token_heads_per_s": value * w.H}
 
     if args.decode_steps > 0 and w.causal and w.D == wl.DECODE_D and w.feature == "elu1":
         result["decode"] = run_decode(la, args, S_out, z_out, dev, stream, ws)
