@@ -26,7 +26,9 @@
  *
  * Conventions for every entry point:
  *  - Tensor pointers are DEVICE pointers owned by the caller, contiguous,
- *    row-major, 16-byte aligned.  Heads are flattened as bh = b * H + h.
+ *    row-major, 16-byte aligned (la_forward_host: q, k, v and out in HOST
+ *    memory, the feature map's W on the device).  Heads are flattened as
+ *    bh = b * H + h.
  *      q, k   [B, H, N, D]        v, out [B, H, N, Dv]     (dtype)
  *      S      [B, H, Dphi, Dv]    z      [B, H, Dphi]      (fp32)
  *      W      [m, D]                                       (fp32)
