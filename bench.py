@@ -216,54 +216,61 @@ def job_rate(units_per_rank_step: float, steps: int, ws: int, max_ms: float) -> 
     return units_per_rank_step * steps * ws / (max_ms / 1e3)
 
 
-def cpu_baseline(w: wl.Workload, q, k, v, W, budget_s=12.0):
-    """The oracle, as it stands, on a bounded sample of heads of the workload."""
-    import numpy as np
+def oracle_sample(w: wl.Workload, budget_s: float, cores: int):
+    """Heads x positions of the workload that one oracle call covers within
+    about ``budget_s``: at least min(B*H, cores) heads, so that every OpenMP
+    thread (one head each) has work; positions, then heads, grow by 4x."""
+    BH = w.B * w.H
+    n_heads = min(BH, max(1, cores))
+    n_pos = min(w.N, 1024)
+    # cost model from the oracle's loop: ~(4 Dphi Dv + elementwise) per token-head
+    per = 4.0 * w.phi_dim * w.Dv + (4 * w.m * w.D if w.feature == "prf" else 0) + 8 * w.D
+    rate = 0.5e9 * min(n_heads, cores)   # fp64 flop/s, a rough guess refined by timing
+    while n_pos < w.N and n_heads * n_pos * 4 * per / rate <= budget_s:
+        n_pos = min(w.N, n_pos * 4)
+    while n_pos == w.N and n_heads < BH and min(BH, n_heads * 4) * n_pos * per / rate <= budget_s:
+        n_heads = min(BH, n_heads * 4)
+    return n_heads, n_pos
 
+
+def cpu_baseline(w: wl.Workload, q, k, v, W, budget_s=12.0, reps_min=1):
+    """The oracle, as it stands, timed on the host cores over a bounded sample
+    of the workload (a whole number of calls, each over the same sample)."""
     import oracle
 
     lib = oracle.load()
     cores = oracle.num_threads(lib)
     BH = w.B * w.H
-    qf = q.reshape(BH, w.N, w.D)
-    kf = k.reshape(BH, w.N, w.D)
-    vf = v.reshape(BH, w.N, w.Dv)
     Wn = W.double().numpy() if W is not None else None
-    # grow the sample (heads x positions) until it takes ~budget_s
-    n_heads, n_pos = 1, min(w.N, 4096)
-    while True:
-        qs = qf[:n_heads, :n_pos].double().numpy()[None]
-        ks = kf[:n_heads, :n_pos].double().numpy()[None]
-        vs = vf[:n_heads, :n_pos].double().numpy()[None]
+    n_heads, n_pos = oracle_sample(w, budget_s / 2, cores)
+
+    def part(t, d):
+        return t.reshape(BH, w.N, d)[:n_heads, :n_pos].double().numpy()[None]
+
+    qs, ks, vs = part(q, w.D), part(k, w.D), part(v, w.Dv)
+    times = []
+    while len(times) < reps_min or (sum(times) < budget_s / 2 and len(times) < 50):
         t0 = time.perf_counter()
         oracle.forward(qs, ks, vs, causal=w.causal, feature=w.feature, W=Wn, lib=lib)
-        dt = time.perf_counter() - t0
-        if dt >= budget_s / 4 or (n_heads == BH and n_pos == w.N):
-            break
-        if n_pos < w.N:
-            n_pos = min(w.N, n_pos * 4)
-        else:
-            n_heads = min(BH, n_heads * 4)
+        times.append(time.perf_counter() - t0)
+    dt = statistics.median(times)
     token_heads = n_heads * n_pos
-    tokens_per_s = token_heads / w.H / dt
-    return {"value": tokens_per_s, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{n_heads} of {BH} heads x first {n_pos} of {w.N} positions "
-                      f"({token_heads} token-heads, fp64 recurrence, OpenMP over heads), "
-                      f"{dt:.2f} s; tokens/s = token-heads / H / seconds"}
+    whole = n_heads == BH and n_pos == w.N
+    return {"value": token_heads / w.H / dt, "unit": "tokens/s",
+            "cores": min(cores, n_heads), "kind": "oracle",
+            "sample": f"{'the whole workload' if whole else 'a sample'}: {n_heads} of {BH} heads x "
+                      f"first {n_pos} of {w.N} positions ({token_heads} token-heads), fp64 "
+                      f"recurrence, OpenMP over heads ({min(cores, n_heads)} threads of {cores}); "
+                      f"median of {len(times)} calls, {dt:.3f} s each; "
+                      f"tokens/s = token-heads / H / seconds",
+            "seconds_per_call": dt, "calls": len(times), "whole_workload": whole}
 
 
-def run_ours(args):
-    ws, rank, local = dist_setup()
-    import causal_linear_attention_map_b300 as la
-    from causal_linear_attention_map_b300 import build as _build
-
-    if rank == 0:
-        _build.build()
-    barrier(ws)
-    la.load()
-    w = workload_of(args)
-    dev = torch.device("cuda", local)
-    stream = torch.cuda.current_stream(dev)
+def measure_forward(la, w: wl.Workload, args, dev, stream, ws, rank, with_e2e=True,
+                    with_cpu=True, keep_state=False):
+    """Time la_forward_ex over workload ``w`` (inputs resident in HBM), then
+    the same metric end to end through la_forward_host; returns the entry
+    for the JSON line (and the exported state when ``keep_state``)."""
     q, k, v = wl.make_qkv(w)
     W = wl.make_W(w.m, w.D) if w.feature == "prf" else None
     dq, dk, dv = (t.to(dev) for t in (q, k, v))
@@ -277,14 +284,10 @@ def run_ours(args):
     scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
 
     def fwd():
-        if w.causal:
-            la.la_forward_ex(dq, dk, dv, causal=True, feature_map=fm, out=out, S_out=S_out,
-                             z_out=z_out, stream=stream)
-        else:
-            la.la_forward_ex(dq, dk, dv, causal=False, feature_map=fm, out=out, S_out=S_out,
-                             z_out=z_out, stream=stream)
+        la.la_forward_ex(dq, dk, dv, causal=w.causal, feature_map=fm, out=out, S_out=S_out,
+                         z_out=z_out, stream=stream)
 
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
     if rank == 0:
         sampler.start()
     for _ in range(args.warmup):
@@ -347,64 +350,135 @@ def run_ours(args):
                 "alg_bytes_per_launch": ab, "alg_flops_per_launch": af,
                 "roofline_time_us": round(max(t_hbm, t_flop) * 1e6, 2),
                 "frac_of_roofline_time": round(max(t_hbm, t_flop) / fwd_s, 4)}
+    entry = {"workload": w.name, "value": value, "unit": "tokens/s", "ms_per_step": ms_step,
+             "steps": args.steps, "warmup": args.warmup,
+             "dtype": "bf16" if w.dtype == "bf16" else "f32",
+             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "Dv": w.Dv,
+                        "causal": w.causal, "feature": w.feature, "m": w.m,
+                        "token_heads_per_step": w.token_heads,
+                        "l2": "L2 flushed between steps (host enqueue hidden behind a device "
+                              "delay before the start event)" if flush else
+                        f"inputs ({in_bytes / 1e6:.0f} MB) larger than L2"},
+             "roofline": roofline, "gpu_launches": launches,
+             # the same rate counted per (position, head): tokens/s x H
+             "token_heads_per_s": value * w.H}
+    if clocks:
+        entry["clocks"] = clocks
 
-    # end to end through the C ABI with host buffers: la_forward_host copies
-    # q, k, v in and out back, overlapping both copy directions with the
-    # forward by head groups
-    hq, hk, hv = (t.pin_memory() for t in (q, k, v))
-    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    if with_e2e:
+        # end to end through the C ABI with host buffers: la_forward_host copies
+        # q, k, v in and out back, overlapping both copy directions with the
+        # forward by head groups
+        hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
 
-    def e2e_step():
-        la.la_forward_host(hq, hk, hv, causal=w.causal, feature_map=fm, out=hout, stream=stream)
+        def e2e_step():
+            la.la_forward_host(hq, hk, hv, causal=w.causal, feature_map=fm, out=hout,
+                               stream=stream)
 
-    for _ in range(2):
-        e2e_step()
+        for _ in range(2):
+            e2e_step()
+        barrier(ws)
+        e_steps = max(3, min(args.steps, 10))
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        e1.record(stream)
+        e1.synchronize()
+        e_ms = max_over_ranks(e0.elapsed_time(e1), ws)
+        entry["e2e"] = {"value": job_rate(tokens, e_steps, ws, e_ms), "unit": "tokens/s",
+                        "h2d_bytes_per_step": in_bytes,
+                        "d2h_bytes_per_step": out.numel() * out.element_size(), "steps": e_steps,
+                        "path": "la_forward_host (C ABI): pinned host q, k, v in, out back; "
+                                "copies in both directions overlapped with the forward by "
+                                "head groups"}
+        del hq, hk, hv, hout
+
+    if with_cpu and rank == 0 and ws == 1:
+        log(f"timing the oracle on host cores ({w.name}) ...")
+        entry["cpu_baseline"] = cpu_baseline(w, q, k, v, W, budget_s=args.cpu_budget)
+    del dq, dk, dv, out, scrub
+    if keep_state:
+        return entry, S_out, z_out
+    del S_out, z_out
+    return entry
+
+
+def run_ours(args):
+    ws, rank, local = dist_setup()
+    import causal_linear_attention_map_b300 as la
+    from causal_linear_attention_map_b300 import build as _build
+
+    if rank == 0:
+        _build.build()
     barrier(ws)
-    e_steps = max(3, min(args.steps, 10))
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e_steps):
-        e2e_step()
-    e1.record(stream)
-    e1.synchronize()
-    e_ms = max_over_ranks(e0.elapsed_time(e1), ws)
-    e2e = {"value": job_rate(tokens, e_steps, ws, e_ms), "unit": "tokens/s",
-           "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out.numel() * out.element_size(),
-           "steps": e_steps,
-           "path": "la_forward_host (C ABI): pinned host q, k, v in, out back; copies in both "
-                   "directions overlapped with the forward by head groups"}
-    del hq, hk, hv, hout
-
-    result = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
-              "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-              "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
-              if w.dtype == "bf16" else "f32", "data": "synthetic (seeded N(0,1)/sqrt(D))",
-              "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "Dv": w.Dv,
-                         "causal": w.causal, "feature": w.feature, "m": w.m,
-                         "token_heads_per_step": w.token_heads,
-                         "l2": "L2 flushed between steps (host enqueue hidden behind a device delay "
-                               "before the start event)" if flush else
-                         f"inputs ({in_bytes / 1e6:.0f} MB) larger than L2",
-                         "parallelism": "replicas" if ws > 1 else "single GPU"},
-              "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
-              # the same rate counted per (position, head): tokens/s x H
-              "token_heads_per_s": value * w.H}
+    la.load()
+    w = workload_of(args)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    head, S_out, z_out = measure_forward(la, w, args, dev, stream, ws, rank,
+                                         with_cpu=not args.no_cpu_baseline, keep_state=True)
+    result = {"metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": ws,
+              "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+              "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+              "dtype": head["dtype"], "data": "synthetic (seeded N(0,1)/sqrt(D))",
+              "config": dict(head["config"],
+                             parallelism="replicas" if ws > 1 else "single GPU"),
+              "roofline": head["roofline"], "e2e": head.get("e2e"),
+              "gpu_launches": head["gpu_launches"], "token_heads_per_s": head["token_heads_per_s"]}
+    if "cpu_baseline" in head:
+        result["cpu_baseline"] = head["cpu_baseline"]
+    if head.get("clocks"):
+        result["clocks"] = head["clocks"]
 
     if args.decode_steps > 0 and w.causal and w.D == wl.DECODE_D and w.feature == "elu1":
         result["decode"] = run_decode(la, args, S_out, z_out, dev, stream, ws)
+    del S_out, z_out
 
-    if rank == 0 and not args.no_cpu_baseline and ws == 1:
-        log("timing the oracle on host cores ...")
-        result["cpu_baseline"] = cpu_baseline(w, q, k, v, W)
-    if clocks:
-        result["clocks"] = clocks
+    # every other workload of the method's table, measured the same way in the
+    # same process (each with its own clocks, roofline and oracle baseline)
+    if args.all_configs and args.seq_len == 0 and args.workload == wl.LONG_65536.name:
+        configs = {w.name: {k_: v_ for k_, v_ in head.items() if k_ != "config"}}
+        for other in wl.WORKLOADS.values():
+            if other.name == w.name:
+                continue
+            log(f"measuring {other.name} ...")
+            configs[other.name] = measure_forward(la, other, args, dev, stream, ws, rank,
+                                                  with_cpu=not args.no_cpu_baseline)
+            torch.cuda.empty_cache()
+        result["configs"] = configs
+        result["gpu_launches"] = sum(c["gpu_launches"] for c in configs.values()) + \
+            result.get("decode", {}).get("launches", 0)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if ws > 1:
         import torch.distributed as dist
 
         dist.destroy_process_group()
+
+
+def l2_copy_gbs(dev, stream, nbytes: int) -> float:
+    """Read+write GB/s of a device copy of ``nbytes`` into another buffer,
+    both small enough to stay in L2 together; best of 5 timed loops."""
+    nbytes = min(nbytes, L2_BYTES // 3)
+    a = torch.ones(nbytes // 4, dtype=torch.float32, device=dev)
+    b = torch.empty_like(a)
+    for _ in range(10):
+        b.copy_(a)
+    best = 0.0
+    for _ in range(5):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(50):
+            b.copy_(a)
+        e1.record(stream)
+        e1.synchronize()
+        best = max(best, 2 * a.numel() * 4 * 50 / (e0.elapsed_time(e1) / 1e3) / 1e9)
+    del a, b
+    return best
 
 
 def run_decode(la, args, S_fwd, z_fwd, dev, stream, ws):
@@ -470,6 +544,7 @@ def run_decode(la, args, S_fwd, z_fwd, dev, stream, ws):
     pk, pk_kind = peaks()
     bps = decode_bytes_per_step(B * H, D, D, D)
     ach = bps * T / (ms / 1e3) / 1e9
+    l2 = l2_copy_gbs(dev, stream, S.numel() * 4)
     res = {"steps_per_s": job_rate(T, 1, ws, ms), "tokens_per_s": job_rate(T * B, 1, ws, ms),
            "ms_total": ms, "us_per_step": ms * 1e3 / T, "decode_steps": T, "B": B, "H": H,
            "D": D, "launches": launches,
@@ -477,7 +552,13 @@ def run_decode(la, args, S_fwd, z_fwd, dev, stream, ws):
                         "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
                         "alg_bytes_per_step": bps, "peak_source": pk_kind,
                         "note": "the 64 MB fp32 state fits in L2 (126 MB), so steps may run "
-                                "from L2; frac can exceed 1"}}
+                                "from L2; frac can exceed 1"},
+           # the same bytes against an L2-resident copy of the state's size, measured here
+           "roofline_l2": {"bound": "l2", "achieved": round(ach, 1), "peak": round(l2, 1),
+                           "unit": "GB/s", "frac": round(ach / l2, 4),
+                           "peak_source": "measured in this run: device copy of a buffer of the "
+                                          "state's size into another (read + write bytes), "
+                                          "both resident in L2, best of 5 x 50 copies"}}
     if graph_ms is not None:
         res["graph"] = {"steps_per_s": job_rate(T, 1, ws, graph_ms), "ms_total": graph_ms,
                         "launches_per_graph": G,
@@ -496,31 +577,55 @@ def workload_of(args) -> wl.Workload:
 # ------------------------------------------------------------ reference arm
 
 def run_reference(args):
+    """The reference arm: the oracle as it stands on the host cores.  One step
+    is one oracle call over the same bounded sample of the workload (the
+    whole workload when it fits the per-step budget); every step is timed."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
+    import oracle
+
     w = workload_of(args)
     q, k, v = wl.make_qkv(w)
     W = wl.make_W(w.m, w.D) if w.feature == "prf" else None
+    lib = oracle.load()
+    cores = oracle.num_threads(lib)
     budget = 60.0 / max(1, args.steps + args.warmup)
-    samples = []
-    base = None
+    n_heads, n_pos = oracle_sample(w, budget, cores)
+    BH = w.B * w.H
+    Wn = W.double().numpy() if W is not None else None
+
+    def part(t, d):
+        return t.reshape(BH, w.N, d)[:n_heads, :n_pos].double().numpy()[None]
+
+    qs, ks, vs = part(q, w.D), part(k, w.D), part(v, w.Dv)
+    times = []
     for i in range(args.warmup + args.steps):
-        base = cpu_baseline(w, q, k, v, W, budget_s=budget)
+        t0 = time.perf_counter()
+        oracle.forward(qs, ks, vs, causal=w.causal, feature=w.feature, W=Wn, lib=lib)
         if i >= args.warmup:
-            samples.append(base["value"])
-    value = statistics.median(samples)
-    base = dict(base, value=value)
-    ms = w.B * w.N / value * 1e3
+            times.append(time.perf_counter() - t0)
+    dt = statistics.median(times)
+    token_heads = n_heads * n_pos
+    value = token_heads / w.H / dt
+    whole = n_heads == BH and n_pos == w.N
+    threads = min(cores, n_heads)
+    sample = (f"{'the whole workload' if whole else 'a sample'}: {n_heads} of {BH} heads x first "
+              f"{n_pos} of {w.N} positions ({token_heads} token-heads) per step, fp64 recurrence, "
+              f"OpenMP over heads ({threads} threads of {cores}); median of {len(times)} timed "
+              f"steps; tokens/s = token-heads / H / seconds")
     print(json.dumps({
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1)/sqrt(D))",
-        "impl": "reference",
+        "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1)/sqrt(D))", "impl": "reference",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "Dv": w.Dv,
-                   "causal": w.causal, "feature": w.feature, "m": w.m},
-        "cpu_baseline": base,
+                   "causal": w.causal, "feature": w.feature, "m": w.m,
+                   "step": "one oracle call over " + ("the whole workload" if whole else
+                                                      f"{token_heads} token-heads of it")},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0}}), flush=True)
 
@@ -534,6 +639,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--decode-steps", type=int, default=wl.DECODE_STEPS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=8.0,
+                    help="seconds of oracle time per workload for cpu_baseline")
+    ap.add_argument("--no-all-configs", dest="all_configs", action="store_false",
+                    help="measure only the named workload (default: the long workload plus "
+                         "every other workload of the table under 'configs')")
     ap.add_argument("--seq-len", type=int, default=0,
                     help="run the named workload at this N instead (a smaller case for profiler "
                          "captures; the JSON line then names the shortened workload)")

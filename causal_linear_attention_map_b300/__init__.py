@@ -26,6 +26,7 @@ LIB_PATH = os.path.join(_PKG, "liblinattn.so")
 LA_F32, LA_BF16 = 0, 1
 LA_PHI_ELU1, LA_PHI_PRF = 0, 1
 LA_OK = 0
+LA_NOALLOC_SCRATCH_BYTES = 4 << 20   # the fixed scratch of la_forward_noncausal_noalloc
 STATUS_NAMES = {0: "LA_OK", -1: "LA_ERR_NULL", -2: "LA_ERR_DIM", -3: "LA_ERR_DTYPE",
                 -4: "LA_ERR_FEATURE", -5: "LA_ERR_CUDA", -6: "LA_ERR_TIMEOUT",
                 -7: "LA_ERR_ALIGN"}

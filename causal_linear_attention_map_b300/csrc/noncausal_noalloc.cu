@@ -9,14 +9,17 @@
 // global memory that the library declares below, so it allocates nothing.
 //
 // Facts a caller needs:
-//  - The array holds LA_NOALLOC_SCRATCH_BYTES (4 MiB).  Every GPU that loads
-//    this library reserves it until the process exits.  A problem needs
+//  - The array holds LA_NOALLOC_SCRATCH_BYTES (4 MiB).  A problem needs
 //    B * H * Dphi * (Dv + 1) * 4 bytes; larger ones are rejected with
 //    LA_ERR_DIM before anything is enqueued.
 //  - On host code the array's name is only a host-side stand-in, not a
 //    device address.  Its device address is looked up once per device with
 //    cudaGetSymbolAddress, with that device current, on the first call made
-//    on that device.  Make that first call before any stream capture.
+//    on that device.  With CUDA's default lazy module loading that first
+//    call is also when this file's module (and with it the array) and the
+//    non-causal kernels are loaded onto the device: make it during start-up,
+//    outside any no-allocation context and before any stream capture.  From
+//    then on the device holds the array until the process exits.
 //  - Every call shares the one array and it keeps the last call's contents;
 //    the accumulators are cleared on the stream at the start of each call.
 //    Calls that overlap on the GPU (other streams, other threads) race on

@@ -152,6 +152,30 @@ def step(S, z, q, k, v, feature="elu1", W=None, lib=None):
     return out, S, z
 
 
+def step_inplace(S, z, q, k, v, feature="elu1", W=None, lib=None):
+    """The same recurrent step as ``step``, applied to S, z in place.
+
+    S [B,H,Dphi,Dv] and z [B,H,Dphi] must be C-contiguous float64 arrays (they
+    are the memories carried from step to step, as in the RNN form); q, k, v
+    as in ``step``.  Returns out [B,H,Dv].  Long decodes over many heads use
+    this to avoid copying the memories at every step.
+    """
+    lib = lib or load()
+    for a in (S, z):
+        if a.dtype != np.float64 or not a.flags["C_CONTIGUOUS"]:
+            raise ValueError("S and z must be C-contiguous float64")
+    q, k, v = _d(q), _d(k), _d(v)
+    B, H, D = q.shape
+    Dv = v.shape[-1]
+    kind, W, m = _fm(feature, W, D)
+    if S.shape != (B, H, phi_dim(D, feature, m), Dv) or z.shape != S.shape[:3]:
+        raise ValueError("memory shape mismatch")
+    out = np.empty((B, H, Dv))
+    lib.oracle_step(_ptr(S), _ptr(z), _ptr(q), _ptr(k), _ptr(v), _ptr(out), B * H, D, Dv,
+                    kind, _ptr(W), m)
+    return out
+
+
 def quadratic_rows(q, k, v, rows, causal=True, feature="elu1", W=None, lib=None):
     """Brute-force masked quadratic form for listed rows of one head.
 

@@ -284,6 +284,14 @@ def pin_step_iterated_equals_forward(lib):
             o, S1, z1 = oracle.step(S1, z1, q[:, :, i], k[:, :, i], v[:, :, i], feature, W,
                                     lib=lib)
             _close(o, ref[:, :, i], rtol=1e-12, what="resume")
+        # the in-place form carries the same memories through the same steps
+        S2, z2 = np.zeros((B, H, P, Dv)), np.zeros((B, H, P))
+        for i in range(N):
+            o = oracle.step_inplace(S2, z2, q[:, :, i], k[:, :, i], v[:, :, i], feature, W,
+                                    lib=lib)
+            _close(o, ref[:, :, i], rtol=1e-12, what=f"in-place step {feature}")
+        _close(S2, Sref, rtol=1e-12, what="in-place final S")
+        _close(z2, zref, rtol=1e-12, what="in-place final z")
 
 
 def pin_head_permutation(lib):

@@ -78,3 +78,29 @@ def test_two_gloo_ranks_agree_on_the_slowest_time_and_the_job_rate():
         assert slowest == 15.0
         # both ranks' units over the slowest rank's time
         assert abs(rate - 1000.0 * 4 * 2 / 0.015) < 1e-6 * rate
+
+
+def test_oracle_sample_gives_every_thread_a_head():
+    for w in wl.WORKLOADS.values():
+        for cores in (1, 8, 16, 64):
+            h, n = bench.oracle_sample(w, 2.0, cores)
+            assert min(w.B * w.H, cores) <= h <= w.B * w.H
+            assert 1 <= n <= w.N
+    # a large budget takes the whole workload
+    assert bench.oracle_sample(wl.IMAGE_3072, 1e9, 8) == (32, 3072)
+
+
+def test_reference_arm_times_whole_steps_of_the_tiny_workload(monkeypatch, capsys):
+    import json
+
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    monkeypatch.setenv("RANK", "0")
+    a = argparse.Namespace(workload=wl.TINY_F32.name, seq_len=0, steps=4, warmup=3)
+    bench.run_reference(a)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert line["config"]["step"] == "one oracle call over the whole workload"
+    # value and ms_per_step describe the same timed steps
+    tokens = wl.TINY_F32.B * wl.TINY_F32.N
+    assert abs(line["value"] * line["ms_per_step"] / 1e3 - tokens) < 1e-6 * tokens
+    assert line["cpu_baseline"]["cores"] == 1   # one head: one thread has work

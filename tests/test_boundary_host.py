@@ -129,3 +129,14 @@ def test_host_forward_validation_codes(lib):
     # nothing to copy or compute: succeeds without touching the device
     assert hf(B=0) == 0
     assert hf(N=0, ptrs=(0, 0, 0, 0)) == 0
+
+
+def test_noalloc_scratch_size_matches_the_header():
+    import re
+
+    import causal_linear_attention_map_b300 as la
+
+    hdr = open(os.path.join(ROOT, "include", "linattn.h")).read()
+    m = re.search(r"#define LA_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", hdr)
+    assert m, "LA_NOALLOC_SCRATCH_BYTES not found in the header"
+    assert la.LA_NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))

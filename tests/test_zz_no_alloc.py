@@ -51,6 +51,39 @@ def test_noalloc_matches_la_forward_twice(la, shape, dtype, feature, m):
         assert_close(np64(out), np64(ref), dtype, what=f"call {call}")
 
 
+def test_noalloc_accepts_the_largest_problem_that_fits(la):
+    """B*H*Dphi*(Dv+1)*4 bytes: 63 heads x 128 x 129 x 4 = 4,161,024 B, the
+    largest elu+1 D = Dv = 128 problem under the 4 MiB limit (64 heads is
+    over it: the next test); results checked against la_forward."""
+    w = wl.small(B=1, H=63, N=300, D=128, Dv=128, causal=False, seed=77)
+    q, k, v = (t.cuda() for t in wl.make_qkv(w))
+    assert 63 * 128 * 129 * 4 <= la.LA_NOALLOC_SCRATCH_BYTES < 64 * 128 * 129 * 4
+    ref = la.la_forward(q, k, v, causal=False)
+    out = torch.full_like(ref, float("nan"))
+    st = _noalloc(la, q, k, v, out, la.FeatureMap().c_struct(), la.LA_BF16)
+    assert st == la.LA_OK, la.la_status_string(st)
+    torch.cuda.synchronize()
+    assert_close(np64(out), np64(ref), "bf16", what="63 heads")
+
+
+def test_noalloc_steady_state_calls_allocate_nothing(la):
+    """After the first call on the device (which loads the array and the
+    kernels), further calls leave the device's free memory and torch's
+    allocator untouched."""
+    w = wl.small(B=2, H=4, N=1000, D=64, Dv=64, causal=False, seed=5)
+    q, k, v = (t.cuda() for t in wl.make_qkv(w))
+    out = torch.empty_like(v)
+    fm = la.FeatureMap().c_struct()
+    assert _noalloc(la, q, k, v, out, fm, la.LA_BF16) == la.LA_OK
+    torch.cuda.synchronize()
+    free0, alloc0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+    for _ in range(3):
+        assert _noalloc(la, q, k, v, out, fm, la.LA_BF16) == la.LA_OK
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert torch.cuda.memory_allocated() == alloc0
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch(la):
     # B*H*Dphi*(Dv+1)*4 bytes: 64 heads x 128 x 129 x 4 = 4.2 MB > 4 MiB
     q = torch.zeros((4, 16, 8, 128), dtype=torch.bfloat16, device="cuda")
