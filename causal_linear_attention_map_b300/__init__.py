@@ -9,6 +9,7 @@ no other implementation: if the library is not built, ``load()`` raises.
     out            = la_forward(q, k, v, causal=True, feature_map=None)
     out, S, z      = la_forward_ex(q, k, v, causal=True, feature_map=None)
     out            = la_step(S, z, q, k, v)           # S, z updated in place
+    dq, dk, dv     = la_backward(q, k, v, dout)       # gradients of sum(dout * out)
 
 Shapes: q, k [B, H, N, D]; v [B, H, N, Dv]; S [B, H, Dphi, Dv] fp32;
 z [B, H, Dphi] fp32; decode q, k [B, H, D], v [B, H, Dv].
@@ -30,7 +31,8 @@ LA_NOALLOC_SCRATCH_BYTES = 4 << 20   # the fixed scratch of la_forward_noncausal
 STATUS_NAMES = {0: "LA_OK", -1: "LA_ERR_NULL", -2: "LA_ERR_DIM", -3: "LA_ERR_DTYPE",
                 -4: "LA_ERR_FEATURE", -5: "LA_ERR_CUDA", -6: "LA_ERR_TIMEOUT",
                 -7: "LA_ERR_ALIGN"}
-EXPORTED = ("la_forward", "la_forward_ex", "la_forward_host", "la_step", "la_status_string",
+EXPORTED = ("la_forward", "la_forward_ex", "la_forward_host", "la_step", "la_backward",
+            "la_status_string",
             "la_check", "la_shutdown", "la_version", "la_launch_count",
             "la_forward_noncausal_noalloc", "la_selftest_timeout")
 
@@ -96,6 +98,8 @@ def load(path: str | None = None):
     lib.la_forward_host.restype = i
     lib.la_step.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, fm, i, vp]
     lib.la_step.restype = i
+    lib.la_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, fm, i, vp]
+    lib.la_backward.restype = i
     lib.la_status_string.argtypes = [i]
     lib.la_status_string.restype = ctypes.c_char_p
     lib.la_check.argtypes = [vp]
@@ -244,6 +248,25 @@ def la_step(S, z, q, k, v, feature_map: FeatureMap | None = None, out=None, stre
                         out.data_ptr(), B, H, D, Dv, fmp, dt, _stream(stream))
     _raise(st)
     return out
+
+
+def la_backward(q, k, v, dout, causal=True, feature_map: FeatureMap | None = None, dq=None, dk=None,
+                dv=None, stream=None):
+    """la_backward: gradients (dq, dk, dv) of sum(dout * out) for out = la_forward(q, k, v)."""
+    B, H, N, D = q.shape
+    Dv = v.shape[-1]
+    if k.shape != q.shape or tuple(v.shape[:3]) != (B, H, N) or dout.shape != v.shape:
+        raise ValueError("shape mismatch between q, k, v, dout")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    dt = _check_tensors(q, k, v, dout, dq, dk, dv)
+    _, fmp = _fm(feature_map)
+    st = load().la_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(), dq.data_ptr(),
+                            dk.data_ptr(), dv.data_ptr(), B, H, N, D, Dv, int(bool(causal)), fmp, dt,
+                            _stream(stream))
+    _raise(st)
+    return dq, dk, dv
 
 
 def la_check(stream=None) -> int:

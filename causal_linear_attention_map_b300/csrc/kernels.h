@@ -55,6 +55,15 @@ size_t noncausal_scratch_bytes(const Problem &p);
 cudaError_t noncausal(const Problem &p, void *scratch, float *S_out, float *z_out,
                       cudaStream_t s);
 
+// Gradients dq, dk, dv of sum(dout * out) for the forward of the same
+// arguments, on CUDA cores (fp32 arithmetic), any dtype and feature map with
+// Dphi * Dv <= 16384 (backward_supported).  Scratch (backward_scratch_bytes):
+// per-segment forward and reverse memories and per-position den, dden.
+bool backward_supported(const Problem &p);
+size_t backward_scratch_bytes(const Problem &p, bool causal);
+cudaError_t backward(const Problem &p, const void *dout, void *dq, void *dk, void *dv, bool causal,
+                     void *scratch, cudaStream_t s);
+
 // One recurrent decode step for BH heads, in place on S [BH, P, Dv], z [BH, P].
 cudaError_t step(float *S, float *z, const void *q, const void *k, const void *v, void *out,
                  long long BH, int D, int Dv, int P, int kind, int m, const float *W,

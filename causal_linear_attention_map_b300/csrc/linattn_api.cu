@@ -157,6 +157,48 @@ int forward_impl(const void *q, const void *k, const void *v, void *out, int B, 
     return cuda_status(e != cudaSuccess ? e : e2);
 }
 
+int backward_impl(const void *q, const void *k, const void *v, const void *dout, void *dq, void *dk,
+                  void *dv, int B, int H, int N, int D, int Dv, int causal, const la_feature_map *fm,
+                  int dtype, void *stream)
+{
+    int kind, m, P;
+    const float *W;
+    int st = check_common(B, H, D, Dv, fm, dtype, &kind, &m, &W, &P);
+    if (st != LA_OK) return st;
+    if (N < 0) return LA_ERR_DIM;
+    const long long BH = (long long)B * H;
+    if (BH > 0x7fffffffLL) return LA_ERR_DIM;
+    if ((long long)P * Dv > 16384) return LA_ERR_DIM;
+    if (BH == 0 || N == 0) return LA_OK;
+    if (!q || !k || !v || !dout || !dq || !dk || !dv) return LA_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dq) ||
+        !aligned16(dk) || !aligned16(dv))
+        return LA_ERR_ALIGN;
+    la::Problem p;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.out = nullptr;
+    p.BH = BH;
+    p.N = N;
+    p.D = D;
+    p.Dv = Dv;
+    p.P = P;
+    p.kind = kind;
+    p.m = m;
+    p.W = W;
+    p.dtype = dtype;
+    DeviceCtx *ctx = nullptr;
+    if ((st = get_ctx(&ctx)) != LA_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    void *scratch = nullptr;
+    if (cudaMallocFromPoolAsync(&scratch, la::backward_scratch_bytes(p, causal != 0), ctx->pool, s) != cudaSuccess)
+        return cuda_status(cudaErrorMemoryAllocation);
+    cudaError_t e = la::backward(p, dout, dq, dk, dv, causal != 0, scratch, s);
+    cudaError_t e2 = cudaFreeAsync(scratch, s);
+    return cuda_status(e != cudaSuccess ? e : e2);
+}
+
 // la_forward_host: at most kHostGroups head groups, each with at least
 // kHostGroupBytes of inputs (a group's forward has a fixed cost of a few
 // launches, so small problems take few groups)
@@ -276,6 +318,13 @@ int la_forward_host(const void *q, const void *k, const void *v, void *out, int 
                     int Dv, int causal, const la_feature_map *fm, int dtype, void *stream)
 {
     return forward_host_impl(q, k, v, out, B, H, N, D, Dv, causal, fm, dtype, stream);
+}
+
+int la_backward(const void *q, const void *k, const void *v, const void *dout, void *dq, void *dk, void *dv,
+                int B, int H, int N, int D, int Dv, int causal, const la_feature_map *fm, int dtype,
+                void *stream)
+{
+    return backward_impl(q, k, v, dout, dq, dk, dv, B, H, N, D, Dv, causal, fm, dtype, stream);
 }
 
 int la_step(float *S, float *z, const void *q, const void *k, const void *v, void *out, int B,

@@ -156,6 +156,31 @@ int la_step(float *S, float *z, const void *q, const void *k, const void *v,
             void *out, int B, int H, int D, int Dv,
             const la_feature_map *fm, int dtype, void *stream);
 
+/*
+ * la_backward -- gradients of the forward ("proposed method", bullet 4: the
+ * gradients of forward and backward propagation are computed in linear time,
+ * with cumulative sums).  For L = sum over all elements of dout * out, where
+ * out is la_forward(q, k, v, ..., causal, fm) with the same arguments:
+ *     dq = dL/dq, dk = dL/dk, dv = dL/dv.
+ * With g_i = phi(q_i), f_j = phi(k_j), den_i = g_i . z_i:
+ *     dnum_i = dout_i / den_i,  dden_i = -(dout_i . out_i) / den_i,
+ *     dL/dg_i = S_i dnum_i + z_i dden_i,
+ *     dL/df_j = R_j v_j + r_j,  dL/dv_j = R_j^T f_j,
+ *     R_j = sum_{i>=j} g_i dnum_i^T,  r_j = sum_{i>=j} g_i dden_i
+ * (all positions instead of i >= j / j <= i when causal = 0), then through
+ * phi to q and k (PRF: W is treated as a constant; no gradient for W).
+ * q, k, dq, dk [B, H, N, D]; v, dout, dv [B, H, N, Dv]; all in `dtype`,
+ * device, 16-byte aligned; dq, dk, dv are written, the rest read.  Same
+ * feature maps, sizes and errors as la_forward, except that Dphi * Dv must
+ * be at most 16384 (else LA_ERR_DIM).  Runs on the CUDA cores with fp32
+ * arithmetic; takes stream-ordered scratch from the library's pool
+ * (per-segment memories, and den, dden per position: 8 bytes per
+ * position and head).  den and out are recomputed, not read.
+ */
+int la_backward(const void *q, const void *k, const void *v, const void *dout,
+                void *dq, void *dk, void *dv, int B, int H, int N, int D, int Dv,
+                int causal, const la_feature_map *fm, int dtype, void *stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *la_status_string(int status);
 

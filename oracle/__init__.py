@@ -59,6 +59,7 @@ def _bind(lib):
     lib.oracle_quadratic_rows.argtypes = [P, P, P, P, L, I, I, I, I, P, I,
                                           ctypes.POINTER(ctypes.c_long), L]
     lib.oracle_phi.argtypes = [P, I, I, P, I, P]
+    lib.oracle_backward.argtypes = [P, P, P, P, P, P, P, L, L, I, I, I, I, P, I]
     lib.oracle_num_threads.restype = I
     return lib
 
@@ -133,6 +134,22 @@ def forward(q, k, v, causal=True, feature="elu1", W=None, return_state=False, li
     lib.oracle_noncausal(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B * H, N, D, Dv,
                          kind, _ptr(W), m)
     return out
+
+
+def backward(q, k, v, dout, causal=True, feature="elu1", W=None, lib=None):
+    """Gradients (dq, dk, dv) of L = sum(dout * out) for the forward of the
+    same arguments; q, k [B,H,N,D], v and dout [B,H,N,Dv]; float64 results."""
+    lib = lib or load()
+    q, k, v, dout = _d(q), _d(k), _d(v), _d(dout)
+    B, H, N, D = q.shape
+    Dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != (B, H, N) or dout.shape != v.shape:
+        raise ValueError("shape mismatch")
+    kind, W, m = _fm(feature, W, D)
+    dq, dk, dv = np.empty(q.shape), np.empty(k.shape), np.empty(v.shape)
+    lib.oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                        B * H, N, D, Dv, int(causal), kind, _ptr(W), m)
+    return dq, dk, dv
 
 
 def step(S, z, q, k, v, feature="elu1", W=None, lib=None):

@@ -248,3 +248,143 @@ void oracle_quadratic_rows(const double *q, const double *k, const double *v,
     }
     free(fk);
 }
+
+/*
+ * The chain rule through phi: dx = J_phi(x)^T df for one D-vector x, given
+ * the cotangent df (Dphi values).  f is scratch for Dphi values.
+ *   elu + 1:  d phi / dx = 1 for x > 0, exp(x) otherwise (elementwise).
+ *   PRF:      d phi_r / dx = phi_r(x) (w_r - x), so
+ *             dx = sum_r df_r phi_r(x) w_r - x sum_r df_r phi_r(x).
+ */
+static void phi_vjp(const double *x, const double *df, int D, int kind,
+                    const double *W, int m, double *dx, double *f)
+{
+    if (kind == ORACLE_PHI_ELU1) {
+        for (int d = 0; d < D; d++)
+            dx[d] = (x[d] > 0.0 ? 1.0 : exp(x[d])) * df[d];
+        return;
+    }
+    oracle_phi(x, D, kind, W, m, f);
+    double s = 0.0;
+    for (int d = 0; d < D; d++)
+        dx[d] = 0.0;
+    for (int r = 0; r < m; r++) {
+        double c = df[r] * f[r];
+        s += c;
+        for (int d = 0; d < D; d++)
+            dx[d] += c * W[(long)r * D + d];
+    }
+    for (int d = 0; d < D; d++)
+        dx[d] -= s * x[d];
+}
+
+/* R += g dn^T ;  r += g dd  (the reverse memories, one query's terms) */
+static void accumulate_reverse(double *R, double *r, const double *g,
+                               const double *dn, double dd, int P, int Dv)
+{
+    for (int a = 0; a < P; a++) {
+        r[a] += g[a] * dd;
+        for (int c = 0; c < Dv; c++)
+            R[(long)a * Dv + c] += g[a] * dn[c];
+    }
+}
+
+/*
+ * Gradients of L = sum_i dout_i . out_i with respect to q, k and v
+ * ("Transformers are RNNs", proposed method b4: the gradients of the
+ * forward and backward propagation are computed in linear time, with
+ * cumulative sums like the forward pass).  With g_i = phi(q_i),
+ * f_j = phi(k_j), num_i = S_i^T g_i, den_i = z_i . g_i, out = num / den:
+ *   dnum_i = dout_i / den_i,   dden_i = -(dout_i . out_i) / den_i
+ *   d g_i  = S_i dnum_i + z_i dden_i                 (forward sweep)
+ *   R_j = sum_{i >= j} g_i dnum_i^T,  r_j = sum_{i >= j} g_i dden_i
+ *   d f_j  = R_j v_j + r_j,   dv_j = R_j^T f_j       (reverse sweep)
+ * then dq, dk through phi (phi_vjp).  The non-causal form uses the sums over
+ * all positions for S, z, R and r.
+ * Layouts as for the forward: q, k, dq, dk [BH, N, D]; v, dout, dv [BH, N, Dv].
+ */
+void oracle_backward(const double *q, const double *k, const double *v,
+                     const double *dout, double *dq, double *dk, double *dv,
+                     long BH, long N, int D, int Dv, int causal, int kind,
+                     const double *W, int m)
+{
+    int P = oracle_phi_dim(D, kind, m);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long h = 0; h < BH; h++) {
+        double *S = calloc((size_t)P * Dv, sizeof(double));
+        double *z = calloc((size_t)P, sizeof(double));
+        double *R = calloc((size_t)P * Dv, sizeof(double));
+        double *r = calloc((size_t)P, sizeof(double));
+        double *f = malloc((size_t)P * sizeof(double));
+        double *g = malloc((size_t)P * sizeof(double));
+        double *dphi = malloc((size_t)P * sizeof(double));
+        double *tmp = malloc((size_t)P * sizeof(double));
+        double *dnum = malloc((size_t)N * Dv * sizeof(double));
+        double *dden = malloc((size_t)N * sizeof(double));
+        const double *qh = q + h * N * D, *kh = k + h * N * D;
+        const double *vh = v + h * N * Dv, *oh = dout + h * N * Dv;
+        if (!causal) {
+            for (long j = 0; j < N; j++) {
+                oracle_phi(kh + j * D, D, kind, W, m, f);
+                update_state(S, z, f, vh + j * Dv, P, Dv);
+            }
+        }
+        /* forward sweep: the memories S_i, z_i, the readout and d g_i */
+        for (long i = 0; i < N; i++) {
+            if (causal) {
+                oracle_phi(kh + i * D, D, kind, W, m, f);
+                update_state(S, z, f, vh + i * Dv, P, Dv);
+            }
+            oracle_phi(qh + i * D, D, kind, W, m, g);
+            double den = 0.0;
+            for (int a = 0; a < P; a++)
+                den += g[a] * z[a];
+            double dot = 0.0;
+            for (int c = 0; c < Dv; c++) {
+                double s = 0.0;
+                for (int a = 0; a < P; a++)
+                    s += g[a] * S[(long)a * Dv + c];
+                dot += oh[i * Dv + c] * (s / den);
+            }
+            dden[i] = -dot / den;
+            for (int c = 0; c < Dv; c++)
+                dnum[i * Dv + c] = oh[i * Dv + c] / den;
+            for (int a = 0; a < P; a++) {
+                double s = z[a] * dden[i];
+                for (int c = 0; c < Dv; c++)
+                    s += S[(long)a * Dv + c] * dnum[i * Dv + c];
+                dphi[a] = s;
+            }
+            phi_vjp(qh + i * D, dphi, D, kind, W, m, dq + (h * N + i) * D, tmp);
+        }
+        if (!causal) {
+            for (long i = 0; i < N; i++) {
+                oracle_phi(qh + i * D, D, kind, W, m, g);
+                accumulate_reverse(R, r, g, dnum + i * Dv, dden[i], P, Dv);
+            }
+        }
+        /* reverse sweep: R_j, r_j over i >= j, then d f_j and dv_j */
+        for (long j = N - 1; j >= 0; j--) {
+            if (causal) {
+                oracle_phi(qh + j * D, D, kind, W, m, g);
+                accumulate_reverse(R, r, g, dnum + j * Dv, dden[j], P, Dv);
+            }
+            oracle_phi(kh + j * D, D, kind, W, m, f);
+            for (int a = 0; a < P; a++) {
+                double s = r[a];
+                for (int c = 0; c < Dv; c++)
+                    s += R[(long)a * Dv + c] * vh[j * Dv + c];
+                dphi[a] = s;
+            }
+            for (int c = 0; c < Dv; c++) {
+                double s = 0.0;
+                for (int a = 0; a < P; a++)
+                    s += R[(long)a * Dv + c] * f[a];
+                dv[(h * N + j) * Dv + c] = s;
+            }
+            phi_vjp(kh + j * D, dphi, D, kind, W, m, dk + (h * N + j) * D, tmp);
+        }
+        free(S); free(z); free(R); free(r); free(f); free(g); free(dphi);
+        free(tmp); free(dnum); free(dden);
+    }
+}

@@ -21,6 +21,12 @@ section "proposed method" b6, for positive random features):
     step iterated N times = the forward pass, head and key/value
     permutations, linearity in V;
   - the PRF kernel's expectation E_w[phi(q).phi(k)] = exp(q.k).
+Gradients ("Transformers are RNNs", proposed method b4: linear-time
+gradients of the same cumulative-sum form):
+  - central finite differences of the forward oracle (itself pinned above);
+  - torch autograd through the masked quadratic form written in torch;
+  - closed forms: constant V gives zero gradients for q and k, and the
+    gradients for v sum to the sum of the output cotangents.
 """
 from __future__ import annotations
 
@@ -323,6 +329,76 @@ def pin_linear_in_v(lib):
         b = 2.0 * oracle.forward(q, k, v1, causal=causal, lib=lib) \
             - 3.0 * oracle.forward(q, k, v2, causal=causal, lib=lib)
         _close(a, b, rtol=1e-12, what="linearity")
+
+
+def _loss(q, k, v, dout, causal, feature, W, lib):
+    return float(np.sum(dout * oracle.forward(q, k, v, causal=causal, feature=feature, W=W,
+                                              lib=lib)))
+
+
+def pin_backward_finite_differences(lib):
+    r = _rng(16)
+    B, H, N, D, Dv = 1, 2, 5, 3, 2
+    h = 1e-5
+    for feature, W in (("elu1", None), ("prf", r.normal(size=(4, D)) * 0.7)):
+        for causal in (True, False):
+            q, k, v, do = (r.normal(size=(B, H, N, x)) for x in (D, D, Dv, Dv))
+            got = oracle.backward(q, k, v, do, causal=causal, feature=feature, W=W, lib=lib)
+            for t, (x, g) in enumerate(zip((q, k, v), got)):
+                fd = np.empty_like(x)
+                for idx in np.ndindex(x.shape):
+                    xp, xm = x.copy(), x.copy()
+                    xp[idx] += h
+                    xm[idx] -= h
+                    args_p = [q, k, v]
+                    args_m = [q, k, v]
+                    args_p[t], args_m[t] = xp, xm
+                    fd[idx] = (_loss(*args_p, do, causal, feature, W, lib)
+                               - _loss(*args_m, do, causal, feature, W, lib)) / (2 * h)
+                err = np.max(np.abs(g - fd)) / max(np.max(np.abs(fd)), 1e-30)
+                assert err <= 1e-7, f"finite differences {feature} causal={causal} d{'qkv'[t]}: {err:.2e}"
+
+
+def _torch_phi(x, feature, W):
+    if feature == "elu1":
+        return torch.nn.functional.elu(x) + 1.0
+    m = W.shape[0]
+    return torch.exp(x @ W.T - 0.5 * (x * x).sum(-1, keepdim=True)) / math.sqrt(m)
+
+
+def pin_backward_torch_autograd_quadratic(lib):
+    r = _rng(17)
+    B, H, N, D, Dv = 2, 1, 9, 4, 3
+    for feature in ("elu1", "prf"):
+        Wn = r.normal(size=(6, D)) * 0.6 if feature == "prf" else None
+        for causal in (True, False):
+            q, k, v, do = (r.normal(size=(B, H, N, x)) for x in (D, D, Dv, Dv))
+            tq, tk, tv = (torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in (q, k, v))
+            Wt = torch.tensor(Wn, dtype=torch.float64) if Wn is not None else None
+            A = _torch_phi(tq, feature, Wt) @ _torch_phi(tk, feature, Wt).transpose(-1, -2)
+            if causal:
+                A = torch.tril(A)
+            out = (A @ tv) / A.sum(-1, keepdim=True)
+            (out * torch.tensor(do)).sum().backward()
+            got = oracle.backward(q, k, v, do, causal=causal, feature=feature, W=Wn, lib=lib)
+            for name, g, t in zip("qkv", got, (tq, tk, tv)):
+                _close(g, t.grad.numpy(), rtol=1e-10, what=f"autograd {feature} causal={causal} d{name}")
+
+
+def pin_backward_constant_values(lib):
+    r = _rng(18)
+    B, H, N, D, Dv = 1, 3, 11, 4, 3
+    for feature, W in (("elu1", None), ("prf", r.normal(size=(5, D)))):
+        for causal in (True, False):
+            q, k = (r.normal(size=(B, H, N, D)) for _ in range(2))
+            v = np.broadcast_to(r.normal(size=(1, 1, 1, Dv)), (B, H, N, Dv)).copy()
+            do = r.normal(size=(B, H, N, Dv))
+            dq, dk, dv = oracle.backward(q, k, v, do, causal=causal, feature=feature, W=W, lib=lib)
+            scale = np.max(np.abs(do)) * np.max(np.abs(v))
+            assert np.max(np.abs(dq)) <= 1e-12 * scale * N, f"constant V: dq != 0 ({feature})"
+            assert np.max(np.abs(dk)) <= 1e-12 * scale * N, f"constant V: dk != 0 ({feature})"
+            # each output is a convex combination of the values: sum_j d out_i / d v_j = I
+            _close(dv.sum(axis=2), do.sum(axis=2), rtol=1e-12, what=f"sum of dv ({feature})")
 
 
 ALL_PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_")]

@@ -140,3 +140,26 @@ def test_noalloc_scratch_size_matches_the_header():
     m = re.search(r"#define LA_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", hdr)
     assert m, "LA_NOALLOC_SCRATCH_BYTES not found in the header"
     assert la.LA_NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+
+
+def test_backward_validation_codes(lib):
+    """la_backward validates like la_forward before anything is enqueued; it
+    also rejects Dphi * Dv above 16384."""
+    import causal_linear_attention_map_b300 as la
+
+    p = [FAKE + 256 * i for i in range(7)]
+
+    def bw(*, B=1, H=2, N=8, D=64, Dv=64, fm=None, dtype=1, ptrs=p, causal=1):
+        fmp = ctypes.byref(fm) if fm is not None else None
+        return lib.la_backward(*ptrs, B, H, N, D, Dv, causal, fmp, dtype, None)
+
+    assert bw(dtype=7) == -3
+    assert bw(D=48) == -2
+    assert bw(N=-1) == -2
+    assert bw(fm=la.la_feature_map(1, 256, FAKE), Dv=128) == -2   # 256 x 128 > 16384
+    assert bw(fm=la.la_feature_map(1, 64, None)) == -4
+    for i in range(7):
+        assert bw(ptrs=p[:i] + [0] + p[i + 1:]) == -1
+    assert bw(ptrs=[FAKE + 8] + p[1:]) == -7
+    assert bw(B=0) == 0
+    assert bw(N=0, ptrs=[0] * 7) == 0

@@ -53,6 +53,15 @@ MUTATIONS = {
     "quadratic_strict_mask": ("long last = causal ? i : N - 1;",
                               "long last = causal ? i - 1 : N - 1;"),
     "z_not_accumulated": ("z[a] += fk[a];", "z[a] = fk[a];"),
+    "bwd_dden_sign": ("dden[i] = -dot / den;", "dden[i] = dot / den;"),
+    "bwd_dq_drops_dden": ("double s = z[a] * dden[i];", "double s = 0.0 * z[a] * dden[i];"),
+    "bwd_dk_drops_r": ("double s = r[a];", "double s = 0.0 * r[a];"),
+    "bwd_dv_uses_phi_q": ("s += R[(long)a * Dv + c] * f[a];", "s += R[(long)a * Dv + c] * g[a];"),
+    "bwd_reverse_exclusive": ("accumulate_reverse(R, r, g, dnum + j * Dv, dden[j], P, Dv);\n            }\n            oracle_phi(kh + j * D, D, kind, W, m, f);",
+                              "}\n            oracle_phi(kh + j * D, D, kind, W, m, f);"),
+    "bwd_elu_vjp_branch": ("(x[d] > 0.0 ? 1.0 : exp(x[d]))", "(x[d] > 0.0 ? exp(x[d]) : 1.0)"),
+    "bwd_prf_vjp_drops_x": ("dx[d] -= s * x[d];", "dx[d] -= 0.0 * s * x[d];"),
+    "bwd_prf_vjp_transposed_W": ("dx[d] += c * W[(long)r * D + d];", "dx[d] += c * W[(long)d * m + r];"),
 }
 
 

@@ -10,7 +10,9 @@ Recipe: q, k, v ~ iid N(0, 1) drawn with ``torch.randn`` from a CPU
 q, k, v; scaled by 1/sqrt(D) for the bf16 workloads (unscaled for the fp32
 one); then cast to the workload dtype.  The PRF projection W [m, D] is iid
 N(0, 1) fp32 from its own seed.  Decode inputs for step t come from seed
-``DECODE_SEED + t``.
+``DECODE_SEED + t``.  The output cotangent of a backward pass, dout
+[B,H,N,Dv], is iid N(0, 1) from seed ``seed + DOUT_SEED_OFFSET``, cast to the
+workload dtype.
 """
 from __future__ import annotations
 
@@ -66,6 +68,7 @@ DECODE_D = 128
 DECODE_STEPS = 4096
 DECODE_SEED = 4000
 W_SEED = 5000
+DOUT_SEED_OFFSET = 7000
 
 TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
 
@@ -86,6 +89,13 @@ def make_qkv(w: Workload, device="cpu"):
             x.mul_(scale)
         out.append(x.to(dt).to(device).contiguous())
     return tuple(out)
+
+
+def make_dout(w: Workload, device="cpu"):
+    """Output cotangent dout [B,H,N,Dv] for a backward pass, iid N(0, 1)."""
+    gen = torch.Generator().manual_seed(w.seed + DOUT_SEED_OFFSET)
+    x = _randn((w.B, w.H, w.N, w.Dv), gen)
+    return x.to(TORCH_DTYPE[w.dtype]).to(device).contiguous()
 
 
 def make_W(m: int, D: int, seed: int = W_SEED, device="cpu"):
