@@ -60,6 +60,8 @@ def _bind(lib):
                                           ctypes.POINTER(ctypes.c_long), L]
     lib.oracle_phi.argtypes = [P, I, I, P, I, P]
     lib.oracle_backward.argtypes = [P, P, P, P, P, P, P, L, L, I, I, I, I, P, I]
+    lib.oracle_prefix_attention.argtypes = [P, P, P, P, L, L, I, I, P]
+    lib.oracle_prefix_step.argtypes = [P, P, P, P, P, L, I, I]
     lib.oracle_num_threads.restype = I
     return lib
 
@@ -150,6 +152,37 @@ def backward(q, k, v, dout, causal=True, feature="elu1", W=None, lib=None):
     lib.oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
                         B * H, N, D, Dv, int(causal), kind, _ptr(W), m)
     return dq, dk, dv
+
+
+def prefix_attention(q, k, v, return_state=False, lib=None):
+    """Softmax attention of one query token per head over every prefix, as an
+    RNN: q [B,H,D], k [B,H,N,D], v [B,H,N,Dv] -> out [B,H,N,Dv] (float64),
+    plus the final state [B,H,Dv+2] = (m, u, w) when ``return_state``."""
+    lib = lib or load()
+    q, k, v = _d(q), _d(k), _d(v)
+    B, H, N, D = k.shape
+    Dv = v.shape[-1]
+    if q.shape != (B, H, D) or v.shape[:3] != (B, H, N):
+        raise ValueError("shape mismatch")
+    out = np.empty((B, H, N, Dv))
+    st = np.empty((B, H, Dv + 2)) if return_state else None
+    lib.oracle_prefix_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B * H, N, D, Dv, _ptr(st))
+    return (out, st) if return_state else out
+
+
+def prefix_step(state, q, k, v, lib=None):
+    """One RNN step of the prefix attention: state [B,H,Dv+2] (m, u, w),
+    q, k [B,H,D], v [B,H,Dv] -> (out [B,H,Dv], new state); inputs unchanged."""
+    lib = lib or load()
+    st = _d(state).copy()
+    q, k, v = _d(q), _d(k), _d(v)
+    B, H, D = q.shape
+    Dv = v.shape[-1]
+    if st.shape != (B, H, Dv + 2):
+        raise ValueError("state shape mismatch")
+    out = np.empty((B, H, Dv))
+    lib.oracle_prefix_step(_ptr(st), _ptr(q), _ptr(k), _ptr(v), _ptr(out), B * H, D, Dv)
+    return out, st
 
 
 def step(S, z, q, k, v, feature="elu1", W=None, lib=None):

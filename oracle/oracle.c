@@ -388,3 +388,66 @@ void oracle_backward(const double *q, const double *k, const double *v,
         free(tmp); free(dnum); free(dden);
     }
 }
+
+/*
+ * Softmax attention as an RNN ("Attention as an RNN", proposed method: a
+ * learned query token q reads keys and values as a many-to-one RNN; its
+ * many-to-many outputs are the outputs after every prefix).  Per head, with
+ * s_i = q . k_i:
+ *     o_k = sum_{i<=k} exp(s_i) v_i / sum_{i<=k} exp(s_i)
+ * evaluated as the RNN cell over the state (m, u, w) = (running max of s,
+ * sum of exp(s_i - m), sum of exp(s_i - m) v_i):
+ *     m' = max(m, s),  u' = u exp(m - m') + exp(s - m'),
+ *     w' = w exp(m - m') + exp(s - m') v,     o = w' / u'.
+ * The initial state is m = -infinity, u = 0, w = 0.  No 1/sqrt(D) factor is
+ * applied to s (the caller scales q).
+ * q [BH, D]; k [BH, N, D]; v, out [BH, N, Dv]; state [BH, Dv + 2] as
+ * (m, u, w_0..w_{Dv-1}): in/out for oracle_prefix_step, out (nullable) for
+ * oracle_prefix_attention.
+ */
+static void prefix_cell(double *st, const double *q, const double *k,
+                        const double *v, double *o, int D, int Dv)
+{
+    double s = 0.0;
+    for (int d = 0; d < D; d++)
+        s += q[d] * k[d];
+    double m = st[0];
+    double mn = s > m ? s : m;
+    double a = (m == -INFINITY) ? 0.0 : exp(m - mn);
+    double b = exp(s - mn);
+    st[0] = mn;
+    st[1] = st[1] * a + b;
+    for (int c = 0; c < Dv; c++) {
+        st[2 + c] = st[2 + c] * a + b * v[c];
+        o[c] = st[2 + c] / st[1];
+    }
+}
+
+void oracle_prefix_attention(const double *q, const double *k, const double *v,
+                             double *out, long BH, long N, int D, int Dv,
+                             double *state_out)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long h = 0; h < BH; h++) {
+        double *st = malloc((size_t)(Dv + 2) * sizeof(double));
+        st[0] = -INFINITY;
+        st[1] = 0.0;
+        for (int c = 0; c < Dv; c++)
+            st[2 + c] = 0.0;
+        for (long i = 0; i < N; i++)
+            prefix_cell(st, q + h * D, k + (h * N + i) * D, v + (h * N + i) * Dv,
+                        out + (h * N + i) * Dv, D, Dv);
+        if (state_out)
+            memcpy(state_out + h * (long)(Dv + 2), st, (size_t)(Dv + 2) * sizeof(double));
+        free(st);
+    }
+}
+
+void oracle_prefix_step(double *state, const double *q, const double *k,
+                        const double *v, double *out, long BH, int D, int Dv)
+{
+#pragma omp parallel for schedule(static)
+    for (long h = 0; h < BH; h++)
+        prefix_cell(state + h * (long)(Dv + 2), q + h * D, k + h * D, v + h * Dv,
+                    out + h * Dv, D, Dv);
+}

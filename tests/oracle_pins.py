@@ -27,6 +27,14 @@ gradients of the same cumulative-sum form):
   - torch autograd through the masked quadratic form written in torch;
   - closed forms: constant V gives zero gradients for q and k, and the
     gradients for v sum to the sum of the output cotangents.
+Softmax attention as an RNN over every prefix (review page "Attention as an
+RNN", proposed method: many-to-one RNN cell, many-to-many outputs by a
+parallel prefix scan, Hillis-Steele):
+  - scipy softmax over each prefix (brute force with a library routine);
+  - a pure-Python Hillis-Steele scan with the associative max-rescaling
+    combine, an independent algorithm for the same outputs;
+  - the last output is full softmax attention (torch); constant V gives V;
+    the step iterated from the empty state gives the scan; scores of +-500.
 """
 from __future__ import annotations
 
@@ -399,6 +407,85 @@ def pin_backward_constant_values(lib):
             assert np.max(np.abs(dk)) <= 1e-12 * scale * N, f"constant V: dk != 0 ({feature})"
             # each output is a convex combination of the values: sum_j d out_i / d v_j = I
             _close(dv.sum(axis=2), do.sum(axis=2), rtol=1e-12, what=f"sum of dv ({feature})")
+
+
+def pin_prefix_softmax_brute_force(lib):
+    r = _rng(20)
+    B, H, N, D, Dv = 2, 2, 23, 5, 3
+    q = r.normal(size=(B, H, D))
+    k = r.normal(size=(B, H, N, D))
+    v = r.normal(size=(B, H, N, Dv))
+    got = oracle.prefix_attention(q, k, v, lib=lib)
+    for b in range(B):
+        for h in range(H):
+            s_ = k[b, h] @ q[b, h]
+            ref = np.stack([scipy.special.softmax(s_[:i + 1]) @ v[b, h, :i + 1] for i in range(N)])
+            _close(got[b, h], ref, rtol=1e-13, what="prefix softmax")
+
+
+def _hillis_steele(s_, v):
+    """Inclusive scan of (m, u, w) with the combine (a, b) -> (max, rescaled
+    sums), Hillis-Steele: log2(N) rounds, element i combines i - 2^d into i."""
+    n = len(s_)
+    st = [(s_[i], 1.0, list(v[i])) for i in range(n)]
+    d = 1
+    while d < n:
+        nxt = list(st)
+        for i in range(d, n):
+            (ma, ua, wa), (mb, ub, wb) = st[i - d], st[i]
+            m = max(ma, mb)
+            ea, eb = math.exp(ma - m), math.exp(mb - m)
+            nxt[i] = (m, ua * ea + ub * eb, [x * ea + y * eb for x, y in zip(wa, wb)])
+        st = nxt
+        d *= 2
+    return [[x / u for x in w] for (_, u, w) in st]
+
+
+def pin_prefix_hillis_steele(lib):
+    r = _rng(21)
+    for N in (1, 2, 7, 16, 33):
+        q = r.normal(size=(1, 1, 4))
+        k = r.normal(size=(1, 1, N, 4)) * 2.0
+        v = r.normal(size=(1, 1, N, 3))
+        got = oracle.prefix_attention(q, k, v, lib=lib)[0, 0]
+        ref = _hillis_steele((k[0, 0] @ q[0, 0]).tolist(), v[0, 0].tolist())
+        _close(got, ref, rtol=1e-13, what=f"Hillis-Steele N={N}")
+
+
+def pin_prefix_last_row_full_softmax_and_constant_v(lib):
+    r = _rng(22)
+    B, H, N, D, Dv = 1, 3, 40, 6, 4
+    q = r.normal(size=(B, H, D))
+    k = r.normal(size=(B, H, N, D))
+    v = r.normal(size=(B, H, N, Dv))
+    got = oracle.prefix_attention(q, k, v, lib=lib)
+    tq, tk, tv = (torch.tensor(a) for a in (q, k, v))
+    full = torch.softmax(torch.einsum("bhd,bhnd->bhn", tq, tk), dim=-1)
+    _close(got[:, :, -1], torch.einsum("bhn,bhnc->bhc", full, tv).numpy(), rtol=1e-13, what="last row")
+    c = np.broadcast_to(r.normal(size=(1, 1, 1, Dv)), v.shape).copy()
+    _close(oracle.prefix_attention(q, k, c, lib=lib), c, rtol=1e-14, what="constant v")
+
+
+def pin_prefix_step_iterated_and_large_scores(lib):
+    r = _rng(23)
+    B, H, N, D, Dv = 2, 1, 17, 3, 2
+    for scale in (1.0, 300.0):   # scores up to about +-500: exp(s) alone over/underflows
+        q = r.normal(size=(B, H, D))
+        k = r.normal(size=(B, H, N, D)) * scale
+        v = r.normal(size=(B, H, N, Dv))
+        ref, st_ref = oracle.prefix_attention(q, k, v, return_state=True, lib=lib)
+        st = np.zeros((B, H, Dv + 2))
+        st[..., 0] = -np.inf
+        outs = []
+        for i in range(N):
+            o, st = oracle.prefix_step(st, q, k[:, :, i], v[:, :, i], lib=lib)
+            outs.append(o)
+        _close(np.stack(outs, axis=2), ref, rtol=1e-12, what=f"step x N scale={scale}")
+        _close(st, st_ref, rtol=1e-12, what="final state")
+        for b in range(B):
+            s_ = k[b, 0] @ q[b, 0]
+            want = np.stack([scipy.special.softmax(s_[:i + 1]) @ v[b, 0, :i + 1] for i in range(N)])
+            _close(ref[b, 0], want, rtol=1e-12, what=f"large scores scale={scale}")
 
 
 ALL_PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_")]

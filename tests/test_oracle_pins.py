@@ -62,6 +62,10 @@ MUTATIONS = {
     "bwd_elu_vjp_branch": ("(x[d] > 0.0 ? 1.0 : exp(x[d]))", "(x[d] > 0.0 ? exp(x[d]) : 1.0)"),
     "bwd_prf_vjp_drops_x": ("dx[d] -= s * x[d];", "dx[d] -= 0.0 * s * x[d];"),
     "bwd_prf_vjp_transposed_W": ("dx[d] += c * W[(long)r * D + d];", "dx[d] += c * W[(long)d * m + r];"),
+    "prefix_u_not_rescaled": ("st[1] = st[1] * a + b;", "st[1] = st[1] + b;"),
+    "prefix_no_running_max": ("double mn = s > m ? s : m;", "double mn = s;"),
+    "prefix_w_drops_weight": ("st[2 + c] = st[2 + c] * a + b * v[c];", "st[2 + c] = st[2 + c] * a + v[c];"),
+    "prefix_score_wrong_index": ("        s += q[d] * k[d];\n    double m = st[0];", "        s += q[d] * k[0];\n    double m = st[0];"),
 }
 
 
