@@ -32,6 +32,7 @@ STATUS_NAMES = {0: "LA_OK", -1: "LA_ERR_NULL", -2: "LA_ERR_DIM", -3: "LA_ERR_DTY
                 -4: "LA_ERR_FEATURE", -5: "LA_ERR_CUDA", -6: "LA_ERR_TIMEOUT",
                 -7: "LA_ERR_ALIGN"}
 EXPORTED = ("la_forward", "la_forward_ex", "la_forward_host", "la_step", "la_backward",
+            "la_prefix_attention", "la_prefix_step",
             "la_status_string",
             "la_check", "la_shutdown", "la_version", "la_launch_count",
             "la_forward_noncausal_noalloc", "la_selftest_timeout")
@@ -100,6 +101,10 @@ def load(path: str | None = None):
     lib.la_step.restype = i
     lib.la_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, fm, i, vp]
     lib.la_backward.restype = i
+    lib.la_prefix_attention.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
+    lib.la_prefix_attention.restype = i
+    lib.la_prefix_step.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, vp]
+    lib.la_prefix_step.restype = i
     lib.la_status_string.argtypes = [i]
     lib.la_status_string.restype = ctypes.c_char_p
     lib.la_check.argtypes = [vp]
@@ -267,6 +272,44 @@ def la_backward(q, k, v, dout, causal=True, feature_map: FeatureMap | None = Non
                             _stream(stream))
     _raise(st)
     return dq, dk, dv
+
+
+def la_prefix_attention(q, k, v, out=None, state_out=None, return_state=False, stream=None):
+    """la_prefix_attention: softmax attention of the query token q [B,H,D] over
+    every prefix of k [B,H,N,D], v [B,H,N,Dv] -> out [B,H,N,Dv] (and the final
+    state [B,H,Dv+2] = (m, u, w) when ``return_state`` or ``state_out``)."""
+    B, H, N, D = k.shape
+    Dv = v.shape[-1]
+    if tuple(q.shape) != (B, H, D) or tuple(v.shape[:3]) != (B, H, N):
+        raise ValueError("shape mismatch between q, k, v")
+    if out is None:
+        out = torch.empty((B, H, N, Dv), dtype=k.dtype, device=k.device)
+    dt = _check_tensors(q, k, v, out)
+    if return_state and state_out is None:
+        state_out = torch.empty((B, H, Dv + 2), dtype=torch.float32, device=k.device)
+    if state_out is not None and (state_out.dtype != torch.float32 or not state_out.is_contiguous()):
+        raise ValueError("state_out must be a contiguous fp32 CUDA tensor")
+    st = load().la_prefix_attention(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                    state_out.data_ptr() if state_out is not None else None,
+                                    B, H, N, D, Dv, dt, _stream(stream))
+    _raise(st)
+    return (out, state_out) if state_out is not None else out
+
+
+def la_prefix_step(state, q, k, v, out=None, stream=None):
+    """la_prefix_step: one token of the prefix-attention RNN; state [B,H,Dv+2]
+    fp32 is updated in place; q, k [B,H,D], v [B,H,Dv] -> out [B,H,Dv]."""
+    B, H, D = q.shape
+    Dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((B, H, Dv), dtype=q.dtype, device=q.device)
+    dt = _check_tensors(q, k, v, out)
+    if state.dtype != torch.float32 or not state.is_contiguous() or tuple(state.shape) != (B, H, Dv + 2):
+        raise ValueError("state must be a contiguous fp32 [B, H, Dv + 2] CUDA tensor")
+    st = load().la_prefix_step(state.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                               B, H, D, Dv, dt, _stream(stream))
+    _raise(st)
+    return out
 
 
 def la_check(stream=None) -> int:

@@ -64,6 +64,17 @@ size_t backward_scratch_bytes(const Problem &p, bool causal);
 cudaError_t backward(const Problem &p, const void *dout, void *dq, void *dk, void *dv, bool causal,
                      void *scratch, cudaStream_t s);
 
+// Softmax attention of one query token per head over every prefix (the
+// many-to-many outputs of attention as an RNN), one pass with decoupled
+// look-back over tiles; state (m, u, w) [BH, Dv + 2].  D, Dv <= 128.
+size_t prefix_scratch_bytes(long long BH, int N, int Dv);
+cudaError_t prefix_attention(const void *q, const void *k, const void *v, void *out, float *state_out,
+                             long long BH, int N, int D, int Dv, int dtype, void *scratch, int *err,
+                             cudaStream_t s);
+cudaError_t prefix_empty_state(float *state, long long BH, int Dv, cudaStream_t s);
+cudaError_t prefix_step(float *state, const void *q, const void *k, const void *v, void *out, long long BH,
+                        int D, int Dv, int dtype, cudaStream_t s);
+
 // One recurrent decode step for BH heads, in place on S [BH, P, Dv], z [BH, P].
 cudaError_t step(float *S, float *z, const void *q, const void *k, const void *v, void *out,
                  long long BH, int D, int Dv, int P, int kind, int m, const float *W,

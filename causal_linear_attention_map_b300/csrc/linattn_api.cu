@@ -199,6 +199,33 @@ int backward_impl(const void *q, const void *k, const void *v, const void *dout,
     return cuda_status(e != cudaSuccess ? e : e2);
 }
 
+int prefix_impl(const void *q, const void *k, const void *v, void *out, float *state_out, int B, int H, int N,
+                int D, int Dv, int dtype, void *stream)
+{
+    if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_DTYPE;
+    if (B < 0 || H < 0 || N < 0 || !head_dim_ok(D) || !head_dim_ok(Dv)) return LA_ERR_DIM;
+    const long long BH = (long long)B * H;
+    if (BH > 0x7fffffffLL || BH * (((long long)N + 255) / 256) > 0x7fffffffLL) return LA_ERR_DIM;
+    if (!aligned16(state_out)) return LA_ERR_ALIGN;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (BH == 0) return LA_OK;
+    if (N == 0) {   // empty sequence: the empty state (m = -inf, u = 0, w = 0)
+        if (!state_out) return LA_OK;
+        return cuda_status(la::prefix_empty_state(state_out, BH, Dv, s));
+    }
+    if (!q || !k || !v || !out) return LA_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return LA_ERR_ALIGN;
+    DeviceCtx *ctx = nullptr;
+    int st = get_ctx(&ctx);
+    if (st != LA_OK) return st;
+    void *scratch = nullptr;
+    if (cudaMallocFromPoolAsync(&scratch, la::prefix_scratch_bytes(BH, N, Dv), ctx->pool, s) != cudaSuccess)
+        return cuda_status(cudaErrorMemoryAllocation);
+    cudaError_t e = la::prefix_attention(q, k, v, out, state_out, BH, N, D, Dv, dtype, scratch, ctx->err_word, s);
+    cudaError_t e2 = cudaFreeAsync(scratch, s);
+    return cuda_status(e != cudaSuccess ? e : e2);
+}
+
 // la_forward_host: at most kHostGroups head groups, each with at least
 // kHostGroupBytes of inputs (a group's forward has a fixed cost of a few
 // launches, so small problems take few groups)
@@ -325,6 +352,26 @@ int la_backward(const void *q, const void *k, const void *v, const void *dout, v
                 void *stream)
 {
     return backward_impl(q, k, v, dout, dq, dk, dv, B, H, N, D, Dv, causal, fm, dtype, stream);
+}
+
+int la_prefix_attention(const void *q, const void *k, const void *v, void *out, float *state_out, int B, int H,
+                        int N, int D, int Dv, int dtype, void *stream)
+{
+    return prefix_impl(q, k, v, out, state_out, B, H, N, D, Dv, dtype, stream);
+}
+
+int la_prefix_step(float *state, const void *q, const void *k, const void *v, void *out, int B, int H, int D,
+                   int Dv, int dtype, void *stream)
+{
+    if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_DTYPE;
+    if (B < 0 || H < 0 || !head_dim_ok(D) || !head_dim_ok(Dv)) return LA_ERR_DIM;
+    const long long BH = (long long)B * H;
+    if (BH > 0x7fffffffLL) return LA_ERR_DIM;
+    if (BH == 0) return LA_OK;
+    if (!state || !q || !k || !v || !out) return LA_ERR_NULL;
+    if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return LA_ERR_ALIGN;
+    return cuda_status(la::prefix_step(state, q, k, v, out, BH, D, Dv, dtype, (cudaStream_t)stream));
 }
 
 int la_step(float *S, float *z, const void *q, const void *k, const void *v, void *out, int B,

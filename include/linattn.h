@@ -181,6 +181,40 @@ int la_backward(const void *q, const void *k, const void *v, const void *dout,
                 void *dq, void *dk, void *dv, int B, int H, int N, int D, int Dv,
                 int causal, const la_feature_map *fm, int dtype, void *stream);
 
+/*
+ * la_prefix_attention -- softmax attention read as an RNN, with its
+ * many-to-many outputs (review page "Attention as an RNN", proposed method:
+ * attention is a many-to-one RNN over the keys and values with a learned
+ * query token q; its outputs after every prefix come from a parallel prefix
+ * scan).  Per head, with s_i = q . k_i (no 1/sqrt(D) factor: scale q):
+ *     out_k = sum_{i<=k} exp(s_i) v_i / sum_{i<=k} exp(s_i)     (k = 0..N-1)
+ * The RNN state is (m, u, w): the largest score so far, sum exp(s_i - m) and
+ * sum exp(s_i - m) v_i.  q [B, H, D]; k [B, H, N, D]; v, out [B, H, N, Dv]
+ * in `dtype` (device); state_out (nullable, device fp32 [B, H, Dv + 2], laid
+ * out as m, u, w_0..w_{Dv-1}) receives each head's state after position
+ * N - 1 (for N = 0: the empty state m = -inf, u = 0, w = 0), which
+ * la_prefix_step continues from.  D, Dv in {16, 32, 64, 128}.  One pass over
+ * K and V (a single-pass scan with decoupled look-back across tiles of 256
+ * positions); takes stream-ordered scratch from the library's pool.  Bounded
+ * waits: a wait on another tile that runs out sets the error that la_check
+ * reports as LA_ERR_TIMEOUT.
+ */
+int la_prefix_attention(const void *q, const void *k, const void *v, void *out,
+                        float *state_out, int B, int H, int N, int D, int Dv,
+                        int dtype, void *stream);
+
+/*
+ * la_prefix_step -- one token of the same RNN for B*H heads ("Attention as
+ * an RNN": new tokens update the constant-size state): with s = q . k,
+ *     m' = max(m, s),  u' = u e^(m - m') + e^(s - m'),
+ *     w' = w e^(m - m') + e^(s - m') v,   out = w' / u'.
+ * state [B, H, Dv + 2] fp32 (in/out, device); q, k [B, H, D], v, out
+ * [B, H, Dv] in `dtype` (device).  Starting from the empty state and
+ * stepping through a sequence gives la_prefix_attention's outputs.
+ */
+int la_prefix_step(float *state, const void *q, const void *k, const void *v, void *out,
+                   int B, int H, int D, int Dv, int dtype, void *stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *la_status_string(int status);
 

@@ -163,3 +163,28 @@ def test_backward_validation_codes(lib):
     assert bw(ptrs=[FAKE + 8] + p[1:]) == -7
     assert bw(B=0) == 0
     assert bw(N=0, ptrs=[0] * 7) == 0
+
+
+def test_prefix_validation_codes(lib):
+    p = [FAKE + 256 * i for i in range(5)]
+
+    def pa(*, B=1, H=2, N=8, D=64, Dv=64, dtype=1, ptrs=p):
+        return lib.la_prefix_attention(*ptrs, B, H, N, D, Dv, dtype, None)
+
+    assert pa(dtype=4) == -3
+    assert pa(D=256) == -2
+    assert pa(Dv=48) == -2
+    assert pa(N=-1) == -2
+    for i in range(4):
+        assert pa(ptrs=p[:i] + [0] + p[i + 1:]) == -1
+    assert pa(ptrs=p[:4] + [FAKE + 4]) == -7
+    assert pa(B=0) == 0
+
+    def ps(*, B=1, H=2, D=64, Dv=64, dtype=1, ptrs=p):
+        return lib.la_prefix_step(*ptrs, B, H, D, Dv, dtype, None)
+
+    assert ps(dtype=4) == -3
+    assert ps(D=20) == -2
+    for i in range(5):
+        assert ps(ptrs=p[:i] + [0] + p[i + 1:]) == -1
+    assert ps(H=0) == 0

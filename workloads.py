@@ -12,7 +12,9 @@ one); then cast to the workload dtype.  The PRF projection W [m, D] is iid
 N(0, 1) fp32 from its own seed.  Decode inputs for step t come from seed
 ``DECODE_SEED + t``.  The output cotangent of a backward pass, dout
 [B,H,N,Dv], is iid N(0, 1) from seed ``seed + DOUT_SEED_OFFSET``, cast to the
-workload dtype.
+workload dtype.  The query token of prefix attention, q [B,H,D], is iid
+N(0, 1) / sqrt(D) (unscaled for fp32 workloads) from seed
+``seed + PREFIX_Q_SEED_OFFSET``.
 """
 from __future__ import annotations
 
@@ -69,6 +71,7 @@ DECODE_STEPS = 4096
 DECODE_SEED = 4000
 W_SEED = 5000
 DOUT_SEED_OFFSET = 7000
+PREFIX_Q_SEED_OFFSET = 8000
 
 TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
 
@@ -95,6 +98,15 @@ def make_dout(w: Workload, device="cpu"):
     """Output cotangent dout [B,H,N,Dv] for a backward pass, iid N(0, 1)."""
     gen = torch.Generator().manual_seed(w.seed + DOUT_SEED_OFFSET)
     x = _randn((w.B, w.H, w.N, w.Dv), gen)
+    return x.to(TORCH_DTYPE[w.dtype]).to(device).contiguous()
+
+
+def make_prefix_q(w: Workload, device="cpu"):
+    """Query token q [B,H,D] of prefix attention (one per head)."""
+    gen = torch.Generator().manual_seed(w.seed + PREFIX_Q_SEED_OFFSET)
+    x = _randn((w.B, w.H, w.D), gen)
+    if w.scaled:
+        x.mul_(1.0 / math.sqrt(w.D))
     return x.to(TORCH_DTYPE[w.dtype]).to(device).contiguous()
 
 
