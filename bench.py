@@ -71,6 +71,35 @@ def alg_flops(w: wl.Workload) -> int:
     return w.token_heads * f
 
 
+def alg_bytes_backward(w: wl.Workload) -> int:
+    """Algorithmic HBM bytes of one backward: read q, k, v, dout; write dq, dk, dv."""
+    e = 2 if w.dtype == "bf16" else 4
+    return w.token_heads * (4 * w.D + 3 * w.Dv) * e
+
+
+def alg_flops_backward(w: wl.Workload) -> int:
+    """Algorithmic FLOPs of the backward's RNN form per token-head: the forward
+    recomputed (4 P Dv), d phi(q) (2 P Dv), the reverse memory (2 P Dv), d phi(k)
+    and dv (4 P Dv), vector terms (10 P + 4 Dv); PRF adds the projections of
+    q and k and their chain rule (16 m D)."""
+    P = w.phi_dim
+    f = 12 * P * w.Dv + 10 * P + 4 * w.Dv
+    if w.feature == "prf":
+        f += 16 * w.m * w.D
+    return w.token_heads * f
+
+
+def alg_bytes_prefix(w: wl.Workload) -> int:
+    """Prefix attention: read k, v and write out per token-head, plus q per head."""
+    e = 2 if w.dtype == "bf16" else 4
+    return w.token_heads * (w.D + 2 * w.Dv) * e + w.B * w.H * w.D * e
+
+
+def alg_flops_prefix(w: wl.Workload) -> int:
+    """Per token-head: the score (2 D), the state update and readout (4 Dv + 6)."""
+    return w.token_heads * (2 * w.D + 4 * w.Dv + 6)
+
+
 def decode_bytes_per_step(BH, P, Dv, D, e=2) -> int:
     """S and z read+write (fp32), q, k, v read and out written (dtype)."""
     return BH * (2 * P * Dv * 4 + 2 * P * 4 + (2 * D + 2 * Dv) * e)
@@ -266,6 +295,75 @@ def cpu_baseline(w: wl.Workload, q, k, v, W, budget_s=12.0, reps_min=1):
             "seconds_per_call": dt, "calls": len(times), "whole_workload": whole}
 
 
+def timed_steps(la, fn, args, dev, stream, ws, rank, scrub):
+    """W warm-up calls of fn, then K timed ones with CUDA events on ``stream``.
+    With ``scrub`` (inputs that fit in L2) every step is timed alone after
+    writing the scrub buffer, behind a device-side delay that covers the host
+    enqueue; else the K steps are timed back to back.  Returns (total ms, the
+    slowest rank's; library launches in the timed region; clocks)."""
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    if rank == 0:
+        sampler.start()
+    for _ in range(args.warmup):
+        fn()
+        if scrub is not None:
+            scrub.fill_(1.0)
+    barrier(ws)
+    n0 = la.la_launch_count()
+    t_wall0 = time.time()
+    if scrub is not None:
+        total_ms = 0.0
+        for _ in range(args.steps):
+            scrub.fill_(1.0)
+            # a device-side delay before the start event, so that the host has
+            # queued the whole call by the time the GPU reaches it (the timed
+            # region then holds only the call's device work; host cost per
+            # call is in e2e)
+            torch.cuda._sleep(HOST_COVER_CYCLES)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            total_ms += e0.elapsed_time(e1)
+    else:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        e1.synchronize()
+        total_ms = e0.elapsed_time(e1)
+    barrier(ws)
+    sampler.mark(t_wall0, time.time())
+    # stop polling nvidia-smi once the timed region is over: its driver queries
+    # would otherwise slow the host-bound e2e steps of the small workloads
+    clocks = sampler.stop() if rank == 0 else None
+    launches = la.la_launch_count() - n0
+    return max_over_ranks(total_ms, ws), launches, clocks
+
+
+def hbm_roofline(ab, af, seconds, kernel):
+    """The roofline entry for ``ab`` algorithmic bytes and ``af`` flops done in
+    ``seconds``: the slower of the HBM time and the dense bf16 tensor time."""
+    pk, pk_kind = peaks()
+    t_hbm = ab / (pk["hbm_gbs"] * 1e9)
+    t_flop = af / (pk["bf16_tflops"] * 1e12)
+    bound = "hbm" if t_hbm >= t_flop else "tensor"
+    if bound == "hbm":
+        achieved, peak, unit = ab / seconds / 1e9, pk["hbm_gbs"], "GB/s"
+    else:
+        achieved, peak, unit = af / seconds / 1e12, pk["bf16_tflops"], "TFLOP/s"
+    return {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4),
+            "peak_source": f"{pk_kind} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})",
+            "kernel": kernel, "alg_bytes_per_launch": ab, "alg_flops_per_launch": af,
+            "roofline_time_us": round(max(t_hbm, t_flop) * 1e6, 2),
+            "frac_of_roofline_time": round(max(t_hbm, t_flop) / seconds, 4)}
+
+
 def measure_forward(la, w: wl.Workload, args, dev, stream, ws, rank, with_e2e=True,
                     with_cpu=True, keep_state=False):
     """Time la_forward_ex over workload ``w`` (inputs resident in HBM), then
@@ -287,48 +385,7 @@ def measure_forward(la, w: wl.Workload, args, dev, stream, ws, rank, with_e2e=Tr
         la.la_forward_ex(dq, dk, dv, causal=w.causal, feature_map=fm, out=out, S_out=S_out,
                          z_out=z_out, stream=stream)
 
-    sampler = ClockSampler(dev.index if dev.index is not None else 0)
-    if rank == 0:
-        sampler.start()
-    for _ in range(args.warmup):
-        fwd()
-        if flush:
-            scrub.fill_(1.0)
-    barrier(ws)
-    n0 = la.la_launch_count()
-    t_wall0 = time.time()
-    if flush:
-        total_ms = 0.0
-        for _ in range(args.steps):
-            scrub.fill_(1.0)
-            # a device-side delay before the start event, so that the host has
-            # queued the whole forward by the time the GPU reaches it (the
-            # timed region then holds only the forward's device work; host
-            # cost per call is in e2e)
-            torch.cuda._sleep(HOST_COVER_CYCLES)
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            fwd()
-            e1.record(stream)
-            e1.synchronize()
-            total_ms += e0.elapsed_time(e1)
-    else:
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            fwd()
-        e1.record(stream)
-        e1.synchronize()
-        total_ms = e0.elapsed_time(e1)
-    barrier(ws)
-    sampler.mark(t_wall0, time.time())
-    # stop polling nvidia-smi once the timed region is over: its driver queries
-    # would otherwise slow the host-bound e2e steps of the small workloads
-    clocks = sampler.stop() if rank == 0 else None
-    launches = la.la_launch_count() - n0
-    total_ms = max_over_ranks(total_ms, ws)
+    total_ms, launches, clocks = timed_steps(la, fwd, args, dev, stream, ws, rank, scrub)
     ms_step = total_ms / args.steps
     tokens = w.B * w.N
     value = job_rate(tokens, args.steps, ws, total_ms)
@@ -406,6 +463,106 @@ def measure_forward(la, w: wl.Workload, args, dev, stream, ws, rank, with_e2e=Tr
     return entry
 
 
+def oracle_timed(w: wl.Workload, call, budget_s: float, cost_factor: float, what: str):
+    """Time ``call(n_heads, n_pos)`` (an oracle routine over the first heads and
+    positions of the workload) on a bounded sample; the sample is sized like
+    oracle_sample with its cost scaled by ``cost_factor``."""
+    import oracle
+
+    cores = oracle.num_threads(oracle.load())
+    n_heads, n_pos = oracle_sample(w, budget_s / 2 / cost_factor, cores)
+    times = []
+    while not times or (sum(times) < budget_s / 2 and len(times) < 20):
+        t0 = time.perf_counter()
+        call(n_heads, n_pos)
+        times.append(time.perf_counter() - t0)
+    dt = statistics.median(times)
+    th = n_heads * n_pos
+    BH = w.B * w.H
+    return {"value": th / w.H / dt, "unit": "tokens/s", "cores": min(cores, n_heads), "kind": "oracle",
+            "sample": f"{n_heads} of {BH} heads x first {n_pos} of {w.N} positions ({th} token-heads), "
+                      f"fp64 {what}, OpenMP over heads; median of {len(times)} calls, {dt:.3f} s each"}
+
+
+def measure_backward(la, w: wl.Workload, args, dev, stream, ws, rank, with_cpu=True):
+    """la_backward over workload ``w`` (inputs resident in HBM)."""
+    q, k, v = wl.make_qkv(w)
+    do = wl.make_dout(w)
+    W = wl.make_W(w.m, w.D) if w.feature == "prf" else None
+    dq_, dk_, dv_, ddo = (t.to(dev) for t in (q, k, v, do))
+    fm = la.FeatureMap("prf", W.to(dev)) if W is not None else None
+    gq, gk, gv = torch.empty_like(dq_), torch.empty_like(dk_), torch.empty_like(dv_)
+    nbytes = sum(t.numel() * t.element_size() for t in (dq_, dk_, dv_, ddo, gq, gk, gv))
+    scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if nbytes < 2 * L2_BYTES else None
+
+    def fn():
+        la.la_backward(dq_, dk_, dv_, ddo, causal=w.causal, feature_map=fm, dq=gq, dk=gk, dv=gv, stream=stream)
+
+    total_ms, launches, clocks = timed_steps(la, fn, args, dev, stream, ws, rank, scrub)
+    ms = total_ms / args.steps
+    entry = {"workload": w.name, "value": job_rate(w.B * w.N, args.steps, ws, total_ms), "unit": "tokens/s",
+             "ms_per_step": ms, "gpu_launches": launches,
+             "roofline": hbm_roofline(alg_bytes_backward(w), alg_flops_backward(w), ms / 1e3,
+                                      "la_backward (all of its launches, timed together)"),
+             "l2": "L2 flushed between steps" if scrub is not None else "tensors larger than L2",
+             "path": "CUDA cores, fp32 arithmetic"}
+    if clocks:
+        entry["clocks"] = clocks
+    if with_cpu and rank == 0 and ws == 1:
+        import oracle
+
+        BH = w.B * w.H
+        Wn = W.double().numpy() if W is not None else None
+
+        def call(nh, npos):
+            sl = lambda t, c: t.reshape(BH, w.N, c)[:nh, :npos].double().numpy()[None]
+            oracle.backward(sl(q, w.D), sl(k, w.D), sl(v, w.Dv), sl(do, w.Dv), causal=w.causal,
+                            feature=w.feature, W=Wn)
+
+        log(f"timing the backward oracle ({w.name}) ...")
+        entry["cpu_baseline"] = oracle_timed(w, call, args.cpu_budget / 2, 3.0, "reverse-mode recurrence")
+    del dq_, dk_, dv_, ddo, gq, gk, gv, scrub
+    return entry
+
+
+def measure_prefix(la, w: wl.Workload, args, dev, stream, ws, rank, with_cpu=True):
+    """la_prefix_attention over the workload's keys and values with its query token."""
+    q = wl.make_prefix_q(w)
+    _, k, v = wl.make_qkv(w)
+    dq_, dk_, dv_ = (t.to(dev) for t in (q, k, v))
+    out = torch.empty_like(dv_)
+    nbytes = sum(t.numel() * t.element_size() for t in (dk_, dv_, out))
+    scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if nbytes < 2 * L2_BYTES else None
+
+    def fn():
+        la.la_prefix_attention(dq_, dk_, dv_, out=out, stream=stream)
+
+    total_ms, launches, clocks = timed_steps(la, fn, args, dev, stream, ws, rank, scrub)
+    ms = total_ms / args.steps
+    entry = {"workload": w.name, "value": job_rate(w.B * w.N, args.steps, ws, total_ms), "unit": "tokens/s",
+             "ms_per_step": ms, "gpu_launches": launches,
+             "roofline": hbm_roofline(alg_bytes_prefix(w), alg_flops_prefix(w), ms / 1e3,
+                                      "prefix_attn_kernel (one launch)"),
+             "l2": "L2 flushed between steps" if scrub is not None else "tensors larger than L2"}
+    if clocks:
+        entry["clocks"] = clocks
+    if with_cpu and rank == 0 and ws == 1:
+        import oracle
+
+        BH = w.B * w.H
+
+        def call(nh, npos):
+            oracle.prefix_attention(q.reshape(BH, w.D)[:nh].double().numpy()[None],
+                                    k.reshape(BH, w.N, w.D)[:nh, :npos].double().numpy()[None],
+                                    v.reshape(BH, w.N, w.Dv)[:nh, :npos].double().numpy()[None])
+
+        log(f"timing the prefix-attention oracle ({w.name}) ...")
+        entry["cpu_baseline"] = oracle_timed(w, call, args.cpu_budget / 2, 1.0 / max(1, w.D // 8),
+                                             "RNN cell over the prefix")
+    del dq_, dk_, dv_, out, scrub
+    return entry
+
+
 def run_ours(args):
     ws, rank, local = dist_setup()
     import causal_linear_attention_map_b300 as la
@@ -451,6 +608,23 @@ def run_ours(args):
         result["configs"] = configs
         result["gpu_launches"] = sum(c["gpu_launches"] for c in configs.values()) + \
             result.get("decode", {}).get("launches", 0)
+    if args.extras and args.seq_len == 0 and args.workload == wl.LONG_65536.name:
+        # the gradients over every workload, and softmax attention as an RNN
+        # over the long and image workloads' keys and values
+        result["backward"] = {}
+        for other in wl.WORKLOADS.values():
+            log(f"measuring the backward of {other.name} ...")
+            result["backward"][other.name] = measure_backward(la, other, args, dev, stream, ws, rank,
+                                                              with_cpu=not args.no_cpu_baseline)
+            torch.cuda.empty_cache()
+        result["prefix_attention"] = {}
+        for other in (wl.LONG_65536, wl.IMAGE_3072):
+            log(f"measuring prefix attention over {other.name} ...")
+            result["prefix_attention"][other.name] = measure_prefix(la, other, args, dev, stream, ws, rank,
+                                                                    with_cpu=not args.no_cpu_baseline)
+            torch.cuda.empty_cache()
+        result["gpu_launches"] += sum(e["gpu_launches"] for e in result["backward"].values()) + \
+            sum(e["gpu_launches"] for e in result["prefix_attention"].values())
     if rank == 0:
         print(json.dumps(result), flush=True)
     if ws > 1:
@@ -641,6 +815,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=8.0,
                     help="seconds of oracle time per workload for cpu_baseline")
+    ap.add_argument("--no-extras", dest="extras", action="store_false",
+                    help="skip the backward and prefix-attention measurements")
     ap.add_argument("--no-all-configs", dest="all_configs", action="store_false",
                     help="measure only the named workload (default: the long workload plus "
                          "every other workload of the table under 'configs')")
