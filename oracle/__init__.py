@@ -23,7 +23,9 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 
 PHI_ELU1 = 0
 PHI_PRF = 1
-_KINDS = {"elu1": PHI_ELU1, "prf": PHI_PRF}
+PHI_NPRF = 2
+PHI_TRF = 3
+_KINDS = {"elu1": PHI_ELU1, "prf": PHI_PRF, "nprf": PHI_NPRF, "trf": PHI_TRF}
 
 _lib = None
 
@@ -78,9 +80,9 @@ def _ptr(a):
 
 def _fm(feature, W, D):
     kind = _KINDS[feature]
-    if kind == PHI_PRF:
+    if kind != PHI_ELU1:
         if W is None:
-            raise ValueError("PRF needs W")
+            raise ValueError("random features need W")
         W = _d(W)
         if W.ndim != 2 or W.shape[1] != D:
             raise ValueError("W must be [m, D]")
@@ -89,7 +91,10 @@ def _fm(feature, W, D):
 
 
 def phi_dim(D, feature="elu1", m=0):
-    return m if _KINDS[feature] == PHI_PRF else D
+    kind = _KINDS[feature]
+    if kind == PHI_ELU1:
+        return D
+    return 2 * m if kind == PHI_TRF else m
 
 
 def num_threads(lib=None) -> int:

@@ -46,6 +46,8 @@
 
 #define ORACLE_PHI_ELU1 0
 #define ORACLE_PHI_PRF 1
+#define ORACLE_PHI_NPRF 2
+#define ORACLE_PHI_TRF 3
 
 int oracle_num_threads(void)
 {
@@ -58,7 +60,9 @@ int oracle_num_threads(void)
 
 int oracle_phi_dim(int D, int kind, int m)
 {
-    return kind == ORACLE_PHI_PRF ? m : D;
+    if (kind == ORACLE_PHI_ELU1)
+        return D;
+    return kind == ORACLE_PHI_TRF ? 2 * m : m;
 }
 
 /* elu(x) + 1 with alpha = 1 ("Transformers are RNNs", main results b2). */
@@ -78,16 +82,29 @@ void oracle_phi(const double *x, int D, int kind, const double *W, int m,
             f[d] = elu_plus_one(x[d]);
         return;
     }
-    /* positive random features: exp(w_r . x - |x|^2 / 2) / sqrt(m) */
     double sq = 0.0;
     for (int d = 0; d < D; d++)
         sq += x[d] * x[d];
     double inv_sqrt_m = 1.0 / sqrt((double)m);
+    /* NPRF reads the direction x / |x| (x = 0 reads as 0) */
+    double scale = (kind == ORACLE_PHI_NPRF && sq > 0.0) ? 1.0 / sqrt(sq) : 1.0;
     for (int r = 0; r < m; r++) {
         double wx = 0.0;
         for (int d = 0; d < D; d++)
             wx += W[(long)r * D + d] * x[d];
-        f[r] = exp(wx - 0.5 * sq) * inv_sqrt_m;
+        wx *= scale;
+        if (kind == ORACLE_PHI_PRF) {
+            /* positive random features: exp(w_r . x - |x|^2 / 2) / sqrt(m) */
+            f[r] = exp(wx - 0.5 * sq) * inv_sqrt_m;
+        } else if (kind == ORACLE_PHI_NPRF) {
+            /* PRF of the unit vector: exp(w_r . x/|x| - 1/2) / sqrt(m) (0 for x = 0: -0) */
+            f[r] = exp(wx - (sq > 0.0 ? 0.5 : 0.0)) * inv_sqrt_m;
+        } else {
+            /* trigonometric: exp(|x|^2 / 2) / sqrt(m) [cos(w_r . x), sin(w_r . x)] */
+            double a = exp(0.5 * sq) * inv_sqrt_m;
+            f[r] = a * cos(wx);
+            f[m + r] = a * sin(wx);
+        }
     }
 }
 
@@ -265,17 +282,49 @@ static void phi_vjp(const double *x, const double *df, int D, int kind,
         return;
     }
     oracle_phi(x, D, kind, W, m, f);
-    double s = 0.0;
-    for (int d = 0; d < D; d++)
+    double sq = 0.0;
+    for (int d = 0; d < D; d++) {
+        sq += x[d] * x[d];
         dx[d] = 0.0;
-    for (int r = 0; r < m; r++) {
-        double c = df[r] * f[r];
-        s += c;
-        for (int d = 0; d < D; d++)
-            dx[d] += c * W[(long)r * D + d];
     }
-    for (int d = 0; d < D; d++)
-        dx[d] -= s * x[d];
+    if (kind == ORACLE_PHI_PRF) {
+        /* d phi_r / dx = phi_r (w_r - x) */
+        double s = 0.0;
+        for (int r = 0; r < m; r++) {
+            double c = df[r] * f[r];
+            s += c;
+            for (int d = 0; d < D; d++)
+                dx[d] += c * W[(long)r * D + d];
+        }
+        for (int d = 0; d < D; d++)
+            dx[d] -= s * x[d];
+    } else if (kind == ORACLE_PHI_NPRF) {
+        /* with y = x/|x|: d phi_r / dy = phi_r w_r, and dy/dx = (I - y y^T) / |x| */
+        if (sq == 0.0)
+            return;
+        double n = sqrt(sq), dy_y = 0.0;
+        for (int r = 0; r < m; r++) {
+            double c = df[r] * f[r];
+            for (int d = 0; d < D; d++)
+                dx[d] += c * W[(long)r * D + d];
+        }
+        for (int d = 0; d < D; d++)
+            dy_y += dx[d] * x[d] / n;
+        for (int d = 0; d < D; d++)
+            dx[d] = (dx[d] - dy_y * x[d] / n) / n;
+    } else {
+        /* phi_c = a cos(u), phi_s = a sin(u), a = exp(|x|^2/2)/sqrt(m), u = W x:
+         * dx = x sum_r (dc_r phi_c + ds_r phi_s) + sum_r w_r (ds_r phi_c - dc_r phi_s) */
+        double s = 0.0;
+        for (int r = 0; r < m; r++) {
+            s += df[r] * f[r] + df[m + r] * f[m + r];
+            double c = df[m + r] * f[r] - df[r] * f[m + r];
+            for (int d = 0; d < D; d++)
+                dx[d] += c * W[(long)r * D + d];
+        }
+        for (int d = 0; d < D; d++)
+            dx[d] += s * x[d];
+    }
 }
 
 /* R += g dn^T ;  r += g dd  (the reverse memories, one query's terms) */

@@ -21,6 +21,12 @@ section "proposed method" b6, for positive random features):
     step iterated N times = the forward pass, head and key/value
     permutations, linearity in V;
   - the PRF kernel's expectation E_w[phi(q).phi(k)] = exp(q.k).
+Further feature maps the same page names (PRF, TRF, Sphere-PRF, ORF, NPRF;
+readings: TRF = exp(|x|^2/2)/sqrt(m) [cos(Wx), sin(Wx)], NPRF = PRF of x/|x|):
+  - TRF's expectation E_w[phi(q).phi(k)] = exp(q.k) (Gaussian W);
+  - NPRF's expectation exp(q.k / (|q| |k|)), and its invariance to scaling
+    each query and key by a positive factor;
+  - their gradients by finite differences (below).
 Gradients ("Transformers are RNNs", proposed method b4: linear-time
 gradients of the same cumulative-sum form):
   - central finite differences of the forward oracle (itself pinned above);
@@ -71,8 +77,15 @@ def _py_phi(x, feature, W):
         return [xi + 1.0 if xi > 0 else math.exp(xi) for xi in x]
     m = len(W)
     sq = sum(xi * xi for xi in x)
-    return [math.exp(sum(w * xi for w, xi in zip(W[r], x)) - sq / 2) / math.sqrt(m)
-            for r in range(m)]
+    if feature == "nprf":
+        n = math.sqrt(sq)
+        x = [xi / n for xi in x]
+        sq = 1.0
+    u = [sum(w * xi for w, xi in zip(W[r], x)) for r in range(m)]
+    if feature == "trf":
+        a = math.exp(sq / 2) / math.sqrt(m)
+        return [a * math.cos(t) for t in u] + [a * math.sin(t) for t in u]
+    return [math.exp(t - sq / 2) / math.sqrt(m) for t in u]
 
 
 def _py_attention(q, k, v, causal, feature, W):
@@ -97,11 +110,14 @@ def _py_attention(q, k, v, causal, feature, W):
 def pin_pure_python_brute_force(lib):
     r = _rng(1)
     for (N, D, Dv, feature, m) in [(7, 3, 2, "elu1", 0), (9, 2, 5, "elu1", 0),
-                                   (6, 3, 4, "prf", 5), (5, 1, 1, "elu1", 0)]:
+                                   (6, 3, 4, "prf", 5), (5, 1, 1, "elu1", 0),
+                                   (6, 3, 2, "nprf", 4), (7, 2, 3, "trf", 6)]:
         q = r.normal(size=(1, 2, N, D))
         k = r.normal(size=(1, 2, N, D))
         v = r.normal(size=(1, 2, N, Dv))
-        W = r.normal(size=(m, D)) if feature == "prf" else None
+        W = r.normal(size=(m, D)) if feature != "elu1" else None
+        if feature == "trf":
+            W = W * 0.3
         Wl = W.tolist() if W is not None else None
         for causal in (True, False):
             got = oracle.forward(q, k, v, causal=causal, feature=feature, W=W, lib=lib)
@@ -251,6 +267,40 @@ def pin_prf_kernel_expectation(lib):
         assert np.all(fq > 0) and np.all(fk > 0)
 
 
+def pin_trf_and_nprf_kernel_expectations(lib):
+    """E over w ~ N(0, I): TRF gives exp(q.k) (the random Fourier features of
+    the Gaussian kernel times exp(|q|^2/2 + |k|^2/2)), NPRF gives
+    exp(q.k / (|q||k|)).  Checked to a few standard errors with m = 2**16."""
+    r = _rng(30)
+    D, m = 4, 1 << 16
+    W = r.normal(size=(m, D))
+    for _ in range(3):
+        q = r.normal(size=D) * 0.4
+        k = r.normal(size=D) * 0.4
+        for feature, target in (("trf", math.exp(float(q @ k))),
+                                ("nprf", math.exp(float(q @ k) / np.linalg.norm(q) / np.linalg.norm(k)))):
+            fq = oracle.phi(q[None], feature, W, lib=lib)[0]
+            fk = oracle.phi(k[None], feature, W, lib=lib)[0]
+            t = fq * fk
+            terms = m * (t[:m] + t[m:]) if feature == "trf" else m * t
+            se = terms.std() / math.sqrt(m)
+            assert abs(float(fq @ fk) - target) < 5 * se + 1e-12, (feature, float(fq @ fk), target, se)
+        assert fq.shape == (2 * m,) or feature != "trf"
+
+
+def pin_nprf_scale_invariance(lib):
+    r = _rng(31)
+    B, H, N, D, Dv = 1, 2, 30, 5, 3
+    W = r.normal(size=(8, D))
+    q, k, v = (r.normal(size=(B, H, N, x)) for x in (D, D, Dv))
+    cq = np.exp(r.normal(size=(B, H, N, 1)))
+    ck = np.exp(r.normal(size=(B, H, N, 1)))
+    for causal in (True, False):
+        a = oracle.forward(q, k, v, causal=causal, feature="nprf", W=W, lib=lib)
+        b = oracle.forward(q * cq, k * ck, v, causal=causal, feature="nprf", W=W, lib=lib)
+        _close(a, b, rtol=1e-12, what=f"NPRF scale invariance causal={causal}")
+
+
 # ------------------------------------------------------------- invariants
 
 def pin_convex_hull(lib):
@@ -348,9 +398,12 @@ def pin_backward_finite_differences(lib):
     r = _rng(16)
     B, H, N, D, Dv = 1, 2, 5, 3, 2
     h = 1e-5
-    for feature, W in (("elu1", None), ("prf", r.normal(size=(4, D)) * 0.7)):
+    for feature, W in (("elu1", None), ("prf", r.normal(size=(4, D)) * 0.7),
+                       ("nprf", r.normal(size=(4, D))), ("trf", r.normal(size=(6, D)) * 0.3)):
         for causal in (True, False):
             q, k, v, do = (r.normal(size=(B, H, N, x)) for x in (D, D, Dv, Dv))
+            if feature == "trf":   # small inputs keep the trigonometric denominator away from 0
+                q, k = q * 0.3, k * 0.3
             got = oracle.backward(q, k, v, do, causal=causal, feature=feature, W=W, lib=lib)
             for t, (x, g) in enumerate(zip((q, k, v), got)):
                 fd = np.empty_like(x)

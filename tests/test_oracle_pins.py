@@ -62,6 +62,14 @@ MUTATIONS = {
     "bwd_elu_vjp_branch": ("(x[d] > 0.0 ? 1.0 : exp(x[d]))", "(x[d] > 0.0 ? exp(x[d]) : 1.0)"),
     "bwd_prf_vjp_drops_x": ("dx[d] -= s * x[d];", "dx[d] -= 0.0 * s * x[d];"),
     "bwd_prf_vjp_transposed_W": ("dx[d] += c * W[(long)r * D + d];", "dx[d] += c * W[(long)d * m + r];"),
+    "nprf_not_normalised": ("double scale = (kind == ORACLE_PHI_NPRF && sq > 0.0) ? 1.0 / sqrt(sq) : 1.0;",
+                            "double scale = 1.0;"),
+    "trf_sin_cos_swapped": ("f[r] = a * cos(wx);\n            f[m + r] = a * sin(wx);",
+                            "f[r] = a * sin(wx);\n            f[m + r] = a * cos(wx);"),
+    "trf_exponent_sign": ("double a = exp(0.5 * sq) * inv_sqrt_m;", "double a = exp(-0.5 * sq) * inv_sqrt_m;"),
+    "bwd_nprf_no_projection": ("dx[d] = (dx[d] - dy_y * x[d] / n) / n;", "dx[d] = dx[d] / n;"),
+    "bwd_trf_rotation_sign": ("double c = df[m + r] * f[r] - df[r] * f[m + r];",
+                              "double c = df[r] * f[m + r] - df[m + r] * f[r];"),
     "prefix_u_not_rescaled": ("st[1] = st[1] * a + b;", "st[1] = st[1] + b;"),
     "prefix_no_running_max": ("double mn = s > m ? s : m;", "double mn = s;"),
     "prefix_w_drops_weight": ("st[2 + c] = st[2 + c] * a + b * v[c];", "st[2 + c] = st[2 + c] * a + v[c];"),
