@@ -25,14 +25,15 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "liblinattn.so")
 
 LA_F32, LA_BF16 = 0, 1
-LA_PHI_ELU1, LA_PHI_PRF = 0, 1
+LA_PHI_ELU1, LA_PHI_PRF, LA_PHI_NPRF, LA_PHI_TRF = 0, 1, 2, 3
+LA_W_GAUSSIAN, LA_W_ORTHOGONAL, LA_W_SPHERE = 0, 1, 2
 LA_OK = 0
 LA_NOALLOC_SCRATCH_BYTES = 4 << 20   # the fixed scratch of la_forward_noncausal_noalloc
 STATUS_NAMES = {0: "LA_OK", -1: "LA_ERR_NULL", -2: "LA_ERR_DIM", -3: "LA_ERR_DTYPE",
                 -4: "LA_ERR_FEATURE", -5: "LA_ERR_CUDA", -6: "LA_ERR_TIMEOUT",
                 -7: "LA_ERR_ALIGN"}
 EXPORTED = ("la_forward", "la_forward_ex", "la_forward_host", "la_step", "la_backward",
-            "la_prefix_attention", "la_prefix_step",
+            "la_prefix_attention", "la_prefix_step", "la_random_features",
             "la_status_string",
             "la_check", "la_shutdown", "la_version", "la_launch_count",
             "la_forward_noncausal_noalloc", "la_selftest_timeout")
@@ -50,30 +51,46 @@ class LinAttnError(RuntimeError):
         self.status = status
 
 
+_KINDS = {"elu1": LA_PHI_ELU1, "prf": LA_PHI_PRF, "nprf": LA_PHI_NPRF, "trf": LA_PHI_TRF}
+
+
 class FeatureMap:
-    """phi: ``FeatureMap()`` is elu(x)+1; ``FeatureMap("prf", W)`` uses the
-    m x D fp32 CUDA tensor W: phi_r(x) = exp(w_r.x - |x|^2/2)/sqrt(m)."""
+    """phi: ``FeatureMap()`` is elu(x)+1; ``FeatureMap(kind, W)`` with an m x D
+    fp32 CUDA tensor W is a random-feature map: "prf" exp(w_r.x - |x|^2/2)/sqrt(m),
+    "nprf" the same of x/|x|, "trf" exp(|x|^2/2)/sqrt(m) [cos(Wx), sin(Wx)]
+    (2m features).  Sphere-PRF and ORF are "prf" with W from la_random_features."""
 
     def __init__(self, kind: str = "elu1", W: torch.Tensor | None = None):
-        if kind not in ("elu1", "prf"):
+        if kind not in _KINDS:
             raise ValueError(kind)
         self.kind = kind
         self.W = W
-        if kind == "prf":
+        if kind != "elu1":
             if W is None or W.dtype != torch.float32 or not W.is_cuda or not W.is_contiguous():
-                raise ValueError("PRF needs W as a contiguous fp32 CUDA tensor [m, D]")
+                raise ValueError("random features need W as a contiguous fp32 CUDA tensor [m, D]")
 
     @property
     def m(self) -> int:
-        return self.W.shape[0] if self.kind == "prf" else 0
+        return self.W.shape[0] if self.kind != "elu1" else 0
 
     def phi_dim(self, D: int) -> int:
-        return self.m if self.kind == "prf" else D
+        if self.kind == "elu1":
+            return D
+        return 2 * self.m if self.kind == "trf" else self.m
 
     def c_struct(self) -> la_feature_map:
-        if self.kind == "prf":
-            return la_feature_map(LA_PHI_PRF, self.W.shape[0], self.W.data_ptr())
+        if self.kind != "elu1":
+            return la_feature_map(_KINDS[self.kind], self.W.shape[0], self.W.data_ptr())
         return la_feature_map(LA_PHI_ELU1, 0, None)
+
+
+def la_random_features(m: int, D: int, seed: int, kind: str = "gaussian") -> torch.Tensor:
+    """W [m, D] fp32 (host) from la_random_features: kind "gaussian",
+    "orthogonal" (ORF) or "sphere" (Sphere-PRF)."""
+    codes = {"gaussian": LA_W_GAUSSIAN, "orthogonal": LA_W_ORTHOGONAL, "sphere": LA_W_SPHERE}
+    W = torch.empty((m, D), dtype=torch.float32)
+    _raise(load().la_random_features(codes[kind], m, D, seed, W.data_ptr()))
+    return W
 
 
 _lib = None
@@ -105,6 +122,8 @@ def load(path: str | None = None):
     lib.la_prefix_attention.restype = i
     lib.la_prefix_step.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, vp]
     lib.la_prefix_step.restype = i
+    lib.la_random_features.argtypes = [i, i, i, ctypes.c_ulonglong, vp]
+    lib.la_random_features.restype = i
     lib.la_status_string.argtypes = [i]
     lib.la_status_string.restype = ctypes.c_char_p
     lib.la_check.argtypes = [vp]

@@ -52,13 +52,13 @@ __host__ __device__ inline BwdSmem bwd_layout(const BwdGeo &g, bool dq_pass)
     L.V = o;   o += C * Dv;
     L.O = o;   o += C * Dv;   // dout (dq pass: then out)
     L.Mn = o;  o += C * Dv;   // dnum
-    L.X = o;   o += g.kind == PHI_PRF ? C * D : 0;   // raw q (dq) or k (dk) rows for the PRF chain rule
+    L.X = o;   o += g.kind != PHI_ELU1 ? C * D : 0;   // raw q (dq) or k (dk) rows for the random-feature chain rule
     L.dX = o;  o += C * P;    // dG or dF before the chain rule through phi
     L.A = o;   o += C * C;
     L.B = o;   o += C * C;
     L.den = o; o += C;
     L.dd = o;  o += C;
-    L.sq = o;  o += C;
+    L.sq = o;  o += 2 * C;   // |x|^2 per row, then the chain rule's two per-row sums
     L.total = o * sizeof(float);
     return L;
 }
@@ -88,15 +88,15 @@ __device__ void phi_rows(const T *__restrict__ x, int t0, int n, const BwdGeo &g
         sq[i] = s;
     }
     __syncthreads();
-    const float inv_sqrt_m = rsqrtf((float)P);
+    const int m = rf_m(g.kind, P);
     for (int idx = threadIdx.x; idx < C * P; idx += blockDim.x) {
         const int i = idx / P, r = idx % P;
         float val = 0.f;
         if (i < n) {
-            const float *wr = W + (long long)r * D;
+            const float *wr = W + (long long)rf_proj(g.kind, r, m) * D;
             float u = 0.f;
             for (int d = 0; d < D; d++) u = fmaf(wr[d], X[i * D + d], u);
-            val = expf(u - 0.5f * sq[i]) * inv_sqrt_m;
+            val = rf_value(g.kind, r, m, u, sq[i]);
         }
         f[idx] = val;
     }
@@ -112,30 +112,65 @@ __device__ void load_rows(const T *__restrict__ x, int t0, int n, int C, int W, 
 }
 
 // The chain rule through phi for rows [0, n): dx = J_phi(x)^T dphi, written
-// to out rows [t0, t0 + n).  elu + 1: d phi / dx = 1 (x > 0), exp(x) else,
-// which is min(phi(x), 1).  PRF: dx = sum_r t_r w_r - x sum_r t_r with
-// t_r = dphi_r phi_r(x).
+// to out rows [t0, t0 + n).  With t_r = dphi_r phi_r (and for TRF the pairs
+// (cos, sin) of projection r):
+//   elu + 1  d phi / dx = 1 (x > 0), exp(x) else, which is min(phi(x), 1)
+//   PRF      dx = sum_r t_r w_r - x sum_r t_r
+//   NPRF     dy = sum_r t_r w_r for y = x/|x|, then dx = (dy - y (y . dy)) / |x|
+//   TRF      dx = x sum_r t_r + sum_r w_r (dsin_r phi_cos_r - dcos_r phi_sin_r)
+// tmp holds 2 C floats.
 template <typename T>
 __device__ void phi_chain(const float *f, const float *dphi, const float *X, const BwdGeo &g,
                           const float *__restrict__ W, int t0, int n, float *tmp, T *__restrict__ out)
 {
-    const int C = g.C, D = g.D, P = g.P;
-    if (g.kind == PHI_ELU1) {
+    const int C = g.C, D = g.D, P = g.P, kind = g.kind;
+    if (kind == PHI_ELU1) {
         for (int idx = threadIdx.x; idx < n * D; idx += blockDim.x)
             out[(long long)t0 * D + idx] = from_f32<T>(dphi[idx] * fminf(f[idx], 1.f));
         return;
     }
+    const int m = rf_m(kind, P);
+    // per row: sum_r t_r and |x|^2
     for (int i = threadIdx.x; i < C; i += blockDim.x) {
-        float s = 0.f;
+        float s = 0.f, sq = 0.f;
         for (int r = 0; r < P; r++) s = fmaf(dphi[i * P + r], f[i * P + r], s);
+        for (int d = 0; d < D; d++) sq = fmaf(X[i * D + d], X[i * D + d], sq);
         tmp[i] = s;
+        tmp[C + i] = sq;
     }
     __syncthreads();
+    if (kind == PHI_NPRF) {
+        // dy into the out buffer's place is not available: form dy . y per row first
+        for (int i = threadIdx.x; i < C; i += blockDim.x) {
+            float dyy = 0.f;
+            const float inv = tmp[C + i] > 0.f ? rsqrtf(tmp[C + i]) : 0.f;
+            for (int d = 0; d < D; d++) {
+                float dy = 0.f;
+                for (int r = 0; r < m; r++) dy = fmaf(dphi[i * P + r] * f[i * P + r], W[(long long)r * D + d], dy);
+                dyy = fmaf(dy, X[i * D + d] * inv, dyy);
+            }
+            tmp[i] = dyy;
+        }
+        __syncthreads();
+    }
     for (int idx = threadIdx.x; idx < n * D; idx += blockDim.x) {
         const int i = idx / D, d = idx % D;
-        float s = 0.f;
-        for (int r = 0; r < P; r++) s = fmaf(dphi[i * P + r] * f[i * P + r], W[(long long)r * D + d], s);
-        out[(long long)t0 * D + idx] = from_f32<T>(s - tmp[i] * X[i * D + d]);
+        float s = 0.f, val;
+        if (kind == PHI_TRF) {
+            for (int r = 0; r < m; r++)
+                s = fmaf(dphi[i * P + m + r] * f[i * P + r] - dphi[i * P + r] * f[i * P + m + r],
+                         W[(long long)r * D + d], s);
+            val = s + tmp[i] * X[i * D + d];
+        } else {
+            for (int r = 0; r < m; r++) s = fmaf(dphi[i * P + r] * f[i * P + r], W[(long long)r * D + d], s);
+            if (kind == PHI_PRF) {
+                val = s - tmp[i] * X[i * D + d];
+            } else {   // NPRF
+                const float inv = tmp[C + i] > 0.f ? rsqrtf(tmp[C + i]) : 0.f;
+                val = (s - tmp[i] * X[i * D + d] * inv) * inv;
+            }
+        }
+        out[(long long)t0 * D + idx] = from_f32<T>(val);
     }
 }
 

@@ -34,6 +34,27 @@ __device__ __forceinline__ float phi_elu1_fast(float x) { return x > 0.f ? x + 1
 
 __host__ __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
+// Random-feature maps with projections u_r = w_r . x (r < m) of a row x with
+// |x|^2 = sq (review page "Stable, Fast and Accurate: Kernelized Attention
+// with RPE", proposed method: PRF, TRF, Sphere-PRF, ORF, NPRF; Sphere-PRF and
+// ORF are PRF with other distributions of W).  kind: 1 PRF, 2 NPRF, 3 TRF
+// (the values of kernels.h's PHI_*).  Feature r of Dphi = rf_dim(kind, m):
+//   PRF   exp(u_r - sq/2) / sqrt(m)
+//   NPRF  PRF of x / |x|:  exp(u_r / |x| - 1/2) / sqrt(m)   (x = 0: 1 / sqrt(m))
+//   TRF   exp(sq/2) / sqrt(m) * (cos u_r for r < m, sin u_{r-m} for r >= m)
+__host__ __device__ __forceinline__ int rf_dim(int kind, int m) { return kind == 3 ? 2 * m : m; }
+__host__ __device__ __forceinline__ int rf_m(int kind, int P) { return kind == 3 ? P / 2 : P; }
+// the projection that feature r reads
+__device__ __forceinline__ int rf_proj(int kind, int r, int m) { return kind == 3 && r >= m ? r - m : r; }
+__device__ __forceinline__ float rf_value(int kind, int r, int m, float u, float sq)
+{
+    const float inv = rsqrtf((float)m);
+    if (kind == 1) return expf(u - 0.5f * sq) * inv;
+    if (kind == 2) return sq > 0.f ? expf(u * rsqrtf(sq) - 0.5f) * inv : inv;
+    const float a = expf(0.5f * sq) * inv;
+    return r < m ? a * cosf(u) : a * sinf(u);
+}
+
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per kernel and
 // device (bit d of the mask: device d < 64; others set it on every call),
 // so that a forward call does not pay for it again.

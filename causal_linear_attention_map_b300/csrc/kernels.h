@@ -10,7 +10,7 @@ namespace la {
 void note_launches(int n);
 
 enum { DT_F32 = 0, DT_BF16 = 1 };
-enum { PHI_ELU1 = 0, PHI_PRF = 1 };
+enum { PHI_ELU1 = 0, PHI_PRF = 1, PHI_NPRF = 2, PHI_TRF = 3 };
 
 // One validated forward problem.  Pointers are device pointers.
 struct Problem {
@@ -18,7 +18,7 @@ struct Problem {
     void *out;
     long long BH;  // B * H heads
     int N, D, Dv;
-    int P;         // feature dimension: D (elu+1) or m (PRF)
+    int P;         // feature dimension: D (elu+1), m (PRF, NPRF) or 2m (TRF)
     int kind;      // PHI_*
     int m;
     const float *W;

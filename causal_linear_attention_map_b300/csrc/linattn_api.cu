@@ -80,8 +80,8 @@ int check_common(int B, int H, int D, int Dv, const la_feature_map *fm, int dtyp
     *kind = fm ? fm->kind : LA_PHI_ELU1;
     *m = 0;
     *W = nullptr;
-    if (*kind == LA_PHI_PRF) {
-        if (!prf_m_ok(fm->m)) return LA_ERR_FEATURE;
+    if (*kind == LA_PHI_PRF || *kind == LA_PHI_NPRF || *kind == LA_PHI_TRF) {
+        if (!prf_m_ok(fm->m) || (*kind == LA_PHI_TRF && fm->m > 128)) return LA_ERR_FEATURE;
         if (!fm->W) return LA_ERR_FEATURE;
         if (!aligned16(fm->W)) return LA_ERR_ALIGN;
         *m = fm->m;
@@ -91,7 +91,7 @@ int check_common(int B, int H, int D, int Dv, const la_feature_map *fm, int dtyp
     }
     if (B < 0 || H < 0) return LA_ERR_DIM;
     if (!head_dim_ok(D) || !head_dim_ok(Dv)) return LA_ERR_DIM;
-    *P = *kind == LA_PHI_PRF ? *m : D;
+    *P = *kind == LA_PHI_ELU1 ? D : *kind == LA_PHI_TRF ? 2 * *m : *m;
     if ((long long)*P * Dv > 32768) return LA_ERR_DIM;
     return LA_OK;
 }

@@ -35,16 +35,16 @@ __device__ void phi_rows(const T *__restrict__ x, long long t0, int n, int D, in
         sq[i] = s;
     }
     __syncthreads();
-    const float inv_sqrt_m = rsqrtf((float)P);
+    const int m = rf_m(kind, P);
     for (int idx = tid; idx < kC * P; idx += blockDim.x) {
         int i = idx / P, r = idx % P;
         float val = 0.f;
         if (i < n) {
             const T *xr = x + (t0 + i) * D;
-            const float *wr = W + (long long)r * D;
+            const float *wr = W + (long long)rf_proj(kind, r, m) * D;
             float u = 0.f;
             for (int d = 0; d < D; d++) u = fmaf(wr[d], to_f32(xr[d]), u);
-            val = expf(u - 0.5f * sq[i]) * inv_sqrt_m;
+            val = rf_value(kind, r, m, u, sq[i]);
         }
         f[idx] = val;
     }

@@ -75,9 +75,10 @@ extern "C" int la_forward_noncausal_noalloc(const void *q, const void *k, const 
     const int kind = fm ? fm->kind : LA_PHI_ELU1;
     int m = 0;
     const float *W = nullptr;
-    if (kind == LA_PHI_PRF) {
+    if (kind == LA_PHI_PRF || kind == LA_PHI_NPRF || kind == LA_PHI_TRF) {
         m = fm->m;
         if (m != 16 && m != 32 && m != 64 && m != 128 && m != 256) return LA_ERR_FEATURE;
+        if (kind == LA_PHI_TRF && m > 128) return LA_ERR_FEATURE;
         if (!fm->W) return LA_ERR_FEATURE;
         if (!a16(fm->W)) return LA_ERR_ALIGN;
         W = fm->W;
@@ -86,7 +87,7 @@ extern "C" int la_forward_noncausal_noalloc(const void *q, const void *k, const 
     }
     if (B < 0 || H < 0 || N < 0 || !dim_ok(D) || !dim_ok(Dv)) return LA_ERR_DIM;
     const long long BH = (long long)B * H;
-    const int P = kind == LA_PHI_PRF ? m : D;
+    const int P = kind == LA_PHI_ELU1 ? D : kind == LA_PHI_TRF ? 2 * m : m;
     if (BH * P * (long long)(Dv + 1) * 4 > (long long)LA_NOALLOC_SCRATCH_BYTES) return LA_ERR_DIM;
     if (BH == 0 || N == 0) return LA_OK;
     if (!q || !k || !v || !out) return LA_ERR_NULL;

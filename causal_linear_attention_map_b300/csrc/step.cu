@@ -34,13 +34,13 @@ __device__ __forceinline__ void phi_vec(const T *__restrict__ x, int D, int P, i
         if (tid == 0) red[0] = s;
     }
     __syncthreads();
-    const float half_sq = 0.5f * red[0];
-    const float inv_sqrt_m = rsqrtf((float)P);
+    const float sq = red[0];
+    const int m = rf_m(kind, P);
     for (int r = tid; r < P; r += blockDim.x) {
-        const float *wr = W + (long long)r * D;
+        const float *wr = W + (long long)rf_proj(kind, r, m) * D;
         float u = 0.f;
         for (int d = 0; d < D; d++) u = fmaf(wr[d], to_f32(x[d]), u);
-        f[r] = expf(u - half_sq) * inv_sqrt_m;
+        f[r] = rf_value(kind, r, m, u, sq);
     }
     __syncthreads();
 }

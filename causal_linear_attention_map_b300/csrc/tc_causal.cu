@@ -1414,7 +1414,7 @@ template <int D, int M>
 __global__ void __launch_bounds__(kNcThreads, 1)
 prf_phi_kernel(const __grid_constant__ CUtensorMap tm_xq, const __grid_constant__ CUtensorMap tm_xk,
                const __grid_constant__ CUtensorMap tm_pq, const __grid_constant__ CUtensorMap tm_pk,
-               const float *__restrict__ W, int T, float log_scale, int *err)
+               const float *__restrict__ W, int T, float log_scale, int normalize, int *err)
 {
     using PL = PrfPlan<D, M>;
     constexpr int NX = PL::NX, NO = PL::NO;
@@ -1571,7 +1571,9 @@ prf_phi_kernel(const __grid_constant__ CUtensorMap tm_xq, const __grid_constant_
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&x_empty[st]);
-            const float shift = 0.5f * ss + log_scale;
+            // PRF: exp(u - |x|^2/2 - ln(m)/2); NPRF (normalize): exp(u/|x| - 1/2 - ln(m)/2)
+            const float uscale = normalize ? (ss > 0.f ? rsqrtf(ss) : 0.f) : 1.f;
+            const float shift = normalize ? (ss > 0.f ? 0.5f : 0.f) + log_scale : 0.5f * ss + log_scale;
             wait_bar(&acc_full[a], (n >> 1) & 1, ctl);
             tc_fence_after();
             if (n >= NO) wait_bar(&o_free[os], ((n / NO) - 1) & 1, ctl);
@@ -1587,8 +1589,8 @@ prf_phi_kernel(const __grid_constant__ CUtensorMap tm_xq, const __grid_constant_
                     uint32_t w[4];
 #pragma unroll
                     for (int i = 0; i < 4; i++)
-                        w[i] = pack_bf16x2(__expf(__uint_as_float(v[8 * j + 2 * i]) - shift),
-                                           __expf(__uint_as_float(v[8 * j + 2 * i + 1]) - shift));
+                        w[i] = pack_bf16x2(__expf(__uint_as_float(v[8 * j + 2 * i]) * uscale - shift),
+                                           __expf(__uint_as_float(v[8 * j + 2 * i + 1]) * uscale - shift));
                     sts128(ot + (uint32_t)(col >> 6) * (kC * 128) + sw128_off(r, (col & 63) >> 3),
                            make_uint4(w[0], w[1], w[2], w[3]));
                 }
@@ -1952,7 +1954,7 @@ cudaError_t run_prf_phi(const Problem &p, void *phq, void *phk, int *err, cudaSt
         return e;
     const float log_scale = (float)(0.5 * std::log((double)M));
     prf_phi_kernel<64, M><<<min(2 * T, num_sms()), kNcThreads, PP::SMEM, s>>>(xq, xk, pq, pk, p.W, T, log_scale,
-                                                                             err);
+                                                                             p.kind == PHI_NPRF ? 1 : 0, err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     note_launches(1);
     return cudaSuccess;
@@ -2088,7 +2090,7 @@ bool tc_causal_supported(const Problem &p)
 
 bool tc_prf_supported(const Problem &p)
 {
-    return p.dtype == DT_BF16 && p.kind == PHI_PRF && p.D == 64 &&
+    return p.dtype == DT_BF16 && (p.kind == PHI_PRF || p.kind == PHI_NPRF) && p.D == 64 &&
            ((p.m == 128 && (p.Dv == 64 || p.Dv == 128)) || (p.m == 256 && p.Dv == 64)) &&
            p.BH * (long long)p.N < (1LL << 31) - kC;
 }
@@ -2096,7 +2098,7 @@ bool tc_prf_supported(const Problem &p)
 size_t tc_scratch_bytes(const Problem &p, bool causal)
 {
     Geo g = plan(p.BH, p.N, num_sms());
-    if (p.kind == PHI_PRF) return prf_layout(p, g, causal).total;
+    if (p.kind == PHI_PRF || p.kind == PHI_NPRF) return prf_layout(p, g, causal).total;
     if (p.D == 64 && p.Dv == 64) return elu_scratch_bytes<64, 64>(g, causal);
     if (p.D == 64 && p.Dv == 128) return elu_scratch_bytes<64, 128>(g, causal);
     if (p.D == 128 && p.Dv == 64) return elu_scratch_bytes<128, 64>(g, causal);
@@ -2106,7 +2108,7 @@ size_t tc_scratch_bytes(const Problem &p, bool causal)
 cudaError_t tc_forward(const Problem &p, bool causal, void *scratch, float *S_out, float *z_out, int *err,
                        cudaStream_t s)
 {
-    if (p.kind == PHI_PRF) {
+    if (p.kind == PHI_PRF || p.kind == PHI_NPRF) {
         if (p.m == 256) return run_prf<256, 64>(p, scratch, S_out, z_out, err, s, causal);
         if (p.Dv == 64) return run_prf<128, 64>(p, scratch, S_out, z_out, err, s, causal);
         return run_prf<128, 128>(p, scratch, S_out, z_out, err, s, causal);

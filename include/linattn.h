@@ -43,11 +43,13 @@
  *    (cudaGetLastError is consumed).  Nothing is thrown and nothing aborts.
  *  - Supported sizes: B, H, N >= 0 (a zero size is a no-op that returns
  *    LA_OK; la_forward_ex then writes zero states); D and Dv in
- *    {16, 32, 64, 128}; PRF m in {16, 32, 64, 128, 256} (else LA_ERR_FEATURE).
- *  - Execution: bf16 inputs with elu+1 and D, Dv in {64, 128}, or with PRF,
- *    D = 64 and (m = 128, Dv in {64, 128}) or (m = 256, Dv = 64), run on the
- *    tensor cores (tcgen05); every other supported case (fp32, other sizes)
- *    runs on the CUDA cores.  Both compute the same sums; rounding differs.
+ *    {16, 32, 64, 128}; random-feature m in {16, 32, 64, 128, 256}, TRF
+ *    m <= 128 (else LA_ERR_FEATURE); Dphi * Dv <= 32768.
+ *  - Execution: bf16 inputs with elu+1 and D, Dv in {64, 128}, or with PRF or
+ *    NPRF, D = 64 and (m = 128, Dv in {64, 128}) or (m = 256, Dv = 64), run on
+ *    the tensor cores (tcgen05); every other supported case (fp32, TRF, other
+ *    sizes) runs on the CUDA cores.  Both compute the same sums; rounding
+ *    differs.
  *  - Scratch: la_forward may take stream-ordered scratch memory from a
  *    library-owned CUDA memory pool on the current device (per-segment
  *    states of the causal scan, partial sums of the non-causal pass, the
@@ -69,15 +71,24 @@ typedef enum {
     LA_BF16 = 1  /* bfloat16 q, k, v, out */
 } la_dtype;
 
+/* Feature maps (review page "Stable, Fast and Accurate: Kernelized Attention
+ * with Relative Positional Encoding", proposed method: PRF, TRF, Sphere-PRF,
+ * ORF and the normalised NPRF are supported maps; the page names them without
+ * formulas, and these are the standard definitions).  Sphere-PRF and ORF are
+ * LA_PHI_PRF with W drawn by la_random_features (LA_W_SPHERE, LA_W_ORTHOGONAL). */
 typedef enum {
-    LA_PHI_ELU1 = 0, /* elu(x) + 1 */
-    LA_PHI_PRF = 1   /* positive random features exp(Wx - |x|^2/2)/sqrt(m) */
+    LA_PHI_ELU1 = 0, /* elu(x) + 1                                        Dphi = D  */
+    LA_PHI_PRF = 1,  /* exp(Wx - |x|^2/2) / sqrt(m)                       Dphi = m  */
+    LA_PHI_NPRF = 2, /* PRF of x/|x|: exp(Wx/|x| - 1/2) / sqrt(m)         Dphi = m  */
+    LA_PHI_TRF = 3   /* exp(|x|^2/2)/sqrt(m) [cos(Wx), sin(Wx)]           Dphi = 2m */
 } la_feature_kind;
 
 /* Feature-map descriptor.  Host memory, read during the call only.
- * kind: la_feature_kind.  m: PRF feature count (ignored for ELU1).
- * W: DEVICE pointer to the m x D fp32 row-major projection (PRF; NULL for
- * ELU1).  A NULL descriptor means ELU1. */
+ * kind: la_feature_kind.  m: the number of projections (rows of W; ignored
+ * for ELU1): 16, 32, 64, 128 or 256 (TRF: at most 128).
+ * W: DEVICE pointer to the m x D fp32 row-major projection (NULL for ELU1).
+ * A NULL descriptor means ELU1.  TRF's features are not positive, so its
+ * denominator can approach zero; PRF and NPRF keep it positive. */
 typedef struct {
     int kind;
     int m;
@@ -214,6 +225,23 @@ int la_prefix_attention(const void *q, const void *k, const void *v, void *out,
  */
 int la_prefix_step(float *state, const void *q, const void *k, const void *v, void *out,
                    int B, int H, int D, int Dv, int dtype, void *stream);
+
+/*
+ * la_random_features -- draw a projection W (m x D fp32, row-major) into
+ * HOST memory `W`, deterministically from `seed` (a SplitMix64 counter
+ * stream turned into N(0, 1) draws by the Box-Muller transform):
+ *   LA_W_GAUSSIAN    every entry iid N(0, 1) (plain PRF / TRF / NPRF);
+ *   LA_W_ORTHOGONAL  orthogonal random features: rows in blocks of D that are
+ *                    orthogonal (Gram-Schmidt of a Gaussian D x D matrix),
+ *                    each row rescaled to the norm of an independent
+ *                    Gaussian D-vector (the last block keeps m mod D rows);
+ *   LA_W_SPHERE      each row uniform on the sphere of radius sqrt(D)
+ *                    (Sphere-PRF).
+ * m, D >= 1.  Host-only: no device work.  Returns LA_ERR_NULL / LA_ERR_DIM /
+ * LA_ERR_FEATURE (unknown w_kind) or LA_OK.
+ */
+typedef enum { LA_W_GAUSSIAN = 0, LA_W_ORTHOGONAL = 1, LA_W_SPHERE = 2 } la_w_kind;
+int la_random_features(int w_kind, int m, int D, unsigned long long seed, float *W);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *la_status_string(int status);

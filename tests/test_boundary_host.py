@@ -188,3 +188,44 @@ def test_prefix_validation_codes(lib):
     for i in range(5):
         assert ps(ptrs=p[:i] + [0] + p[i + 1:]) == -1
     assert ps(H=0) == 0
+
+
+def test_random_features_draws(lib):
+    """la_random_features (host): deterministic by seed; Gaussian moments;
+    ORF rows orthogonal within blocks of D with Gaussian-like norms; Sphere
+    rows of norm sqrt(D); each gives valid positive random features for the
+    softmax kernel (E[phi(q).phi(k)] = exp(q.k), through the oracle's map)."""
+    import math
+
+    import numpy as np
+
+    import causal_linear_attention_map_b300 as la
+    import oracle
+
+    m, D = 4096, 16
+    Wg = la.la_random_features(m, D, 11).numpy()
+    assert np.array_equal(Wg, la.la_random_features(m, D, 11).numpy())
+    assert not np.array_equal(Wg, la.la_random_features(m, D, 12).numpy())
+    assert abs(Wg.mean()) < 0.02 and abs(Wg.var() - 1.0) < 0.03
+    Wo = la.la_random_features(m + 5, D, 3, "orthogonal").numpy().astype(np.float64)
+    for b0 in range(0, m + 5, D):
+        blk = Wo[b0:b0 + D]
+        G = blk @ blk.T
+        nrm = np.sqrt(np.diag(G))
+        off = G - np.diag(np.diag(G))
+        assert np.max(np.abs(off)) <= 1e-5 * np.max(nrm) ** 2
+    assert abs(np.mean(np.sum(Wo ** 2, axis=1)) - D) < 0.05 * D   # E|w|^2 = D, as for Gaussian rows
+    Ws = la.la_random_features(m, D, 4, "sphere").numpy().astype(np.float64)
+    assert np.allclose(np.linalg.norm(Ws, axis=1), math.sqrt(D), rtol=1e-6)
+    r = np.random.default_rng(0)
+    q, k = r.normal(size=D) * 0.3, r.normal(size=D) * 0.3
+    for W in (Wg, Wo, Ws):
+        W = W[: (m // D) * D].astype(np.float64)
+        fq = oracle.phi(q[None], "prf", W)[0]
+        fk = oracle.phi(k[None], "prf", W)[0]
+        t = W.shape[0] * fq * fk
+        assert abs(float(fq @ fk) - math.exp(float(q @ k))) < 5 * t.std() / math.sqrt(W.shape[0])
+    st = lib.la_random_features(7, m, D, 1, ctypes.c_void_p(FAKE))
+    assert st == -4
+    assert lib.la_random_features(0, 0, D, 1, ctypes.c_void_p(FAKE)) == -2
+    assert lib.la_random_features(0, m, D, 1, None) == -1
