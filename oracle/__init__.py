@@ -64,6 +64,7 @@ def _bind(lib):
     lib.oracle_backward.argtypes = [P, P, P, P, P, P, P, L, L, I, I, I, I, P, I]
     lib.oracle_prefix_attention.argtypes = [P, P, P, P, L, L, I, I, P]
     lib.oracle_prefix_step.argtypes = [P, P, P, P, P, L, I, I]
+    lib.oracle_rpe.argtypes = [P, P, P, P, P, L, L, I, I, I, I, I, P, I]
     lib.oracle_num_threads.restype = I
     return lib
 
@@ -157,6 +158,23 @@ def backward(q, k, v, dout, causal=True, feature="elu1", W=None, lib=None):
     lib.oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
                         B * H, N, D, Dv, int(causal), kind, _ptr(W), m)
     return dq, dk, dv
+
+
+def rpe(q, k, v, b, causal=True, feature="elu1", W=None, lib=None):
+    """Kernelized attention with a Toeplitz relative-position weight exp(b):
+    q, k [B,H,N,D], v [B,H,N,Dv], b [H, 2N-1] (index t + N - 1 for t = i - j)
+    -> out [B,H,N,Dv] (float64)."""
+    lib = lib or load()
+    q, k, v, b = _d(q), _d(k), _d(v), _d(b)
+    B, H, N, D = q.shape
+    Dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != (B, H, N) or b.shape != (H, 2 * N - 1):
+        raise ValueError("shape mismatch")
+    kind, W, m = _fm(feature, W, D)
+    out = np.empty((B, H, N, Dv))
+    lib.oracle_rpe(_ptr(q), _ptr(k), _ptr(v), _ptr(b), _ptr(out), B * H, N, H, D, Dv, int(causal),
+                   kind, _ptr(W), m)
+    return out
 
 
 def prefix_attention(q, k, v, return_state=False, lib=None):

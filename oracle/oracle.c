@@ -500,3 +500,51 @@ void oracle_prefix_step(double *state, const double *q, const double *k,
         prefix_cell(state + h * (long)(Dv + 2), q + h * D, k + h * D, v + h * Dv,
                     out + h * Dv, D, Dv);
 }
+
+/*
+ * Kernelized attention with relative positional encoding ("Stable, Fast and
+ * Accurate: Kernelized Attention with Relative Positional Encoding",
+ * proposed method: the RPE matrix is Toeplitz - its entry depends only on
+ * i - j - and multiplies the kernelized attention elementwise):
+ *   out_i = sum_{j in J(i)} c_{i-j} (phi(q_i).phi(k_j)) v_j
+ *           / sum_{j in J(i)} c_{i-j} phi(q_i).phi(k_j),      c_t = exp(b_t)
+ * with J(i) = {0..i} (causal) or all positions.  b [H, 2N - 1] holds the
+ * log-weights of head h at index t + N - 1 for t = i - j in [-(N-1), N-1]
+ * (heads bh = b_idx * H + h share row h).  Written out directly, O(N^2).
+ */
+void oracle_rpe(const double *q, const double *k, const double *v,
+                const double *b, double *out, long BH, long N, int H, int D,
+                int Dv, int causal, int kind, const double *W, int m)
+{
+    int P = oracle_phi_dim(D, kind, m);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long h = 0; h < BH; h++) {
+        const double *bh = b + (h % H) * (2 * N - 1);
+        double *fk = malloc((size_t)N * P * sizeof(double));
+        double *fq = malloc((size_t)P * sizeof(double));
+        double *num = malloc((size_t)Dv * sizeof(double));
+        for (long j = 0; j < N; j++)
+            oracle_phi(k + (h * N + j) * D, D, kind, W, m, fk + j * P);
+        for (long i = 0; i < N; i++) {
+            oracle_phi(q + (h * N + i) * D, D, kind, W, m, fq);
+            double den = 0.0;
+            for (int c = 0; c < Dv; c++)
+                num[c] = 0.0;
+            long last = causal ? i : N - 1;
+            for (long j = 0; j <= last; j++) {
+                double a = 0.0;
+                for (int x = 0; x < P; x++)
+                    a += fq[x] * fk[j * P + x];
+                a *= exp(bh[i - j + N - 1]);
+                den += a;
+                for (int c = 0; c < Dv; c++)
+                    num[c] += a * v[(h * N + j) * Dv + c];
+            }
+            for (int c = 0; c < Dv; c++)
+                out[(h * N + i) * Dv + c] = num[c] / den;
+        }
+        free(fk);
+        free(fq);
+        free(num);
+    }
+}

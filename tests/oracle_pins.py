@@ -33,6 +33,13 @@ gradients of the same cumulative-sum form):
   - torch autograd through the masked quadratic form written in torch;
   - closed forms: constant V gives zero gradients for q and k, and the
     gradients for v sum to the sum of the output cotangents.
+Kernelized attention with a Toeplitz relative-position weight (review page
+"Stable, Fast and Accurate: Kernelized Attention with RPE", proposed method:
+the Toeplitz structure, multiplied through by FFT in O(n log n)):
+  - the page's own algorithm, written with numpy's FFT: each Toeplitz
+    matrix-vector product as a circulant convolution of length 2N;
+  - b = 0 gives plain kernelized attention (the forward oracle); a constant
+    added to b changes nothing; pure-Python brute force.
 Softmax attention as an RNN over every prefix (review page "Attention as an
 RNN", proposed method: many-to-one RNN cell, many-to-many outputs by a
 parallel prefix scan, Hillis-Steele):
@@ -539,6 +546,73 @@ def pin_prefix_step_iterated_and_large_scores(lib):
             s_ = k[b, 0] @ q[b, 0]
             want = np.stack([scipy.special.softmax(s_[:i + 1]) @ v[b, 0, :i + 1] for i in range(N)])
             _close(ref[b, 0], want, rtol=1e-12, what=f"large scores scale={scale}")
+
+
+def _rpe_fft(q, k, v, b, causal, feature, W):
+    """The page's FFT method for one head: for every feature a and value
+    column c (and c = the denominator's column of ones), the sequence
+    y_j = phi(k_j)_a v_j,c is convolved with the Toeplitz weights
+    w_t = exp(b_t) (zero for t < 0 when causal) by FFT, and the results are
+    read out with phi(q_i)."""
+    N = q.shape[0]
+    fq = oracle.phi(q, feature, W)
+    fk = oracle.phi(k, feature, W)
+    wt = np.exp(b)                              # index t + N - 1
+    if causal:
+        wt = np.where(np.arange(2 * N - 1) >= N - 1, wt, 0.0)
+    L = 4 * N                                   # room for the full linear convolution
+    Wf = np.fft.rfft(np.concatenate([wt, np.zeros(L - (2 * N - 1))]))
+    vv = np.concatenate([v, np.ones((N, 1))], axis=1)
+    num = np.zeros((N, vv.shape[1]))
+    for a in range(fk.shape[1]):
+        y = fk[:, a:a + 1] * vv                 # [N, Dv + 1]
+        conv = np.fft.irfft(np.fft.rfft(y, n=L, axis=0) * Wf[:, None], n=L, axis=0)
+        # (w * y)[n] with w shifted by N - 1: output i reads n = i + N - 1
+        num += fq[:, a:a + 1] * conv[N - 1:2 * N - 1]
+    return num[:, :-1] / num[:, -1:]
+
+
+def pin_rpe_matches_the_fft_method(lib):
+    r = _rng(40)
+    B, H, N, D, Dv = 1, 2, 19, 3, 2
+    q, k, v = (r.normal(size=(B, H, N, x)) for x in (D, D, Dv))
+    b = r.normal(size=(H, 2 * N - 1)) * 0.7
+    for feature, W in (("elu1", None), ("prf", r.normal(size=(5, D)))):
+        for causal in (True, False):
+            got = oracle.rpe(q, k, v, b, causal=causal, feature=feature, W=W, lib=lib)
+            for h in range(H):
+                ref = _rpe_fft(q[0, h], k[0, h], v[0, h], b[h], causal, feature, W)
+                _close(got[0, h], ref, rtol=1e-10, what=f"RPE vs FFT {feature} causal={causal}")
+
+
+def pin_rpe_zero_bias_and_shift(lib):
+    r = _rng(41)
+    B, H, N, D, Dv = 2, 2, 25, 4, 3
+    q, k, v = (r.normal(size=(B, H, N, x)) for x in (D, D, Dv))
+    for causal in (True, False):
+        got = oracle.rpe(q, k, v, np.zeros((H, 2 * N - 1)), causal=causal, lib=lib)
+        _close(got, oracle.forward(q, k, v, causal=causal, lib=lib), rtol=1e-12, what="b = 0")
+        b = r.normal(size=(H, 2 * N - 1))
+        _close(oracle.rpe(q, k, v, b + 3.0, causal=causal, lib=lib),
+               oracle.rpe(q, k, v, b, causal=causal, lib=lib), rtol=1e-12, what="b + const")
+
+
+def pin_rpe_pure_python(lib):
+    r = _rng(42)
+    N, D, Dv = 8, 2, 2
+    q, k, v = (r.normal(size=(1, 1, N, x)) for x in (D, D, Dv))
+    b = r.normal(size=(1, 2 * N - 1))
+    for causal in (True, False):
+        got = oracle.rpe(q, k, v, b, causal=causal, lib=lib)[0, 0]
+        fq = [_py_phi(x, "elu1", None) for x in q[0, 0].tolist()]
+        fk = [_py_phi(x, "elu1", None) for x in k[0, 0].tolist()]
+        for i in range(N):
+            num, den = [0.0] * Dv, 0.0
+            for j in range(i + 1 if causal else N):
+                a = sum(x * y for x, y in zip(fq[i], fk[j])) * math.exp(b[0, i - j + N - 1])
+                den += a
+                num = [n_ + a * v[0, 0, j, c] for c, n_ in enumerate(num)]
+            _close(got[i], [n_ / den for n_ in num], rtol=1e-12, what=f"RPE brute force {causal}")
 
 
 ALL_PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_")]

@@ -70,6 +70,9 @@ MUTATIONS = {
     "bwd_nprf_no_projection": ("dx[d] = (dx[d] - dy_y * x[d] / n) / n;", "dx[d] = dx[d] / n;"),
     "bwd_trf_rotation_sign": ("double c = df[m + r] * f[r] - df[r] * f[m + r];",
                               "double c = df[r] * f[m + r] - df[m + r] * f[r];"),
+    "rpe_offset_sign": ("a *= exp(bh[i - j + N - 1]);", "a *= exp(bh[j - i + N - 1]);"),
+    "rpe_weight_on_num_only": ("                den += a;\n                for (int c = 0; c < Dv; c++)\n                    num[c] += a * v[(h * N + j) * Dv + c];",
+                               "                den += a / exp(bh[i - j + N - 1]);\n                for (int c = 0; c < Dv; c++)\n                    num[c] += a * v[(h * N + j) * Dv + c];"),
     "prefix_u_not_rescaled": ("st[1] = st[1] * a + b;", "st[1] = st[1] + b;"),
     "prefix_no_running_max": ("double mn = s > m ? s : m;", "double mn = s;"),
     "prefix_w_drops_weight": ("st[2 + c] = st[2 + c] * a + b * v[c];", "st[2 + c] = st[2 + c] * a + v[c];"),
