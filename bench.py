@@ -100,6 +100,20 @@ def alg_flops_prefix(w: wl.Workload) -> int:
     return w.token_heads * (2 * w.D + 4 * w.Dv + 6)
 
 
+def alg_bytes_rpe(w: wl.Workload) -> int:
+    """Kernelized attention with RPE: read q, k, v and b, write out."""
+    e = 2 if w.dtype == "bf16" else 4
+    return w.token_heads * (2 * w.D + 2 * w.Dv) * e + w.H * (2 * w.N - 1) * 4
+
+
+def alg_flops_rpe(w: wl.Workload) -> int:
+    """The weighted form's work: per (query, key) pair the score (2 Dphi), the
+    weight (1) and the accumulation of the value and the denominator
+    (2 Dv + 2); N(N+1)/2 pairs per head when causal, N^2 otherwise."""
+    pairs = w.N * (w.N + 1) // 2 if w.causal else w.N * w.N
+    return w.B * w.H * pairs * (2 * w.phi_dim + 2 * w.Dv + 3)
+
+
 def decode_bytes_per_step(BH, P, Dv, D, e=2) -> int:
     """S and z read+write (fp32), q, k, v read and out written (dtype)."""
     return BH * (2 * P * Dv * 4 + 2 * P * 4 + (2 * D + 2 * Dv) * e)
@@ -525,6 +539,52 @@ def measure_backward(la, w: wl.Workload, args, dev, stream, ws, rank, with_cpu=T
     return entry
 
 
+def measure_rpe(la, w: wl.Workload, args, dev, stream, ws, rank, with_cpu=True):
+    """la_forward_rpe over the workload with its relative-position log-weights."""
+    q, k, v = wl.make_qkv(w)
+    b = wl.make_rpe_bias(w)
+    dq_, dk_, dv_, db = (t.to(dev) for t in (q, k, v, b))
+    out = torch.empty_like(dv_)
+    nbytes = sum(t.numel() * t.element_size() for t in (dq_, dk_, dv_, out))
+    scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if nbytes < 2 * L2_BYTES else None
+
+    def fn():
+        la.la_forward_rpe(dq_, dk_, dv_, db, causal=w.causal, out=out, stream=stream)
+
+    total_ms, launches, clocks = timed_steps(la, fn, args, dev, stream, ws, rank, scrub)
+    ms = total_ms / args.steps
+    entry = {"workload": w.name, "value": job_rate(w.B * w.N, args.steps, ws, total_ms), "unit": "tokens/s",
+             "ms_per_step": ms, "gpu_launches": launches,
+             "roofline": hbm_roofline(alg_bytes_rpe(w), alg_flops_rpe(w), ms / 1e3,
+                                      "rpe_tc_kernel (one launch; chunk-against-chunk weighted form)"),
+             "l2": "L2 flushed between steps" if scrub is not None else "tensors larger than L2"}
+    if clocks:
+        entry["clocks"] = clocks
+    if with_cpu and rank == 0 and ws == 1:
+        import oracle
+
+        BH = w.B * w.H
+
+        def call(nh, npos):
+            sl = lambda t, c: t.reshape(BH, w.N, c)[:nh, :npos].double().numpy()[None]
+            bb = np64_bias(b, nh, npos, w)
+            oracle.rpe(sl(q, w.D), sl(k, w.D), sl(v, w.Dv), bb, causal=w.causal)
+
+        log(f"timing the RPE oracle ({w.name}) ...")
+        entry["cpu_baseline"] = oracle_timed(w, call, args.cpu_budget / 2, w.N / 64.0,
+                                             "quadratic weighted form")
+    del dq_, dk_, dv_, db, out, scrub
+    return entry
+
+
+def np64_bias(b, nh, npos, w):
+    """The log-weight rows of the first nh heads (head index bh % H) for the
+    first npos positions: b[h, t + N - 1] for |t| < npos."""
+    rows = [int(i % w.H) for i in range(nh)]
+    c = w.N - 1
+    return b[rows][:, c - (npos - 1):c + npos].double().numpy()
+
+
 def measure_prefix(la, w: wl.Workload, args, dev, stream, ws, rank, with_cpu=True):
     """la_prefix_attention over the workload's keys and values with its query token."""
     q = wl.make_prefix_q(w)
@@ -623,8 +683,17 @@ def run_ours(args):
             result["prefix_attention"][other.name] = measure_prefix(la, other, args, dev, stream, ws, rank,
                                                                     with_cpu=not args.no_cpu_baseline)
             torch.cuda.empty_cache()
+        # kernelized attention with a Toeplitz relative-position weight, over the
+        # non-causal and the image workloads
+        result["rpe"] = {}
+        for other in (wl.NONCAUSAL_4096, wl.IMAGE_3072):
+            log(f"measuring attention with RPE over {other.name} ...")
+            result["rpe"][other.name] = measure_rpe(la, other, args, dev, stream, ws, rank,
+                                                    with_cpu=not args.no_cpu_baseline)
+            torch.cuda.empty_cache()
         result["gpu_launches"] += sum(e["gpu_launches"] for e in result["backward"].values()) + \
-            sum(e["gpu_launches"] for e in result["prefix_attention"].values())
+            sum(e["gpu_launches"] for e in result["prefix_attention"].values()) + \
+            sum(e["gpu_launches"] for e in result["rpe"].values())
     if rank == 0:
         print(json.dumps(result), flush=True)
     if ws > 1:

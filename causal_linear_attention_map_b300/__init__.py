@@ -33,7 +33,7 @@ STATUS_NAMES = {0: "LA_OK", -1: "LA_ERR_NULL", -2: "LA_ERR_DIM", -3: "LA_ERR_DTY
                 -4: "LA_ERR_FEATURE", -5: "LA_ERR_CUDA", -6: "LA_ERR_TIMEOUT",
                 -7: "LA_ERR_ALIGN"}
 EXPORTED = ("la_forward", "la_forward_ex", "la_forward_host", "la_step", "la_backward",
-            "la_prefix_attention", "la_prefix_step", "la_random_features",
+            "la_prefix_attention", "la_prefix_step", "la_random_features", "la_forward_rpe",
             "la_status_string",
             "la_check", "la_shutdown", "la_version", "la_launch_count",
             "la_forward_noncausal_noalloc", "la_selftest_timeout")
@@ -124,6 +124,8 @@ def load(path: str | None = None):
     lib.la_prefix_step.restype = i
     lib.la_random_features.argtypes = [i, i, i, ctypes.c_ulonglong, vp]
     lib.la_random_features.restype = i
+    lib.la_forward_rpe.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, fm, i, vp]
+    lib.la_forward_rpe.restype = i
     lib.la_status_string.argtypes = [i]
     lib.la_status_string.restype = ctypes.c_char_p
     lib.la_check.argtypes = [vp]
@@ -291,6 +293,25 @@ def la_backward(q, k, v, dout, causal=True, feature_map: FeatureMap | None = Non
                             _stream(stream))
     _raise(st)
     return dq, dk, dv
+
+
+def la_forward_rpe(q, k, v, bias, causal=True, feature_map: FeatureMap | None = None, out=None, stream=None):
+    """la_forward_rpe: kernelized attention with the Toeplitz weight exp(bias)
+    (bias: fp32 CUDA [H, 2N-1], index t + N - 1 for t = i - j)."""
+    B, H, N, D = q.shape
+    Dv = v.shape[-1]
+    if k.shape != q.shape or tuple(v.shape[:3]) != (B, H, N):
+        raise ValueError("shape mismatch between q, k, v")
+    if tuple(bias.shape) != (H, 2 * N - 1) or bias.dtype != torch.float32 or not bias.is_contiguous():
+        raise ValueError("bias must be a contiguous fp32 [H, 2N - 1] tensor")
+    if out is None:
+        out = torch.empty((B, H, N, Dv), dtype=q.dtype, device=q.device)
+    dt = _check_tensors(q, k, v, out)
+    _, fmp = _fm(feature_map)
+    st = load().la_forward_rpe(q.data_ptr(), k.data_ptr(), v.data_ptr(), bias.data_ptr(), out.data_ptr(),
+                               B, H, N, D, Dv, int(bool(causal)), fmp, dt, _stream(stream))
+    _raise(st)
+    return out
 
 
 def la_prefix_attention(q, k, v, out=None, state_out=None, return_state=False, stream=None):

@@ -75,6 +75,13 @@ cudaError_t prefix_empty_state(float *state, long long BH, int Dv, cudaStream_t 
 cudaError_t prefix_step(float *state, const void *q, const void *k, const void *v, void *out, long long BH,
                         int D, int Dv, int dtype, cudaStream_t s);
 
+// Kernelized attention with a Toeplitz relative-position weight exp(b_{i-j}),
+// b [H, 2N - 1] fp32 (device): the tensor-core kernel for bf16 elu+1 with D,
+// Dv in {64, 128} (rpe_tc_supported), else a CUDA-core kernel.
+bool rpe_tc_supported(const Problem &p);
+cudaError_t rpe_tc_forward(const Problem &p, const float *bias, int H, bool causal, int *err, cudaStream_t s);
+cudaError_t rpe_forward(const Problem &p, const float *bias, int H, bool causal, int *err, cudaStream_t s);
+
 // One recurrent decode step for BH heads, in place on S [BH, P, Dv], z [BH, P].
 cudaError_t step(float *S, float *z, const void *q, const void *k, const void *v, void *out,
                  long long BH, int D, int Dv, int P, int kind, int m, const float *W,

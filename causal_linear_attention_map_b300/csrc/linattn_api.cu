@@ -226,6 +226,38 @@ int prefix_impl(const void *q, const void *k, const void *v, void *out, float *s
     return cuda_status(e != cudaSuccess ? e : e2);
 }
 
+int rpe_impl(const void *q, const void *k, const void *v, const float *bias, void *out, int B, int H, int N, int D,
+             int Dv, int causal, const la_feature_map *fm, int dtype, void *stream)
+{
+    int kind, m, P;
+    const float *W;
+    int st = check_common(B, H, D, Dv, fm, dtype, &kind, &m, &W, &P);
+    if (st != LA_OK) return st;
+    if (N < 0) return LA_ERR_DIM;
+    const long long BH = (long long)B * H;
+    if (BH > 0x7fffffffLL || (long long)N * 2 > 0x7fffffffLL) return LA_ERR_DIM;
+    if (BH == 0 || N == 0) return LA_OK;
+    if (!q || !k || !v || !bias || !out) return LA_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(bias)) return LA_ERR_ALIGN;
+    la::Problem p;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.out = out;
+    p.BH = BH;
+    p.N = N;
+    p.D = D;
+    p.Dv = Dv;
+    p.P = P;
+    p.kind = kind;
+    p.m = m;
+    p.W = W;
+    p.dtype = dtype;
+    DeviceCtx *ctx = nullptr;
+    if ((st = get_ctx(&ctx)) != LA_OK) return st;
+    return cuda_status(la::rpe_forward(p, bias, H, causal != 0, ctx->err_word, (cudaStream_t)stream));
+}
+
 // la_forward_host: at most kHostGroups head groups, each with at least
 // kHostGroupBytes of inputs (a group's forward has a fixed cost of a few
 // launches, so small problems take few groups)
@@ -372,6 +404,12 @@ int la_prefix_step(float *state, const void *q, const void *k, const void *v, vo
     if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
         return LA_ERR_ALIGN;
     return cuda_status(la::prefix_step(state, q, k, v, out, BH, D, Dv, dtype, (cudaStream_t)stream));
+}
+
+int la_forward_rpe(const void *q, const void *k, const void *v, const float *bias, void *out, int B, int H, int N,
+                   int D, int Dv, int causal, const la_feature_map *fm, int dtype, void *stream)
+{
+    return rpe_impl(q, k, v, bias, out, B, H, N, D, Dv, causal, fm, dtype, stream);
 }
 
 int la_step(float *S, float *z, const void *q, const void *k, const void *v, void *out, int B,

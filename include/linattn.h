@@ -193,6 +193,26 @@ int la_backward(const void *q, const void *k, const void *v, const void *dout,
                 int causal, const la_feature_map *fm, int dtype, void *stream);
 
 /*
+ * la_forward_rpe -- kernelized attention with relative positional encoding
+ * (review page "Stable, Fast and Accurate: Kernelized Attention with
+ * Relative Positional Encoding", proposed method: the RPE matrix is Toeplitz
+ * - it depends only on i - j - and multiplies the kernelized attention):
+ *   out_i = sum_{j in J(i)} c_{i-j} (phi(q_i).phi(k_j)) v_j
+ *           / sum_{j in J(i)} c_{i-j} phi(q_i).phi(k_j),        c_t = exp(b_t)
+ * with J(i) = {0..i} when causal, else all positions.  bias: DEVICE fp32
+ * [H, 2N - 1], row h the log-weights b of head h (shared by every batch
+ * row), b_t at index t + N - 1 for t = i - j.  Other arguments, layouts and
+ * feature maps as la_forward.  The page multiplies by the Toeplitz matrix
+ * with FFTs; this library evaluates the weighted form chunk against chunk
+ * (O(N^2) work per head, on the tensor cores for bf16 elu+1 with D, Dv in
+ * {64, 128}, else on the CUDA cores): see the source for the cost
+ * comparison.  Allocates nothing; bounded waits report through la_check.
+ */
+int la_forward_rpe(const void *q, const void *k, const void *v, const float *bias, void *out,
+                   int B, int H, int N, int D, int Dv, int causal,
+                   const la_feature_map *fm, int dtype, void *stream);
+
+/*
  * la_prefix_attention -- softmax attention read as an RNN, with its
  * many-to-many outputs (review page "Attention as an RNN", proposed method:
  * attention is a many-to-one RNN over the keys and values with a learned

@@ -104,3 +104,16 @@ def test_reference_arm_times_whole_steps_of_the_tiny_workload(monkeypatch, capsy
     tokens = wl.TINY_F32.B * wl.TINY_F32.N
     assert abs(line["value"] * line["ms_per_step"] / 1e3 - tokens) < 1e-6 * tokens
     assert line["cpu_baseline"]["cores"] == 1   # one head: one thread has work
+
+
+def test_rpe_sample_bias_rows_match_the_head_and_offsets():
+    import numpy as np
+    import torch
+
+    w = wl.small(B=2, H=3, N=10, D=4, Dv=4)
+    b = torch.arange(3 * 19, dtype=torch.float32).reshape(3, 19)
+    got = bench.np64_bias(b, 4, 6, w)   # heads 0..3 -> rows 0, 1, 2, 0; offsets |t| < 6
+    assert got.shape == (4, 11)
+    assert np.array_equal(got[3], b[0, 4:15].double().numpy())
+    # offset 0 of the sample sits in its middle, as in the full row
+    assert got[1, 5] == b[1, 9]

@@ -14,7 +14,9 @@ N(0, 1) fp32 from its own seed.  Decode inputs for step t come from seed
 [B,H,N,Dv], is iid N(0, 1) from seed ``seed + DOUT_SEED_OFFSET``, cast to the
 workload dtype.  The query token of prefix attention, q [B,H,D], is iid
 N(0, 1) / sqrt(D) (unscaled for fp32 workloads) from seed
-``seed + PREFIX_Q_SEED_OFFSET``.
+``seed + PREFIX_Q_SEED_OFFSET``.  The relative-position log-weights of
+kernelized attention with RPE, b [H, 2N-1] fp32, are iid N(0, 0.5^2) from
+seed ``seed + RPE_SEED_OFFSET``.
 """
 from __future__ import annotations
 
@@ -72,6 +74,7 @@ DECODE_SEED = 4000
 W_SEED = 5000
 DOUT_SEED_OFFSET = 7000
 PREFIX_Q_SEED_OFFSET = 8000
+RPE_SEED_OFFSET = 9000
 
 TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
 
@@ -108,6 +111,12 @@ def make_prefix_q(w: Workload, device="cpu"):
     if w.scaled:
         x.mul_(1.0 / math.sqrt(w.D))
     return x.to(TORCH_DTYPE[w.dtype]).to(device).contiguous()
+
+
+def make_rpe_bias(w: Workload, device="cpu"):
+    """Relative-position log-weights b [H, 2N-1] fp32 (index t + N - 1)."""
+    gen = torch.Generator().manual_seed(w.seed + RPE_SEED_OFFSET)
+    return _randn((w.H, 2 * w.N - 1), gen).mul_(0.5).to(device).contiguous()
 
 
 def make_W(m: int, D: int, seed: int = W_SEED, device="cpu"):
