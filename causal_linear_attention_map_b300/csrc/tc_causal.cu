@@ -18,8 +18,9 @@
 // aggregate form (AGG = true: each item only sums phi(K)^T V and colsum
 // phi(K) over its segment, into scratch), a small scan turns those sums into
 // exclusive prefixes over segments, and the output form (AGG = false) starts
-// each segment's chunk recurrence from its prefix.  Items are handed out from
-// a global ticket counter.  (Chaining the segment states from CTA to CTA in
+// each segment's chunk recurrence from its prefix.  CTA b takes item b first;
+// further items (when there are more items than CTAs) come from a global
+// ticket counter.  (Chaining the segment states from CTA to CTA in
 // one pass was measured slower: under a full HBM load every link costs
 // several microseconds of global-memory round trips, and the chain advances
 // one segment per link.)
@@ -32,7 +33,8 @@
 //               each K tile's phi, then the segment's sums to scratch.)
 //   warps 8-11  phi warps, one per lane quadrant (one tile row per thread):
 //               phi(K) in place on the K tile in shared memory.
-//   warp 12     TMA producer of Q tiles and item scheduler.
+//   warp 12     TMA producer of Q tiles and item scheduler (in the
+//               aggregate form, which reads no Q, warp 13 hands out items).
 //   warp 13     TMA producer of K tiles.
 //   warp 14     TMA producer of V tiles (lane 0) and TMA store of the output
 //               tiles (lane 1).
@@ -398,8 +400,8 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
     if (warp == kProducerWarp || warp == kKWarp || warp == kVWarp) {
         // ---------------------------------------- Q / K / V tile producers
-        // The Q producer also hands out the items.  The segment-sum form
-        // streams a segment's K, V; the output form streams its Q, K, V (K
+        // The Q producer also hands out the items (the K producer in the
+        // segment-sum form).  The segment-sum form streams a segment's K, V; the output form streams its Q, K, V (K
         // and V a second time: the two passes are too far apart for L2 to
         // keep them).
         if (lane == 0) {
@@ -434,14 +436,21 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 n++;
                 return true;
             };
+            // Items: CTA b takes item b first, then tickets from the counter
+            // (offset by the grid size).  The role that hands them out is one
+            // whose loads pace it (Q here; K in the segment-sum form, which
+            // reads no Q), so that it takes its next ticket only once the
+            // current item's loads are all issued, never one an idle CTA
+            // would have taken.
+            const int item_role = AGG ? 1 : 0;
             for (int it = 0; ok; it++) {
                 const int slot = it & 1;
                 int item = -1;
-                if (role == 0) {
+                if (role == item_role) {
                     ok = it < 2 || wait_bar(&item_empty[slot], ((it >> 1) - 1) & 1, ctl);
                     // no new item once any CTA of this launch has given up a wait
                     if (ok && !*abort_cta && !*ctl.glob) {
-                        item = atomicAdd(sc.ticket, 1);
+                        item = it == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(sc.ticket, 1);
                         if (item >= g.n_items) item = -1;
                     }
                     item_slot[slot] = item;
@@ -1138,7 +1147,8 @@ nc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const bool ok = it < 2 || wait_bar(&item_empty[slot], ((it >> 1) - 1) & 1, ctl);
             int item = -1;
             if (ok && !*abort_cta && !*ctl.glob) {   // (not after another CTA gave up a wait)
-                item = atomicAdd(sc.ticket, 1);
+                // item b for CTA b first, then tickets offset by the grid size
+                item = it == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(sc.ticket, 1);
                 if (item >= g.n_items) item = -1;
             }
             item_slot[slot] = item;
