@@ -498,6 +498,14 @@ def oracle_timed(w: wl.Workload, call, budget_s: float, cost_factor: float, what
                       f"fp64 {what}, OpenMP over heads; median of {len(times)} calls, {dt:.3f} s each"}
 
 
+def backward_path(w: wl.Workload) -> str:
+    """Which kernels la_backward runs for workload ``w`` (the library's rule)."""
+    if w.dtype == "bf16" and w.feature == "elu1" and w.D == w.Dv and w.D in (64, 128):
+        return ("tensor cores (tcgen05 kind::f16): fp16 operands, dnum as an fp16 hi + lo pair, "
+                "per-chunk power-of-two scales, fp32 accumulation")
+    return "CUDA cores, fp32 arithmetic"
+
+
 def measure_backward(la, w: wl.Workload, args, dev, stream, ws, rank, with_cpu=True):
     """la_backward over workload ``w`` (inputs resident in HBM)."""
     q, k, v = wl.make_qkv(w)
@@ -519,7 +527,7 @@ def measure_backward(la, w: wl.Workload, args, dev, stream, ws, rank, with_cpu=T
              "roofline": hbm_roofline(alg_bytes_backward(w), alg_flops_backward(w), ms / 1e3,
                                       "la_backward (all of its launches, timed together)"),
              "l2": "L2 flushed between steps" if scrub is not None else "tensors larger than L2",
-             "path": "CUDA cores, fp32 arithmetic"}
+             "path": backward_path(w)}
     if clocks:
         entry["clocks"] = clocks
     if with_cpu and rank == 0 and ws == 1:

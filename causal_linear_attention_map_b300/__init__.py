@@ -31,7 +31,7 @@ LA_OK = 0
 LA_NOALLOC_SCRATCH_BYTES = 4 << 20   # the fixed scratch of la_forward_noncausal_noalloc
 STATUS_NAMES = {0: "LA_OK", -1: "LA_ERR_NULL", -2: "LA_ERR_DIM", -3: "LA_ERR_DTYPE",
                 -4: "LA_ERR_FEATURE", -5: "LA_ERR_CUDA", -6: "LA_ERR_TIMEOUT",
-                -7: "LA_ERR_ALIGN"}
+                -7: "LA_ERR_ALIGN", -8: "LA_ERR_RANGE"}
 EXPORTED = ("la_forward", "la_forward_ex", "la_forward_host", "la_step", "la_backward",
             "la_prefix_attention", "la_prefix_step", "la_random_features", "la_forward_rpe",
             "la_status_string",

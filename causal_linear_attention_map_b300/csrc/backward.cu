@@ -1,6 +1,7 @@
 // backward.cu -- gradients of the linear-attention forward with respect to
 // q, k and v, on CUDA cores (fp32 arithmetic), chunked and cut into segments
-// like the forward.
+// like the forward: every dtype and feature map (bf16 elu+1 with D = Dv in
+// {64, 128} goes to the tensor-core kernel of backward_tc.cu instead).
 //
 // Method (review page "Transformers are RNNs", proposed method b4: the
 // gradients of forward and backward propagation are computed in linear time
@@ -486,8 +487,18 @@ cudaError_t launch_backward(const Problem &p, const void *dout, void *dq, void *
 
 bool backward_supported(const Problem &p) { return (long long)p.P * p.Dv <= 16384; }
 
+cudaError_t backward_scan(float *st, long long BH, int nseg, int elems, int mode, cudaStream_t s)
+{
+    const dim3 sgrid((unsigned)cdiv(elems, kBT), (unsigned)BH);
+    bwd_scan_kernel<<<sgrid, kBT, 0, s>>>(st, nseg, elems, mode);
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) note_launches(1);
+    return e;
+}
+
 size_t backward_scratch_bytes(const Problem &p, bool causal)
 {
+    if (backward_tc_supported(p)) return backward_tc_scratch_bytes(p, causal);
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -497,8 +508,9 @@ size_t backward_scratch_bytes(const Problem &p, bool causal)
 }
 
 cudaError_t backward(const Problem &p, const void *dout, void *dq, void *dk, void *dv, bool causal,
-                     void *scratch, cudaStream_t s)
+                     void *scratch, int *err, cudaStream_t s)
 {
+    if (backward_tc_supported(p)) return backward_tc(p, dout, dq, dk, dv, causal, scratch, err, s);
     if (p.dtype == DT_F32) return launch_backward<float>(p, dout, dq, dk, dv, causal, scratch, s);
     return launch_backward<__nv_bfloat16>(p, dout, dq, dk, dv, causal, scratch, s);
 }

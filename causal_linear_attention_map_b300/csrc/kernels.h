@@ -56,13 +56,23 @@ cudaError_t noncausal(const Problem &p, void *scratch, float *S_out, float *z_ou
                       cudaStream_t s);
 
 // Gradients dq, dk, dv of sum(dout * out) for the forward of the same
-// arguments, on CUDA cores (fp32 arithmetic), any dtype and feature map with
-// Dphi * Dv <= 16384 (backward_supported).  Scratch (backward_scratch_bytes):
-// per-segment forward and reverse memories and per-position den, dden.
+// arguments, any dtype and feature map with Dphi * Dv <= 16384
+// (backward_supported): on the tensor cores for bf16 elu+1 with D = Dv in
+// {64, 128} (backward_tc_supported, fp16 operands; an operand outside fp16's
+// range sets the error word to 2), else on the CUDA cores (fp32 arithmetic).
+// Scratch (backward_scratch_bytes): per-segment forward and reverse memories
+// and per-position den, dden.
 bool backward_supported(const Problem &p);
 size_t backward_scratch_bytes(const Problem &p, bool causal);
 cudaError_t backward(const Problem &p, const void *dout, void *dq, void *dk, void *dv, bool causal,
-                     void *scratch, cudaStream_t s);
+                     void *scratch, int *err, cudaStream_t s);
+bool backward_tc_supported(const Problem &p);
+size_t backward_tc_scratch_bytes(const Problem &p, bool causal);
+cudaError_t backward_tc(const Problem &p, const void *dout, void *dq, void *dk, void *dv, bool causal,
+                        void *scratch, int *err, cudaStream_t s);
+// Exclusive prefix (mode 0), exclusive suffix (1) or total (2) over a head's
+// segments of the per-segment memories st [BH, nseg, elems], in place.
+cudaError_t backward_scan(float *st, long long BH, int nseg, int elems, int mode, cudaStream_t s);
 
 // Softmax attention of one query token per head over every prefix (the
 // many-to-many outputs of attention as an RNN), one pass with decoupled

@@ -194,7 +194,7 @@ int backward_impl(const void *q, const void *k, const void *v, const void *dout,
     void *scratch = nullptr;
     if (cudaMallocFromPoolAsync(&scratch, la::backward_scratch_bytes(p, causal != 0), ctx->pool, s) != cudaSuccess)
         return cuda_status(cudaErrorMemoryAllocation);
-    cudaError_t e = la::backward(p, dout, dq, dk, dv, causal != 0, scratch, s);
+    cudaError_t e = la::backward(p, dout, dq, dk, dv, causal != 0, scratch, ctx->err_word, s);
     cudaError_t e2 = cudaFreeAsync(scratch, s);
     return cuda_status(e != cudaSuccess ? e : e2);
 }
@@ -441,6 +441,7 @@ const char *la_status_string(int status)
     case LA_ERR_CUDA: return "LA_ERR_CUDA: a CUDA launch, allocation or query failed";
     case LA_ERR_TIMEOUT: return "LA_ERR_TIMEOUT: a bounded device-side wait ran out";
     case LA_ERR_ALIGN: return "LA_ERR_ALIGN: a tensor pointer is not 16-byte aligned";
+    case LA_ERR_RANGE: return "LA_ERR_RANGE: an operand of the tensor-core backward is outside fp16's range";
     default: return "unknown linattn status";
     }
 }
@@ -457,7 +458,7 @@ int la_check(void *stream)
     if (flag) {
         if (cudaMemset(ctx->err_word, 0, sizeof(int)) != cudaSuccess)
             return cuda_status(cudaErrorUnknown);
-        return LA_ERR_TIMEOUT;
+        return flag == 2 ? LA_ERR_RANGE : LA_ERR_TIMEOUT;
     }
     return LA_OK;
 }

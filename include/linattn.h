@@ -103,7 +103,9 @@ typedef enum {
     LA_ERR_FEATURE = -4, /* bad feature map (unknown kind, PRF without W, bad m) */
     LA_ERR_CUDA = -5,    /* a CUDA launch, allocation or query failed */
     LA_ERR_TIMEOUT = -6, /* a bounded device-side wait ran out (reported by la_check) */
-    LA_ERR_ALIGN = -7    /* a tensor pointer is not 16-byte aligned */
+    LA_ERR_ALIGN = -7,   /* a tensor pointer is not 16-byte aligned */
+    LA_ERR_RANGE = -8    /* the tensor-core backward met a value outside fp16's
+                            range (reported by la_check) */
 } la_status;
 
 /*
@@ -183,8 +185,14 @@ int la_step(float *S, float *z, const void *q, const void *k, const void *v,
  * q, k, dq, dk [B, H, N, D]; v, dout, dv [B, H, N, Dv]; all in `dtype`,
  * device, 16-byte aligned; dq, dk, dv are written, the rest read.  Same
  * feature maps, sizes and errors as la_forward, except that Dphi * Dv must
- * be at most 16384 (else LA_ERR_DIM).  Runs on the CUDA cores with fp32
- * arithmetic; takes stream-ordered scratch from the library's pool
+ * be at most 16384 (else LA_ERR_DIM).  bf16 elu+1 with D = Dv in {64, 128}
+ * runs on the tensor cores with fp16 operands (dnum as an fp16 hi + lo pair,
+ * per-chunk power-of-two scales; fp32 accumulation); a phi(q), phi(k) or v
+ * of magnitude >= 65520, scores phi(q).phi(k) or intra-chunk terms that
+ * overflow fp16 after those scales, or a denominator below 1e-30, make
+ * la_check report LA_ERR_RANGE (the results are then not to be used; the
+ * fp32 path takes such inputs).  Every other case runs on the CUDA cores with fp32
+ * arithmetic.  Takes stream-ordered scratch from the library's pool
  * (per-segment memories, and den, dden per position: 8 bytes per
  * position and head).  den and out are recomputed, not read.
  */
@@ -269,7 +277,8 @@ const char *la_status_string(int status);
 /*
  * la_check -- synchronise `stream` and report deferred device-side errors:
  * LA_ERR_TIMEOUT if a bounded wait inside a kernel of this library ran out
- * since the last la_check on this device (the flag is then cleared),
+ * since the last la_check on this device, LA_ERR_RANGE if the tensor-core
+ * backward met a value outside fp16's range (either flag is then cleared),
  * LA_ERR_CUDA if the stream reports an error, else LA_OK.
  */
 int la_check(void *stream);

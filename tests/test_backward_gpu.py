@@ -99,3 +99,54 @@ def test_backward_matches_finite_differences_of_the_gpu_forward(la):
             lm = (la.la_forward(*(a.float() for a in args_m.values()), causal=True) * do).double().sum()
             fd = float((lp - lm) / (2 * h))
             assert abs(fd - float(g[idx])) <= 2e-3 * max(1.0, abs(fd)), (name, idx, fd, float(g[idx]))
+
+
+# ---- the tensor-core path (bf16, elu+1, D = Dv in {64, 128}): fp16 operands,
+# dnum as an fp16 hi + lo pair, per-chunk power-of-two scales
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("N,D,B,H", [(2048 + 77, 64, 1, 2), (1000 + 17, 128, 2, 1), (128, 64, 1, 1),
+                                     (129, 128, 1, 1), (4096, 128, 1, 3)])
+def test_backward_tc_unscaled_inputs(la, causal, N, D, B, H):
+    """Unscaled N(0, 1) q, k, v (|x| up to ~4.5): phi up to ~5.5, several
+    segments per head; the same 2e-2 row-relative bar."""
+    w = wl.small(B=B, H=H, N=N, D=D, Dv=D, causal=causal, dtype="bf16", scaled=False, seed=N + D + 31)
+    _check(la, w)
+
+
+def test_backward_tc_large_but_in_range_values(la):
+    """One k entry of 2e4 and one v entry of -8e3 (phi and the memories well
+    beyond the usual scale, inside fp16's range after the power-of-two
+    scales): no flag, and the gradients still match."""
+    w = wl.small(B=1, H=2, N=700, D=64, Dv=64, causal=True, dtype="bf16", scaled=False, seed=77)
+    q, k, v = wl.make_qkv(w)
+    do = wl.make_dout(w)
+    q = (q.float() * 0.5).to(torch.bfloat16)
+    k = k.clone()
+    v = v.clone()
+    k[0, 1, 5, 3] = 20000.0
+    v[0, 0, 9, 7] = -8000.0
+    assert la.la_check() == 0
+    grads = la.la_backward(q.cuda(), k.cuda(), v.cuda(), do.cuda(), causal=True)
+    assert la.la_check() == 0
+    ref = oracle.backward(np64(q), np64(k), np64(v), np64(do), causal=True)
+    floor = 1e-4 * float(do.abs().max()) * float(v.abs().max())
+    for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
+        assert_grad_close(np64(g.cpu()), r, "bf16", what=name, floor=floor)
+
+
+def test_backward_tc_out_of_range_is_reported(la):
+    """A v entry beyond fp16's range (1e5) cannot take the fp16 tensor-core
+    path: la_check reports LA_ERR_RANGE once, then the flag is clear."""
+    w = wl.small(B=1, H=1, N=300, D=64, Dv=64, causal=True, dtype="bf16", seed=5)
+    q, k, v = wl.make_qkv(w)
+    do = wl.make_dout(w)
+    v = v.clone()
+    v[0, 0, 17, 2] = 1.0e5
+    assert la.la_check() == 0
+    la.la_backward(q.cuda(), k.cuda(), v.cuda(), do.cuda(), causal=True)
+    assert la.la_check() == {v_: k_ for k_, v_ in la.STATUS_NAMES.items()}["LA_ERR_RANGE"]
+    assert la.la_check() == 0
+    # the same inputs in fp32 take the CUDA-core path, which has no such limit
+    la.la_backward(q.float().cuda(), k.float().cuda(), v.float().cuda(), do.float().cuda(), causal=True)
+    assert la.la_check() == 0
