@@ -38,10 +38,11 @@
 //   2^-k on the carried memory tile ([S|z] or mu [R|r]) so that its largest
 //          entry stays below 2^14, and the same 2^-k on P and B, so that the
 //          products that share an accumulator carry the same factor.
-// Inputs whose phi or v exceed fp16's range (|x| >= 65520), whose scaled
-// scores or intra-chunk B do, or whose denominators underflow set the
-// library's error word (reported by la_check as LA_ERR_RANGE); they belong
-// on the fp32 CUDA-core backward.
+// Inputs with a q, k or v entry of magnitude >= 2^16 (whose phi or value has
+// no finite fp16) or not finite, whose scaled scores or intra-chunk B
+// overflow fp16, or whose denominators underflow set the library's error
+// word (reported by la_check as LA_ERR_RANGE); they belong on the fp32
+// CUDA-core backward.
 //
 // Tiles: Q, K, dout in 128-byte swizzle (64-column boxes), converted in
 // place (phi to fp16 for Q and K); V, M and the memories in 32-byte swizzle
@@ -85,7 +86,17 @@ struct BtcPlan {
     static constexpr int ZB = DD * E * 2;             // the carried memory tile, DD rows, same form
     static constexpr int G0 = 0, F0 = QB, O0 = 2 * QB, V0 = 3 * QB, M0 = V0 + VB, Z0 = M0 + MB;
     static constexpr int RED = Z0 + ZB;               // 2 x 128 floats (row-sum halves) + 8 (block reductions)
-    static constexpr int TILES = RED + 2048;
+    // Gradient rows are staged as bf16 (row stride RS, padded against bank
+    // conflicts) and copied out by the whole block in full rows.  At D = 128
+    // the memory tile's region serves for dq and dk (it is dead by then) and
+    // dv goes out directly; at D = 64 a region of its own serves all three.
+    static constexpr int RS = DD * 2 + 16;
+    static constexpr int STG = RED + 2048;
+    static constexpr int STGB = DD == 64 ? kBC * RS : 0;
+    static constexpr int TILES = STG + STGB;
+    static constexpr int STAGE_QK = DD == 64 ? STG : Z0;
+    static constexpr int STAGE_V = DD == 64 ? STG : -1;
+    static_assert(DD == 64 || kBC * RS <= ZB, "the memory tile's region holds a staged gradient chunk");
     static constexpr int RAW = TILES + 1024 + 1024;   // + alignment + barriers
     static constexpr int SMEM = RAW > 116 * 1024 ? RAW : 116 * 1024;   // one CTA per SM (all of TMEM)
     static constexpr int XW = E > 128 ? E : 128;
@@ -175,30 +186,43 @@ __device__ __forceinline__ void put_zside16(uint32_t tile, int bs, int r, int c0
     sts128(tile + b_soff(r, c0 + 8, bs), make_uint4(l, l, l, l));
 }
 
-// phi = elu + 1 of 8 bf16 -> 8 fp16 (fp32 arithmetic, one rounding)
-__device__ __forceinline__ uint4 phi_f16x8(uint4 x, bool &big)
+// The largest |x| seen, as packed bf16 magnitudes: a bf16 of magnitude >= 2^16
+// (bits >= 0x4780, the first above 65280) has no finite fp16, nor has
+// phi = x + 1 of it; every smaller bf16 and its phi fit.
+constexpr uint32_t kBf16TooBig = 0x4780u;
+__device__ __forceinline__ bool bf16_max_too_big(uint32_t amax)
+{
+    return (amax >> 16) >= kBf16TooBig || (amax & 0xffffu) >= kBf16TooBig;
+}
+
+// phi = elu + 1 = max(x, 0) + 2^(min(x, 0) log2 e) of 8 bf16 -> 8 fp16, in
+// half2 arithmetic (x is exact in fp16; x + 1 rounds once; the exponential
+// of a negative x is within a few fp16 ulps of it, and below 1 in size)
+__device__ __forceinline__ uint4 phi_f16x8(uint4 x, uint32_t &amax)
 {
     const uint32_t in[4] = {x.x, x.y, x.z, x.w};
+    const __half2 zero = __float2half2_rn(0.f), l2e = __float2half2_rn(1.4426950408889634f);
     uint32_t o[4];
 #pragma unroll
     for (int i = 0; i < 4; i++) {
+        amax = __vmaxu2(amax, in[i] & 0x7fff7fffu);
         const float2 t = unpack_bf16x2(in[i]);
-        const float a = phi_elu1_fast(t.x), b = phi_elu1_fast(t.y);
-        big = big || f16_overflows(a) || f16_overflows(b);
-        o[i] = pack_f16x2(a, b);
+        const __half2 hx = __floats2half2_rn(t.x, t.y);
+        const __half2 p = __hadd2(__hmax2(hx, zero), h2exp2(__hmul2(__hmin2(hx, zero), l2e)));
+        o[i] = *reinterpret_cast<const uint32_t *>(&p);
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // 8 bf16 -> 8 fp16
-__device__ __forceinline__ uint4 bf16_to_f16x8(uint4 x, bool &big)
+__device__ __forceinline__ uint4 bf16_to_f16x8(uint4 x, uint32_t &amax)
 {
     const uint32_t in[4] = {x.x, x.y, x.z, x.w};
     uint32_t o[4];
 #pragma unroll
     for (int i = 0; i < 4; i++) {
+        amax = __vmaxu2(amax, in[i] & 0x7fff7fffu);
         const float2 t = unpack_bf16x2(in[i]);
-        big = big || f16_overflows(t.x) || f16_overflows(t.y);
         o[i] = pack_f16x2(t.x, t.y);
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
@@ -413,37 +437,53 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 for (int b = 0; b < DD / 16; b++) tma_prefetch_3d(&tm_v, b * 16, nrow, h);
             }
         }
+        float dnv = 0.f, ddv = 0.f;  // this row's den and dden (dk/dv pass: read back from the dq pass)
+        if constexpr (PASS == 2) {   // (their loads in flight while the tiles are converted)
+            if (valid) {
+                dnv = den_g[(long long)h * g.N + row0 + r];
+                ddv = dd_g[(long long)h * g.N + row0 + r];
+            }
+        }
         ok = ok && wait_all(ld, ldph);
         if (!ok) break;
         ldph ^= 1;
         pending_ld = false;
         // ---- phi in place on this thread's half row of G and F (F rows past N become zero), as fp16;
-        //      V as fp16
+        //      V as fp16 (all loads of a tile issued before its math)
         {
             constexpr int JH = DD / 16;
-#pragma unroll 1
-            for (int j = 0; j < JH; j++) {
-                const uint32_t of = b_toff(r, hg * JH + j);
-                if (PASS != 0) sts128(G0 + of, phi_f16x8(lds128(G0 + of), big));
-                sts128(F0 + of, valid ? phi_f16x8(lds128(F0 + of), big) : make_uint4(0, 0, 0, 0));
+            uint32_t amax = 0u;
+            uint4 x[JH];
+            if constexpr (PASS != 0) {
+#pragma unroll
+                for (int j = 0; j < JH; j++) x[j] = lds128(G0 + b_toff(r, hg * JH + j));
+#pragma unroll
+                for (int j = 0; j < JH; j++) sts128(G0 + b_toff(r, hg * JH + j), phi_f16x8(x[j], amax));
             }
-#pragma unroll 1
-            for (int i = tid; i < kBC * DD / 8; i += kBThreads)   // the V boxes, 16 B at a time
-                sts128(V0 + 16 * i, bf16_to_f16x8(lds128(V0 + 16 * i), big));
+#pragma unroll
+            for (int j = 0; j < JH; j++) x[j] = lds128(F0 + b_toff(r, hg * JH + j));
+#pragma unroll
+            for (int j = 0; j < JH; j++) {
+                const uint4 f = phi_f16x8(x[j], amax);   // (rows past N are zero-filled: phi = 1, then dropped)
+                sts128(F0 + b_toff(r, hg * JH + j), valid ? f : make_uint4(0, 0, 0, 0));
+            }
+            constexpr int NV = kBC * DD / 8 / kBThreads;   // the V boxes, 16 B at a time
+            uint4 y[NV];
+#pragma unroll
+            for (int i = 0; i < NV; i++) y[i] = lds128(V0 + 16 * (tid + i * kBThreads));
+#pragma unroll
+            for (int i = 0; i < NV; i++) sts128(V0 + 16 * (tid + i * kBThreads), bf16_to_f16x8(y[i], amax));
+            big |= bf16_max_too_big(amax);
         }
         float mu = 1.f, zsc = 1.f;   // the chunk's M scale and memory-tile scale
-        float dnv = 0.f, ddv = 0.f;  // this row's den and dden (dk/dv pass: read back from the dq pass)
         if constexpr (PASS == 1) {
             zsc = memory_tile(1.f);
         }
         if constexpr (PASS == 2) {
-            if (valid) {
-                dnv = den_g[(long long)h * g.N + row0 + r];
-                ddv = dd_g[(long long)h * g.N + row0 + r];
-            }
             const float mind = -block_max(valid ? -dnv : -INFINITY);
-            big = big || (mind < 1e-30f);
+            big |= mind < 1e-30f;
             mu = mind < INFINITY && mind >= 1e-30f ? pow2_floor(mind) : 1.f;
+            const float fm = valid ? mu / dnv : 0.f;
             // mu M = [mu dout / den (hi; lo into the dout tile) | mu dden (hi | lo side block)]
             constexpr int JH = DD / 16;
             float f[HALF];
@@ -454,8 +494,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
                 for (int i = 0; i < 4; i++) {
                     const float2 t = unpack_bf16x2(u[i]);
-                    f[8 * j + 2 * i] = valid ? t.x * mu / dnv : 0.f;
-                    f[8 * j + 2 * i + 1] = valid ? t.y * mu / dnv : 0.f;
+                    f[8 * j + 2 * i] = t.x * fm;
+                    f[8 * j + 2 * i + 1] = t.y * fm;
                 }
             }
             __syncthreads();   // every row of dout read before its tile takes the lo parts
@@ -466,7 +506,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 for (int i = 0; i < 8; i++) {
                     hi[i] = f16_round(f[cb + i]);
                     lo[i] = f[cb + i] - hi[i];
-                    big = big || f16_overflows(f[cb + i]);
+                    big |= f16_overflows(f[cb + i]);
                 }
                 put8_f16(M0, MBS, r, hg * HALF + cb, hi);
                 put8_f16(ML0, MBS, r, hg * HALF + cb, lo);
@@ -510,7 +550,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 pk[i] = pack_f16x2(x0, x1);
                 pk[16 + i] = pack_f16x2(x2, x3);
             }
-            big = big || f16_overflows(mx);
+            big |= f16_overflows(mx);
             tmem_st32x2_nowait(tmem + lane_base + PL::T_P + hg * 32, pk);
             tmem_st_wait();
             publish();
@@ -555,15 +595,18 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 tmem_st_wait();
             }
         };
-        // fp32 TMEM rows of X times `f` -> the bf16 gradient rows (times min(phi, 1) of `phi_tile` when given)
-        auto store_grad = [&](__nv_bfloat16 *dst_base, float f, uint32_t phi_tile) {
+        // fp32 TMEM rows of X times `f` -> the bf16 gradient rows (times min(phi, 1) of `phi_tile` when
+        // given), staged in shared memory at byte offset `stage` and copied out in full rows (stage < 0:
+        // stored by each thread directly)
+        auto store_grad = [&](__nv_bfloat16 *dst_base, float f, uint32_t phi_tile, int stage) {
             constexpr int JH = DD / 16;
+            const uint32_t stg = base + (uint32_t)stage;
             uint32_t x[32];
 #pragma unroll
             for (int cb = 0; cb < HALF; cb += 32) {
                 tld32(tmem + lane_base + PL::T_X + hg * HALF + cb, x);
                 tmem_ld_wait();
-                if (valid) {
+                if (stage >= 0 || valid) {
                     uint4 *dst = reinterpret_cast<uint4 *>(dst_base + ((long long)h * g.N + row0 + r) * DD + hg * HALF + cb);
 #pragma unroll
                     for (int j = 0; j < 4; j++) {
@@ -586,8 +629,23 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         for (int i = 0; i < 4; i++)
                             o[i] = pack_bf16x2(__uint_as_float(x[8 * j + 2 * i]) * w[2 * i],
                                                __uint_as_float(x[8 * j + 2 * i + 1]) * w[2 * i + 1]);
-                        dst[j] = make_uint4(o[0], o[1], o[2], o[3]);
+                        if (stage >= 0)
+                            sts128(stg + r * PL::RS + (hg * HALF + cb + 8 * j) * 2, make_uint4(o[0], o[1], o[2], o[3]));
+                        else
+                            dst[j] = make_uint4(o[0], o[1], o[2], o[3]);
                     }
+                }
+            }
+            if (stage >= 0) {
+                __syncthreads();
+                constexpr int CPR = DD / 8;   // 16 B pieces per row
+                const int nrows = min(kBC, g.N - row0);
+#pragma unroll
+                for (int i = tid; i < kBC * CPR; i += kBThreads) {
+                    const int row = i / CPR, pc = i % CPR;
+                    if (row < nrows)
+                        *reinterpret_cast<uint4 *>(dst_base + ((long long)h * g.N + row0 + row) * DD + pc * 8) =
+                            lds128(stg + row * PL::RS + pc * 16);
                 }
             }
         };
@@ -636,8 +694,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 for (int cb = 0; cb < HALF; cb += 32) {
                     tld32(tmem + lane_base + PL::T_X + hg * HALF + cb, n0);
                     tmem_ld_wait();
-                    den = (__uint_as_float(d[0]) + __uint_as_float(d[8])) / zsc;
-                    const float inv_n = 1.f / (zsc * den);   // NUM = X / zsc; out = NUM / den
+                    const float xden = __uint_as_float(d[0]) + __uint_as_float(d[8]);   // zsc den
+                    den = xden * (1.f / zsc);
+                    const float inv_n = 1.f / xden;   // NUM = X / zsc; out = NUM / den = X / (zsc den)
+                    const float rden = valid ? 1.f / den : 0.f;
 #pragma unroll
                     for (int j = 0; j < 4; j++) {
                         const uint4 x = lds128(O0 + b_toff(r, (hg * HALF + cb) / 8 + j));
@@ -648,8 +708,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                             const int k2 = 8 * j + 2 * i;
                             part = fmaf(t.x, __uint_as_float(n0[k2]) * inv_n, part);
                             part = fmaf(t.y, __uint_as_float(n0[k2 + 1]) * inv_n, part);
-                            dn[cb + k2] = valid ? t.x / den : 0.f;
-                            dn[cb + k2 + 1] = valid ? t.y / den : 0.f;
+                            dn[cb + k2] = t.x * rden;
+                            dn[cb + k2 + 1] = t.y * rden;
                         }
                     }
                 }
@@ -657,7 +717,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 __syncthreads();   // (also: every row of dout has been read)
                 const float dd = valid ? -(red[r] + red[kBC + r]) / den : 0.f;
                 const float mind = -block_max(valid ? -den : -INFINITY);
-                big = big || (mind < 1e-30f);
+                big |= mind < 1e-30f;
                 mu = mind < INFINITY && mind >= 1e-30f ? pow2_floor(mind) : 1.f;
 #pragma unroll
                 for (int cb = 0; cb < HALF; cb += 8) {
@@ -667,7 +727,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         const float f = dn[cb + i] * mu;
                         hi[i] = f16_round(f);
                         lo[i] = f - hi[i];
-                        big = big || f16_overflows(f);
+                        big |= f16_overflows(f);
                     }
                     put8_f16(M0, MBS, r, hg * HALF + cb, hi);
                     put8_f16(ML0, MBS, r, hg * HALF + cb, lo);
@@ -718,7 +778,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                                 id_s, 1u);
             }
             finish_mma();
-            store_grad(grad_a, 1.f / (zsc * mu), G0);
+            store_grad(grad_a, 1.f / (zsc * mu), G0, PL::STAGE_QK);
             tc_fence_before();
             __syncthreads();   // X has been read
             // updates: S|z += F^T [V|1] (causal) into T_SZ; X = mu G^T M (-> R|r)
@@ -775,7 +835,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 }
             }
             finish_mma();
-            store_grad(grad_b, 1.f / (zsc * mu), 0u);
+            store_grad(grad_b, 1.f / (zsc * mu), 0u, PL::STAGE_V);
             tc_fence_before();
             __syncthreads();   // (X is read before the next product overwrites it)
             // (3) X = Vx (mu M)^T -> zsc mu B^T (i >= j)
@@ -811,7 +871,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                                 id_r, (causal || kb > 0) ? 1u : 0u);
             }
             finish_mma();
-            store_grad(grad_a, 1.f / (zsc * mu), F0);
+            store_grad(grad_a, 1.f / (zsc * mu), F0, PL::STAGE_QK);
             tc_fence_before();
             __syncthreads();   // X has been read
             // R|r += G^T M (causal)

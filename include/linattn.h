@@ -187,9 +187,9 @@ int la_step(float *S, float *z, const void *q, const void *k, const void *v,
  * feature maps, sizes and errors as la_forward, except that Dphi * Dv must
  * be at most 16384 (else LA_ERR_DIM).  bf16 elu+1 with D = Dv in {64, 128}
  * runs on the tensor cores with fp16 operands (dnum as an fp16 hi + lo pair,
- * per-chunk power-of-two scales; fp32 accumulation); a phi(q), phi(k) or v
- * of magnitude >= 65520, scores phi(q).phi(k) or intra-chunk terms that
- * overflow fp16 after those scales, or a denominator below 1e-30, make
+ * per-chunk power-of-two scales; fp32 accumulation); a q, k or v entry of
+ * magnitude >= 2^16 or not finite, scores phi(q).phi(k) or intra-chunk terms
+ * that overflow fp16 after those scales, or a denominator below 1e-30, make
  * la_check report LA_ERR_RANGE (the results are then not to be used; the
  * fp32 path takes such inputs).  Every other case runs on the CUDA cores with fp32
  * arithmetic.  Takes stream-ordered scratch from the library's pool
