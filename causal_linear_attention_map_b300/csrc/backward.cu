@@ -231,16 +231,26 @@ __global__ void bwd_scan_kernel(float *__restrict__ st, int nseg, int elems, int
     float *p = st + h * nseg * (long long)elems + e;
     if (mode == 2) {
         float t = 0.f;
+#pragma unroll 8
         for (int s = 0; s < nseg; s++) t += p[(long long)s * elems];
         for (int s = 0; s < nseg; s++) p[(long long)s * elems] = t;
         return;
     }
+    // eight segments' loads in flight at a time, then their stores
     float run = 0.f;
-    for (int i = 0; i < nseg; i++) {
-        const int s = mode == 0 ? i : nseg - 1 - i;
-        const float x = p[(long long)s * elems];
-        p[(long long)s * elems] = run;
-        run += x;
+    for (int i0 = 0; i0 < nseg; i0 += 8) {
+        float x[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            const int i = i0 + j, s = mode == 0 ? i : nseg - 1 - i;
+            x[j] = i < nseg ? p[(long long)s * elems] : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            const int i = i0 + j, s = mode == 0 ? i : nseg - 1 - i;
+            if (i < nseg) p[(long long)s * elems] = run;
+            run += x[j];
+        }
     }
 }
 

@@ -177,6 +177,13 @@ struct Scratch {
     float *den_part; // [BH, N]
     int pre_rows;    // feature rows per prefix slot (split feature maps: both halves' rows,
     int pre_off;     // this pass's from row pre_off); else DP and 0
+    // Non-causal readout: nsum > 0 means preS / prez hold nsum per-segment sums
+    // per head ([BH, nsum, DP, DV], [BH, nsum, DP]) that the readout adds up
+    // itself (the CTAs of segment 0 also write the totals to exS / exz when
+    // given); nsum = 0 means they hold the totals ([BH, DP, DV], [BH, DP]).
+    int nsum;
+    float *exS;
+    float *exz;
 };
 
 // What the kernel applies to the Q and K tiles and how it finishes a chunk.
@@ -1282,23 +1289,47 @@ nc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const int c0 = s * g.L, nc = min(g.L, g.NC - c0);
             // S (bf16) and ZP for this head, once the last item's products are done
             if (ni > 0) wait_bar(s_free, (ni - 1) & 1, ctl);
-            griddep_wait();   // the totals kernel (this grid's prerequisite) has completed
-            for (int row = r; row < DP; row += kC) {   // the head's totals (sc.preS, sc.prez: [BH, DP, DV], [BH, DP])
-                const float *src = sc.preS + (long long)h * DP * DV + (long long)row * DV + grp * HALF;
+            griddep_wait();   // the totals kernel (or the segment-sum pass) has completed
+            // the head's totals: read (nsum = 0), or added up from its segments' sums
+            const int nsl = sc.nsum > 0 ? sc.nsum : 1;
+            const bool exp_tot = sc.nsum > 0 && s == 0;   // this CTA exports the totals
+            for (int row = r; row < DP; row += kC) {
+                const float *src = sc.preS + (long long)h * nsl * DP * DV + (long long)row * DV + grp * HALF;
 #pragma unroll
                 for (int cb = 0; cb < HALF; cb += 32) {
+                    float4 acc[8];
+#pragma unroll
+                    for (int i = 0; i < 8; i++) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int t = 0; t < nsl; t++)
+#pragma unroll
+                        for (int i = 0; i < 8; i++) {
+                            const float4 x = __ldcg(reinterpret_cast<const float4 *>(src + (long long)t * DP * DV + cb) + i);
+                            acc[i].x += x.x;
+                            acc[i].y += x.y;
+                            acc[i].z += x.z;
+                            acc[i].w += x.w;
+                        }
                     uint32_t v[32];
 #pragma unroll
-                    for (int i = 0; i < 32; i += 4) {
-                        const float4 x = __ldcg(reinterpret_cast<const float4 *>(src + cb + i));
-                        v[i] = __float_as_uint(x.x);
-                        v[i + 1] = __float_as_uint(x.y);
-                        v[i + 2] = __float_as_uint(x.z);
-                        v[i + 3] = __float_as_uint(x.w);
+                    for (int i = 0; i < 8; i++) {
+                        v[4 * i] = __float_as_uint(acc[i].x);
+                        v[4 * i + 1] = __float_as_uint(acc[i].y);
+                        v[4 * i + 2] = __float_as_uint(acc[i].z);
+                        v[4 * i + 3] = __float_as_uint(acc[i].w);
+                    }
+                    if (exp_tot && sc.exS) {
+                        float4 *dst = reinterpret_cast<float4 *>(sc.exS + ((long long)h * DP + row) * DV + grp * HALF + cb);
+#pragma unroll
+                        for (int i = 0; i < 8; i++) dst[i] = acc[i];
                     }
                     sprev_store32_sw32<DP>(s_addr, row, grp * HALF + cb, v);
                 }
-                if (grp == 0) zp_store(z_addr, row, __ldcg(sc.prez + (long long)h * DP + row));
+                if (grp == 0) {
+                    float zt = 0.f;
+                    for (int t = 0; t < nsl; t++) zt += __ldcg(sc.prez + ((long long)h * nsl + t) * DP + row);
+                    if (exp_tot && sc.exz) sc.exz[(long long)h * DP + row] = zt;
+                    zp_store(z_addr, row, zt);
+                }
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -1777,6 +1808,9 @@ Scratch carve(void *scratch, const Geo &g)
     sc.den_part = nullptr;
     sc.pre_rows = DP;
     sc.pre_off = 0;
+    sc.nsum = 0;
+    sc.exS = nullptr;
+    sc.exz = nullptr;
     return sc;
 }
 
@@ -1841,7 +1875,7 @@ cudaError_t run_causal(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
 template <int DP, int DV, int AMODE>
 cudaError_t run_totals(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv_agg, const CUtensorMap &to,
                        Geo g, void *scratch, float *totS, float *totz, int tot_rows, int row_off, int *err,
-                       cudaStream_t s)
+                       cudaStream_t s, bool with_totals = true)
 {
     using PL = Plan<DP, DV>;
     const int sms = num_sms();
@@ -1852,6 +1886,10 @@ cudaError_t run_totals(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
     tc_causal_kernel<DP, DV, true, AMODE><<<min(g.n_items, sms), kThreads, PL::SMEM, s>>>(
         tq, tk, tv_agg, to, g, sc, nullptr, nullptr, nullptr, err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (!with_totals) {   // the readout adds the segment sums up itself
+        note_launches(1);
+        return cudaSuccess;
+    }
     const int sz = DP * DV + DP;
     if ((e = launch_dependent(nc_total_kernel, dim3(cdiv(sz, 256), (unsigned)g.BH), dim3(256), 0, s,
                               (const float *)sc.preS, (const float *)sc.prez, g.nseg, DP * DV, DP, totS, totz,
@@ -1864,12 +1902,18 @@ cudaError_t run_totals(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
 // Non-causal, second half: out = phi(Q) S / phi(Q) z from the totals.
 template <int DP, int DV, bool PHI>
 cudaError_t run_readout(const CUtensorMap &tq, const CUtensorMap &to, Geo g, void *scratch, float *totS,
-                        float *totz, int *err, cudaStream_t s)
+                        float *totz, int *err, cudaStream_t s, float *S_out = nullptr, float *z_out = nullptr)
 {
     using NP = NcPlan<DP, DV>;
     Scratch sc = carve<DP, DV>(scratch, g);
-    sc.preS = totS;
-    sc.prez = totz;
+    if (totS) {   // the totals kernel's output
+        sc.preS = totS;
+        sc.prez = totz;
+    } else {      // the segment sums of the segment-sum pass, added up by the readout (which exports them)
+        sc.nsum = g.nseg;
+        sc.exS = S_out;
+        sc.exz = z_out;
+    }
     sc.ticket = (int *)((unsigned char *)scratch + 8);   // cleared with the header by run_totals
     cudaError_t e;
     if ((e = set_max_smem_once<nc_out_kernel<DP, DV, PHI>>(NP::SMEM)) != cudaSuccess)
@@ -1881,6 +1925,11 @@ cudaError_t run_readout(const CUtensorMap &tq, const CUtensorMap &to, Geo g, voi
     note_launches(1);
     return cudaSuccess;
 }
+
+// Non-causal elu+1: with at most this many segments per head the readout reads
+// and adds the segment sums itself (a few tens of KB per CTA from L2) instead
+// of waiting for a totals kernel.
+constexpr int kNcFoldSegs = 4;
 
 cudaError_t export_totals(float *S_out, float *z_out, const float *totS, const float *totz, long long BH, int P,
                           int Dv, cudaStream_t s)
@@ -1911,6 +1960,12 @@ cudaError_t run_elu(const Problem &p, void *scratch, float *S_out, float *z_out,
                                            z_out, err, s);
     float *totS = (float *)((unsigned char *)scratch + seg_scratch_bytes<DP, DV>(g, true));
     float *totz = totS + (size_t)g.BH * DP * DV;
+    if (g.nseg <= kNcFoldSegs) {
+        // few segments per head: the readout adds them up (no totals kernel)
+        cudaError_t e = run_totals<DP, DV, kModeElu>(tq, tk, tva, to, g, scratch, totS, totz, DP, 0, err, s, false);
+        if (e == cudaSuccess) e = run_readout<DP, DV, true>(tq, to, g, scratch, nullptr, nullptr, err, s, S_out, z_out);
+        return e;
+    }
     cudaError_t e = run_totals<DP, DV, kModeElu>(tq, tk, tva, to, g, scratch, totS, totz, DP, 0, err, s);
     if (e == cudaSuccess) e = run_readout<DP, DV, true>(tq, to, g, scratch, totS, totz, err, s);
     if (e == cudaSuccess) e = export_totals(S_out, z_out, totS, totz, g.BH, DP, DV, s);

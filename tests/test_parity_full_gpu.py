@@ -162,15 +162,24 @@ def test_prf_launch_plan(la):
 
 def test_noncausal_launch_plan(la):
     """Non-causal bf16 elu+1 with D, Dv in {64, 128}: the segment-sum pass, the
-    per-head total and the readout (three kernels); other shapes: the
-    CUDA-core reduction and readout."""
-    for (H, D, expect) in ((2, 128, 3), (160, 64, 3)):
+    per-head total and the readout (three kernels); with at most four
+    segments per head the readout adds the segment sums itself (two)."""
+    for (H, D, expect) in ((2, 128, 3), (160, 64, 2), (40, 64, 2)):
         w = wl.small(B=1, H=H, N=1024, D=D, Dv=D, causal=False, seed=6)
         q, k, v = (t.cuda() for t in wl.make_qkv(w))
         n0 = la.la_launch_count()
         la.la_forward(q, k, v, causal=False)
         torch.cuda.synchronize()
         assert la.la_launch_count() - n0 == expect, (H, D)
+
+
+@pytest.mark.parametrize("H,N,D", [(40, 128 * 9 + 3, 64), (37, 128 * 4 + 100, 128), (160, 300, 64)])
+def test_noncausal_readout_adds_segment_sums(la, H, N, D):
+    """Non-causal with one to four segments per head: the readout adds the
+    segment sums itself and exports the totals (every head, both memories)."""
+    w = wl.small(B=1, H=H, N=N, D=D, Dv=D, causal=False, seed=N + H + 3)
+    err, _ = _forward_and_check(la, w)
+    assert err <= 2e-2
 
 
 @pytest.mark.parametrize("causal", [True, False])
