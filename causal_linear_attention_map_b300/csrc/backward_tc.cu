@@ -51,7 +51,9 @@
 // hi | lo pairs (columns 0, 1 and 8, 9) after R and dnum.  The lo part of
 // dnum takes the dout tile's place once M is formed.  The stages of a chunk
 // run one after another (one thread issues, every thread waits on the
-// commit); the next chunk's tiles are prefetched into L2 meanwhile.
+// commit).  The next chunk's F and V tiles are loaded as soon as the chunk's
+// products no longer read them, its G and dout tiles after the last product,
+// and the chunk after it is prefetched into L2.
 //
 // Launches: the forward memories' segment sums (this file's kernel in its
 // sums-only form), their exclusive prefix, the dq pass (which writes den,
@@ -244,7 +246,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const uint32_t base = b_align1k(smem_u32(smem_raw));
     unsigned char *gbase = smem_raw + (base - smem_u32(smem_raw));
     uint64_t *bar = reinterpret_cast<uint64_t *>(gbase + PL::TILES);
-    uint64_t *ld = bar, *mb = bar + 1;
+    uint64_t *ld = bar, *mb = bar + 1, *ldb = bar + 4;   // ld: G, dout tiles; ldb: F, V tiles
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 2);
     volatile int *abort_cta = reinterpret_cast<volatile int *>(bar + 3);
     float *red = reinterpret_cast<float *>(gbase + PL::RED);
@@ -262,6 +264,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
     if (tid == 0) {
         mbar_init(ld, 1);
+        mbar_init(ldb, 1);
         mbar_init(mb, 1);
         *abort_cta = 0;
         fence_mbar_init();
@@ -280,9 +283,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
-    bool ok = true, pending_ld = false;   // pending_ld: thread 0 issued tile loads not yet waited for
+    bool ok = true, pend_a = false, pend_b = false;   // thread 0 issued tile loads not yet waited for
     bool big = false;                     // this thread saw a value outside fp16's range
-    uint32_t ldph = 0, mbph = 0;
+    uint32_t ldph = 0, ldbph = 0, mbph = 0;
     // bounded wait by every thread, made block-uniform
     auto wait_all = [&](uint64_t *b, uint32_t parity) {
         bool w = !*abort_cta;
@@ -410,32 +413,44 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
     const int cfirst = PASS == 2 ? c1 - 1 : c0, cstep = PASS == 2 ? -1 : 1;
     const int nchunks = c1 - c0;
+    // tile loads (thread 0): G and dout of chunk cc on `ld`; F and V on `ldb`, with the
+    // tiles of the chunk after it (the cidx + 1-th of the segment) prefetched into L2
+    auto issue_a = [&](int cc) {
+        if constexpr (PASS != 0) {
+            mbar_arrive_expect_tx(ld, 2 * PL::QB);
+            pend_a = true;
+            for (int b = 0; b < DD / 64; b++) {
+                tma_load_3d(gbase + PL::G0 + b * (kBC * 128), &tm_q, ld, b * 64, cc * kBC, h);
+                tma_load_3d(gbase + PL::O0 + b * (kBC * 128), &tm_o, ld, b * 64, cc * kBC, h);
+            }
+        }
+    };
+    auto issue_b = [&](int cc, int cidx) {
+        mbar_arrive_expect_tx(ldb, PL::QB + kBC * DD * 2);
+        pend_b = true;
+        for (int b = 0; b < DD / 64; b++)
+            tma_load_3d(gbase + PL::F0 + b * (kBC * 128), &tm_k, ldb, b * 64, cc * kBC, h);
+        for (int b = 0; b < DD / 16; b++)
+            tma_load_3d(gbase + PL::V0 + b * MBS, &tm_v, ldb, b * 16, cc * kBC, h);
+        if (cidx + 1 < nchunks) {
+            const int nrow = (cc + cstep) * kBC;
+            for (int b = 0; b < DD / 64; b++) {
+                if (PASS != 0) tma_prefetch_3d(&tm_q, b * 64, nrow, h);
+                tma_prefetch_3d(&tm_k, b * 64, nrow, h);
+                if (PASS != 0) tma_prefetch_3d(&tm_o, b * 64, nrow, h);
+            }
+            for (int b = 0; b < DD / 16; b++) tma_prefetch_3d(&tm_v, b * 16, nrow, h);
+        }
+    };
     for (int ci = 0; ci < nchunks && ok; ci++) {
         const int c = cfirst + ci * cstep;
         const int row0 = c * kBC;
         const bool valid = row0 + r < g.N;
-        // ---- tiles: G (q), F (k), V, dout; the next chunk's into L2
-        if (tid == 0) {
-            const bool need_q = PASS != 0, need_o = PASS != 0;
-            const uint32_t bytes = PL::QB + kBC * DD * 2 + (need_q ? PL::QB : 0) + (need_o ? PL::QB : 0);
-            mbar_arrive_expect_tx(ld, bytes);
-            pending_ld = true;
-            for (int b = 0; b < DD / 64; b++) {
-                if (need_q) tma_load_3d(gbase + PL::G0 + b * (kBC * 128), &tm_q, ld, b * 64, row0, h);
-                tma_load_3d(gbase + PL::F0 + b * (kBC * 128), &tm_k, ld, b * 64, row0, h);
-                if (need_o) tma_load_3d(gbase + PL::O0 + b * (kBC * 128), &tm_o, ld, b * 64, row0, h);
-            }
-            for (int b = 0; b < DD / 16; b++)
-                tma_load_3d(gbase + PL::V0 + b * MBS, &tm_v, ld, b * 16, row0, h);
-            if (ci + 1 < nchunks) {
-                const int nrow = (c + cstep) * kBC;
-                for (int b = 0; b < DD / 64; b++) {
-                    if (need_q) tma_prefetch_3d(&tm_q, b * 64, nrow, h);
-                    tma_prefetch_3d(&tm_k, b * 64, nrow, h);
-                    if (need_o) tma_prefetch_3d(&tm_o, b * 64, nrow, h);
-                }
-                for (int b = 0; b < DD / 16; b++) tma_prefetch_3d(&tm_v, b * 16, nrow, h);
-            }
+        // ---- tiles: the first chunk's here; a later chunk's F, V (and G, dout) are
+        //      issued by the previous chunk as soon as its products no longer read them
+        if (ci == 0 && tid == 0) {
+            issue_a(c);
+            issue_b(c, ci);
         }
         float dnv = 0.f, ddv = 0.f;  // this row's den and dden (dk/dv pass: read back from the dq pass)
         if constexpr (PASS == 2) {   // (their loads in flight while the tiles are converted)
@@ -444,10 +459,15 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 ddv = dd_g[(long long)h * g.N + row0 + r];
             }
         }
-        ok = ok && wait_all(ld, ldph);
+        ok = ok && wait_all(ldb, ldbph);
+        ldbph ^= 1;
+        pend_b = false;
+        if constexpr (PASS != 0) {
+            ok = ok && wait_all(ld, ldph);
+            ldph ^= 1;
+            pend_a = false;
+        }
         if (!ok) break;
-        ldph ^= 1;
-        pending_ld = false;
         // ---- phi in place on this thread's half row of G and F (F rows past N become zero), as fp16;
         //      V as fp16 (all loads of a tile issued before its math)
         {
@@ -528,6 +548,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                                 sw32_desc(V0 + (kk / 8) * 256, MBS, 256), id, 1u);
             }
             finish_mma();
+            if (tid == 0 && ok && ci + 1 < nchunks) issue_b(c + cstep, ci + 1);
             continue;
         }
 
@@ -651,7 +672,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         };
 
         if constexpr (PASS == 1) {
-            // (1) X = G F^T -> P
+            // (1) X = G F^T -> P; and S|z += F^T [V|1] for the next chunk (the memory
+            //     tile of this chunk is made), so that F and V are free after (4)
             if (causal) {
                 if (tid == 0 && ok) {
                     tc_fence_after();
@@ -662,6 +684,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         mma_bf16_ss(tmem + PL::T_X, sw128_desc(G0 + off, 16, 1024), sw128_desc(F0 + off, 16, 1024), id,
                                     kk > 0 ? 1u : 0u);
                     }
+                    constexpr uint32_t id_s = idesc_f16(128, E, 1, 1);
+#pragma unroll
+                    for (int kk = 0; kk < kBC; kk += 16)
+                        mma_bf16_ss(tmem + PL::T_SZ, sw128_desc(F0 + (kk / 8) * 1024, lboT, 1024),
+                                    sw32_desc(V0 + (kk / 8) * 256, MBS, 256), id_s, 1u);
                 }
                 finish_mma();
                 tril_to_p(false);
@@ -778,22 +805,17 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                                 id_s, 1u);
             }
             finish_mma();
+            if (tid == 0 && ok && ci + 1 < nchunks) issue_b(c + cstep, ci + 1);   // F and V are free
             store_grad(grad_a, 1.f / (zsc * mu), G0, PL::STAGE_QK);
             tc_fence_before();
             __syncthreads();   // X has been read
-            // updates: S|z += F^T [V|1] (causal) into T_SZ; X = mu G^T M (-> R|r)
+            // X = mu G^T M (-> R|r)
             if (tid == 0 && ok) {
                 tc_fence_after();
-                if (causal) {
-                    constexpr uint32_t id = idesc_f16(128, E, 1, 1);
-#pragma unroll
-                    for (int kk = 0; kk < kBC; kk += 16)
-                        mma_bf16_ss(tmem + PL::T_SZ, sw128_desc(F0 + (kk / 8) * 1024, lboT, 1024),
-                                    sw32_desc(V0 + (kk / 8) * 256, MBS, 256), id, 1u);
-                }
                 issue_r_update(true);
             }
             finish_mma();
+            if (tid == 0 && ok && ci + 1 < nchunks) issue_a(c + cstep);   // G and dout are free
             add_r_update();
         }
 
@@ -873,7 +895,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             finish_mma();
             store_grad(grad_a, 1.f / (zsc * mu), F0, PL::STAGE_QK);
             tc_fence_before();
-            __syncthreads();   // X has been read
+            __syncthreads();   // X and F have been read
+            if (tid == 0 && ok && ci + 1 < nchunks) issue_b(c + cstep, ci + 1);   // F and V are free
             // R|r += G^T M (causal)
             if (causal) {
                 if (tid == 0 && ok) {
@@ -881,8 +904,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     issue_r_update(true);
                 }
                 finish_mma();
-                add_r_update();
             }
+            if (tid == 0 && ok && ci + 1 < nchunks) issue_a(c + cstep);   // G and dout are free
+            if (causal) add_r_update();
         }
         publish();
     }
@@ -917,7 +941,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     if (tid == 0) {
         mma_commit(mb);
         mbar_wait(mb, mbph, nullptr, 0, kBBudget);
-        if (pending_ld) mbar_wait(ld, ldph, nullptr, 0, kBBudget);
+        if (pend_a) mbar_wait(ld, ldph, nullptr, 0, kBBudget);
+        if (pend_b) mbar_wait(ldb, ldbph, nullptr, 0, kBBudget);
     }
     tc_fence_before();
     __syncthreads();
