@@ -27,9 +27,10 @@
 // the small part x.  bf16 operands (8 significant bits) lose it: a model of
 // this chunk algebra with bf16 operands and exact sums missed the fp64
 // oracle by 2-42% row-relative on dq.  Here the operands are fp16 (11
-// significant bits) and M, whose rounding matters most, is carried as an
-// fp16 hi + lo pair (every product with M is issued for both parts); the
-// same model then stays within 7e-3 on dq, dk and dv (N up to 16384,
+// significant bits) and M, whose rounding matters most for dq, is carried as
+// an fp16 hi + lo pair in the products of the dq pass that give dG (the R
+// updates and the dk/dv pass use its hi part alone); the same model then
+// stays within 6.7e-3 on dq, 6.4e-3 on dk and 7e-4 on dv (N up to 16384,
 // scaled and unscaled inputs, causal and not).  fp16's range is handled by
 // exact powers of two, chosen per chunk:
 //   mu   = 2^floor(log2(min den of the chunk's rows)): M is stored as mu M
@@ -48,8 +49,8 @@
 // place (phi to fp16 for Q and K); V, M and the memories in 32-byte swizzle
 // blocks of 16 columns followed by a 16-column side block: ONES after V
 // (columns 0-7 one), z hi | lo after S (columns 0-7 | 8-15), r and dden as
-// hi | lo pairs (columns 0, 1 and 8, 9) after R and dnum.  The lo part of
-// dnum takes the dout tile's place once M is formed.  The stages of a chunk
+// hi | lo pairs (columns 0, 1 and 8, 9) after R and dnum.  In the dq pass
+// the lo part of dnum takes the dout tile's place once M is formed.  The stages of a chunk
 // run one after another (one thread issues, every thread waits on the
 // commit).  The next chunk's F and V tiles are loaded as soon as the chunk's
 // products no longer read them, its G and dout tiles after the last product,
@@ -518,18 +519,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     f[8 * j + 2 * i + 1] = t.y * fm;
                 }
             }
-            __syncthreads();   // every row of dout read before its tile takes the lo parts
+            // (a single fp16 part here: the dk/dv pass is not sensitive to it)
 #pragma unroll
             for (int cb = 0; cb < HALF; cb += 8) {
-                float hi[8], lo[8];
 #pragma unroll
-                for (int i = 0; i < 8; i++) {
-                    hi[i] = f16_round(f[cb + i]);
-                    lo[i] = f[cb + i] - hi[i];
-                    big |= f16_overflows(f[cb + i]);
-                }
-                put8_f16(M0, MBS, r, hg * HALF + cb, hi);
-                put8_f16(ML0, MBS, r, hg * HALF + cb, lo);
+                for (int i = 0; i < 8; i++) big |= f16_overflows(f[cb + i]);
+                put8_f16(M0, MBS, r, hg * HALF + cb, f + cb);
             }
             if (hg == 0) put_side16(M0, MBS, r, DD, valid ? ddv * mu : 0.f);
             zsc = memory_tile(mu);
@@ -576,17 +571,13 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             tmem_st_wait();
             publish();
         };
-        // X += G^T (mu M) for both parts of M (the R|r update; X then holds mu times it)
+        // X = G^T (mu M), M's hi part only (the R|r update; X then holds mu times it)
         auto issue_r_update = [&](bool first) {
-            constexpr uint32_t id = idesc_f16(128, E, 1, 1), id_lo = idesc_f16(128, DD, 1, 1);
+            constexpr uint32_t id = idesc_f16(128, E, 1, 1);
 #pragma unroll
             for (int kk = 0; kk < kBC; kk += 16)
                 mma_bf16_ss(tmem + PL::T_X, sw128_desc(G0 + (kk / 8) * 1024, lboT, 1024),
                             sw32_desc(M0 + (kk / 8) * 256, MBS, 256), id, (!first || kk > 0) ? 1u : 0u);
-#pragma unroll
-            for (int kk = 0; kk < kBC; kk += 16)
-                mma_bf16_ss(tmem + PL::T_X, sw128_desc(G0 + (kk / 8) * 1024, lboT, 1024),
-                            sw32_desc(ML0 + (kk / 8) * 256, MBS, 256), id_lo, 1u);
         };
         // T_RR += X / mu (rows < DD)
         auto add_r_update = [&]() {
@@ -844,10 +835,6 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     for (int kk = 0; kk < kBC; kk += 16)
                         mma_bf16_ts(tmem + PL::T_X, tmem + PL::T_P + kk / 2, sw32_desc(M0 + (kk / 8) * 256, MBS, 256),
                                     id, kk > 0 ? 1u : 0u);
-#pragma unroll
-                    for (int kk = 0; kk < kBC; kk += 16)
-                        mma_bf16_ts(tmem + PL::T_X, tmem + PL::T_P + kk / 2, sw32_desc(ML0 + (kk / 8) * 256, MBS, 256),
-                                    id, 1u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < DD; kk += 16) {
@@ -869,10 +856,6 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     for (int kb = 0; kb < E / 16; kb++)
                         mma_bf16_ss(tmem + PL::T_X, sw32_desc(V0 + kb * MBS, 16, 256), sw32_desc(M0 + kb * MBS, 16, 256),
                                     id, kb > 0 ? 1u : 0u);
-#pragma unroll
-                    for (int kb = 0; kb < DD / 16; kb++)
-                        mma_bf16_ss(tmem + PL::T_X, sw32_desc(V0 + kb * MBS, 16, 256), sw32_desc(ML0 + kb * MBS, 16, 256),
-                                    id, 1u);
                 }
                 finish_mma();
                 tril_to_p(true);
