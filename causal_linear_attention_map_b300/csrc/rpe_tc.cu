@@ -55,7 +55,12 @@ struct RpePlan {
     static constexpr int SMEM = TILES + 2048 > 116 * 1024 ? TILES + 2048 : 116 * 1024;
     static constexpr int NQ16 = DV + 16;
     static constexpr int T_NUM = 0, T_P = 160, T_A0 = 256;   // TMEM columns; A regions at 256 and 384
+    // P slots: two (at 96 and 160) when NUM | DEN leaves room (Dv = 64), so that
+    // P of chunk kc + 1 is written while the product of chunk kc reads P(kc)
+    static constexpr int NP = NQ16 <= 96 ? 2 : 1;
+    static constexpr int T_P1 = 96;
     static_assert(NQ16 <= T_P && T_P + 64 <= T_A0, "TMEM plan");
+    static_assert(NP == 1 || (NQ16 <= T_P1 && T_P1 + 64 <= T_P), "TMEM plan");
     static_assert(SMEM <= 227 * 1024, "shared memory plan");
 };
 
@@ -79,8 +84,8 @@ rpe_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     unsigned char *gbase = smem_raw + (base - smem_u32(smem_raw));
     uint64_t *bar = reinterpret_cast<uint64_t *>(gbase + PL::TILES);
     uint64_t *q_full = bar, *q_ready = bar + 1, *k_full = bar + 2, *k_ready = bar + 4, *v_full = bar + 6,
-             *kv_empty = bar + 8, *a_full = bar + 10, *a_free = bar + 12, *p_ready = bar + 14, *p_free = bar + 15,
-             *num_full = bar + 16;
+             *kv_empty = bar + 8, *a_full = bar + 10, *a_free = bar + 12, *num_full = bar + 16;
+    uint64_t *p_ready = bar + 20, *p_free = bar + 22;   // [NP] each
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 17);
     volatile int *abort_cta = reinterpret_cast<volatile int *>(bar + 18);
     float *cw = reinterpret_cast<float *>(gbase + PL::CW);
@@ -119,8 +124,10 @@ rpe_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             mbar_init(&a_full[i], 1);
             mbar_init(&a_free[i], kRWarps);
         }
-        mbar_init(p_ready, kRWarps);
-        mbar_init(p_free, 1);
+        for (int i = 0; i < PL::NP; i++) {
+            mbar_init(&p_ready[i], kRWarps);
+            mbar_init(&p_free[i], 1);
+        }
         mbar_init(num_full, 1);
         *abort_cta = 0;
         fence_mbar_init();
@@ -197,18 +204,19 @@ rpe_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             if (ok) mma1(0);
             for (int kc = 0; kc < nkc && ok; kc++) {
                 if (kc + 1 < nkc) mma1(kc + 1);
-                const int st = kc % kRNS;
-                ok = ok && wait(p_ready, kc & 1) && wait(&v_full[st], (kc / kRNS) & 1);
+                const int st = kc % kRNS, ps = kc % PL::NP;
+                const uint32_t tp = ps ? PL::T_P1 : PL::T_P;
+                ok = ok && wait(&p_ready[ps], (kc / PL::NP) & 1) && wait(&v_full[st], (kc / kRNS) & 1);
                 tc_fence_after();
                 if (ok) {
                     const uint32_t va = base + PL::V0 + st * PL::VB;
 #pragma unroll
                     for (int kk = 0; kk < kRC; kk += 16)
-                        mma_bf16_ts(tmem + PL::T_NUM, tmem + PL::T_P + kk / 2,
+                        mma_bf16_ts(tmem + PL::T_NUM, tmem + tp + kk / 2,
                                     sw32_desc(va + (kk / 8) * 256, kRC * 32, 256), id_pv,
                                     (kc > 0 || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(p_free);
+                mma_commit(&p_free[ps]);
                 mma_commit(&kv_empty[st]);
             }
             mma_commit(num_full);
@@ -250,15 +258,21 @@ rpe_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             if (lane == 0) mbar_arrive(&k_ready[st]);
         };
         if (nkc > 0) phi_k(0);
+        // the log-weight b_t of this thread's window offset u = threadIdx.x for key
+        // chunk kc: t = (q0 - k0) + u - 127 (read one chunk ahead, off the critical path)
+        auto bias_at = [&](int kc) {
+            const long long t = (long long)(q0 - kc * kRC) + threadIdx.x - (kRC - 1);
+            return threadIdx.x < 2 * kRC - 1 && t > -N && t < N ? bh[t + N - 1] : -INFINITY;
+        };
+        float bnext = nkc > 0 ? bias_at(0) : -INFINITY;
         for (int kc = 0; kc < nkc; kc++) {
+            const float bcur = bnext;
+            if (kc + 1 < nkc) bnext = bias_at(kc + 1);
             if (kc + 1 < nkc) phi_k(kc + 1);
-            const int rg = kc & 1, k0 = kc * kRC;
+            const int rg = kc & 1;
             // weights c_t for t = (q0 - k0) + u - 127, u in [0, 255)
             float *w = cw + (kc & 1) * 256;
-            if (threadIdx.x < 2 * kRC - 1) {
-                const long long t = (long long)(q0 - k0) + threadIdx.x - (kRC - 1);
-                w[threadIdx.x] = (t > -N && t < N) ? __expf(bh[t + N - 1]) : 0.f;
-            }
+            if (threadIdx.x < 2 * kRC - 1) w[threadIdx.x] = bcur == -INFINITY ? 0.f : __expf(bcur);
             asm volatile("bar.sync 1, %0;" ::"n"(kRWarps * 32) : "memory");
             ok = ok && wait_w(&a_full[rg], (kc >> 1) & 1);
             tc_fence_after();
@@ -282,13 +296,14 @@ rpe_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 pk[16 + i] = pack_bf16x2(diag && c + 32 > r ? 0.f : __uint_as_float(a1[2 * i]) * w2,
                                          diag && c + 33 > r ? 0.f : __uint_as_float(a1[2 * i + 1]) * w3);
             }
-            if (kc > 0) ok = ok && wait_w(p_free, (kc - 1) & 1);   // MMA2 of chunk kc - 1 has read P
+            const int ps = kc % PL::NP;   // the P slot of this chunk, free once the product of kc - NP has read it
+            if (kc >= PL::NP) ok = ok && wait_w(&p_free[ps], ((kc / PL::NP) - 1) & 1);
             tc_fence_after();
-            tmem_st32_nowait(tmem + lane_base + PL::T_P + grp * 32, pk);
+            tmem_st32_nowait(tmem + lane_base + (ps ? PL::T_P1 : PL::T_P) + grp * 32, pk);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_ready);
+            if (lane == 0) mbar_arrive(&p_ready[ps]);
         }
         // out = NUM / DEN for this thread's row and column half
         ok = ok && wait_w(num_full, 0);
