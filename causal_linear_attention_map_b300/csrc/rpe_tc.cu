@@ -38,7 +38,6 @@ constexpr int kRC = 128;                 // chunk (queries and keys)
 constexpr int kRWarps = 8;               // TMEM warps
 constexpr int kRProd = 8, kRMma = 9;
 constexpr int kRThreads = 10 * 32;
-constexpr int kRNS = 2;                  // K / V ring depth
 constexpr long long kRBudget = 4000000000LL;
 constexpr int kRErr = 1;
 
@@ -46,10 +45,14 @@ template <int D, int DV>
 struct RpePlan {
     static constexpr int QB = kRC * D * 2;            // Q or K tile (128-byte swizzle, 64-column boxes)
     static constexpr int VB = kRC * (DV + 16) * 2;    // V slot: DV / 16 boxes of 16 columns + ONES
+    // K / V ring depth: as deep as shared memory allows, up to 4 (the load of key
+    // chunk kc + NS is issued once the product of chunk kc has read its slot)
+    static constexpr int kFix = QB + 2 * 256 * 4 + 2048;
+    static constexpr int NS = kFix + 4 * (QB + VB) <= 227 * 1024 ? 4 : kFix + 3 * (QB + VB) <= 227 * 1024 ? 3 : 2;
     static constexpr int Q0 = 0;
     static constexpr int K0 = Q0 + QB;
-    static constexpr int V0 = K0 + kRNS * QB;
-    static constexpr int CW = V0 + kRNS * VB;         // weights window [2][256] fp32
+    static constexpr int V0 = K0 + NS * QB;
+    static constexpr int CW = V0 + NS * VB;           // weights window [2][256] fp32
     static constexpr int TILES = CW + 2 * 256 * 4;
     // at least 116 KB, so that one CTA holds an SM (it allocates all 512 TMEM columns)
     static constexpr int SMEM = TILES + 2048 > 116 * 1024 ? TILES + 2048 : 116 * 1024;
@@ -83,8 +86,8 @@ rpe_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const uint32_t base = r_align1k(smem_u32(smem_raw));
     unsigned char *gbase = smem_raw + (base - smem_u32(smem_raw));
     uint64_t *bar = reinterpret_cast<uint64_t *>(gbase + PL::TILES);
-    uint64_t *q_full = bar, *q_ready = bar + 1, *k_full = bar + 2, *k_ready = bar + 4, *v_full = bar + 6,
-             *kv_empty = bar + 8, *a_full = bar + 10, *a_free = bar + 12, *num_full = bar + 16;
+    uint64_t *q_full = bar, *q_ready = bar + 1, *a_full = bar + 10, *a_free = bar + 12, *num_full = bar + 16;
+    uint64_t *k_full = bar + 24, *k_ready = bar + 28, *v_full = bar + 32, *kv_empty = bar + 36;   // [NS] each
     uint64_t *p_ready = bar + 20, *p_free = bar + 22;   // [NP] each
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 17);
     volatile int *abort_cta = reinterpret_cast<volatile int *>(bar + 18);
@@ -114,7 +117,7 @@ rpe_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         mbar_init(q_ready, kRWarps);
-        for (int i = 0; i < kRNS; i++) {
+        for (int i = 0; i < PL::NS; i++) {
             mbar_init(&k_full[i], 1);
             mbar_init(&k_ready[i], kRWarps);
             mbar_init(&v_full[i], 1);
@@ -134,7 +137,7 @@ rpe_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
     if (warp < kRWarps) {   // the ONES block after each V slot's DV / 16 boxes
         const uint32_t one = pack_bf16x2(1.f, 1.f);
-        for (int i = threadIdx.x; i < kRNS * kRC; i += kRWarps * 32) {
+        for (int i = threadIdx.x; i < PL::NS * kRC; i += kRWarps * 32) {
             const int st = i / kRC, r = i % kRC;
             const uint32_t blk = base + PL::V0 + st * PL::VB + (DV / 16) * (kRC * 32);
             sts128(blk + sw32_off(r, 0), make_uint4(one, one, one, one));
@@ -160,8 +163,8 @@ rpe_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 tma_load_3d(gbase + PL::Q0 + b * (kRC * 128), &tm_q, q_full, b * 64, qc * kRC, h);
             int issued = 0;
             for (int kc = 0; kc < nkc; kc++) {
-                const int st = kc % kRNS;
-                if (kc >= kRNS && !wait(&kv_empty[st], ((kc / kRNS) - 1) & 1)) break;
+                const int st = kc % PL::NS;
+                if (kc >= PL::NS && !wait(&kv_empty[st], ((kc / PL::NS) - 1) & 1)) break;
                 mbar_arrive_expect_tx(&k_full[st], PL::QB);
                 for (int b = 0; b < D / 64; b++)
                     tma_load_3d_hint(gbase + PL::K0 + st * PL::QB + b * (kRC * 128), &tm_k, &k_full[st], b * 64,
@@ -174,9 +177,9 @@ rpe_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
             // loads still in flight after an abort land before the CTA exits
             mbar_wait(q_full, 0, nullptr, 0, kRBudget);
-            for (int kc = issued > kRNS ? issued - kRNS : 0; kc < issued; kc++) {
-                mbar_wait(&k_full[kc % kRNS], (kc / kRNS) & 1, nullptr, 0, kRBudget);
-                mbar_wait(&v_full[kc % kRNS], (kc / kRNS) & 1, nullptr, 0, kRBudget);
+            for (int kc = issued > PL::NS ? issued - PL::NS : 0; kc < issued; kc++) {
+                mbar_wait(&k_full[kc % PL::NS], (kc / PL::NS) & 1, nullptr, 0, kRBudget);
+                mbar_wait(&v_full[kc % PL::NS], (kc / PL::NS) & 1, nullptr, 0, kRBudget);
             }
         }
     } else if (warp == kRMma) {
@@ -186,9 +189,9 @@ rpe_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             constexpr uint32_t id_pv = idesc_bf16(128, PL::NQ16, 0, 1);
             bool ok = wait(q_ready, 0);
             auto mma1 = [&](int kc) {
-                const int st = kc % kRNS, rg = kc & 1;
+                const int st = kc % PL::NS, rg = kc & 1;
                 if (kc >= 2) ok = ok && wait(&a_free[rg], ((kc >> 1) - 1) & 1);
-                ok = ok && wait(&k_ready[st], (kc / kRNS) & 1);
+                ok = ok && wait(&k_ready[st], (kc / PL::NS) & 1);
                 tc_fence_after();
                 if (ok) {
                     const uint32_t qa = base + PL::Q0, ka = base + PL::K0 + st * PL::QB;
@@ -204,9 +207,9 @@ rpe_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             if (ok) mma1(0);
             for (int kc = 0; kc < nkc && ok; kc++) {
                 if (kc + 1 < nkc) mma1(kc + 1);
-                const int st = kc % kRNS, ps = kc % PL::NP;
+                const int st = kc % PL::NS, ps = kc % PL::NP;
                 const uint32_t tp = ps ? PL::T_P1 : PL::T_P;
-                ok = ok && wait(&p_ready[ps], (kc / PL::NP) & 1) && wait(&v_full[st], (kc / kRNS) & 1);
+                ok = ok && wait(&p_ready[ps], (kc / PL::NP) & 1) && wait(&v_full[st], (kc / PL::NS) & 1);
                 tc_fence_after();
                 if (ok) {
                     const uint32_t va = base + PL::V0 + st * PL::VB;
@@ -252,8 +255,8 @@ rpe_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (lane == 0) mbar_arrive(q_ready);
         const int q0 = qc * kRC;
         auto phi_k = [&](int kc) {
-            const int st = kc % kRNS;
-            ok = ok && wait_w(&k_full[st], (kc / kRNS) & 1);
+            const int st = kc % PL::NS;
+            ok = ok && wait_w(&k_full[st], (kc / PL::NS) & 1);
             if (ok) phi_half(base + PL::K0 + st * PL::QB, kc * kRC + r >= N);
             if (lane == 0) mbar_arrive(&k_ready[st]);
         };
