@@ -17,9 +17,12 @@
 // between key chunks, so the product of chunk kc + 1 runs while the TMEM
 // warps turn chunk kc into P.
 //
-// Roles (10 warps): warps 0-7 TMEM warps (phi in place on the Q tile and on
+// Roles (18 warps): warps 0-15 TMEM warps (phi in place on the Q tile and on
 // each K tile, P, the epilogue; warp w owns TMEM lanes 32 (w % 4).. and
-// column half w / 4), warp 8 the TMA producer, warp 9 the MMA thread.
+// column quarter w / 4), warp 16 the TMA producer, warp 17 the MMA thread.
+// The K / V ring is as deep as shared memory allows (4 slots at D = Dv =
+// 64): with two, the load of key chunk kc + 2 waited for the product of
+// chunk kc, and the TMEM warps waited for that load.
 // Every wait is bounded: on expiry the library's error word is set and all
 // roles finish without waiting.
 #include <cuda.h>
@@ -35,9 +38,10 @@ namespace {
 using namespace tc;
 
 constexpr int kRC = 128;                 // chunk (queries and keys)
-constexpr int kRWarps = 8;               // TMEM warps
-constexpr int kRProd = 8, kRMma = 9;
-constexpr int kRThreads = 10 * 32;
+constexpr int kRWarps = 16;              // TMEM warps: 4 lane quadrants x 4 column groups
+constexpr int kRGroups = kRWarps / 4;
+constexpr int kRProd = kRWarps, kRMma = kRWarps + 1;
+constexpr int kRThreads = (kRWarps + 2) * 32;
 constexpr long long kRBudget = 4000000000LL;
 constexpr int kRErr = 1;
 
@@ -81,7 +85,7 @@ rpe_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               __nv_bfloat16 *__restrict__ out, int BH, int N, int H, int causal, int *err)
 {
     using PL = RpePlan<D, DV>;
-    constexpr int HALF = DV / 2;
+    constexpr int QTR = DV / kRGroups;   // NUM columns per thread in the epilogue
     extern __shared__ unsigned char smem_raw[];
     const uint32_t base = r_align1k(smem_u32(smem_raw));
     unsigned char *gbase = smem_raw + (base - smem_u32(smem_raw));
@@ -230,20 +234,15 @@ rpe_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int qd = warp & 3, grp = warp >> 2;
         const int r = qd * 32 + lane;
         const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
-        constexpr int JH = D / 16;   // 16 B chunks per half row
-        // phi in place on this thread's half row of a tile; `zero`: the row is past the sequence
+        constexpr int JH = D / 8 / kRGroups;   // 16 B chunks per quarter row
+        // phi in place on this thread's quarter row of a tile; `zero`: the row is past the sequence
         auto phi_half = [&](uint32_t t, bool zero) {
-#pragma unroll 1
-            for (int j0 = 0; j0 < JH; j0 += 4) {
-                uint4 x[4];
+            uint4 x[JH];
 #pragma unroll
-                for (int j = 0; j < 4; j++)
-                    if (j0 + j < JH) x[j] = lds128(t + r_tile_off(r, grp * JH + j0 + j));
+            for (int j = 0; j < JH; j++) x[j] = lds128(t + r_tile_off(r, grp * JH + j));
 #pragma unroll
-                for (int j = 0; j < 4; j++)
-                    if (j0 + j < JH)
-                        sts128(t + r_tile_off(r, grp * JH + j0 + j), zero ? make_uint4(0, 0, 0, 0) : phi_elu1_bf16x8(x[j]));
-            }
+            for (int j = 0; j < JH; j++)
+                sts128(t + r_tile_off(r, grp * JH + j), zero ? make_uint4(0, 0, 0, 0) : phi_elu1_bf16x8(x[j]));
             fence_proxy_async_smem();
             __syncwarp();
         };
@@ -279,30 +278,26 @@ rpe_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             asm volatile("bar.sync 1, %0;" ::"n"(kRWarps * 32) : "memory");
             ok = ok && wait_w(&a_full[rg], (kc >> 1) & 1);
             tc_fence_after();
-            uint32_t a0[32], a1[32];
-            const uint32_t ra = tmem + lane_base + PL::T_A0 + rg * 128 + grp * 64;
+            uint32_t a0[32];
+            const uint32_t ra = tmem + lane_base + PL::T_A0 + rg * 128 + grp * 32;
             tmem_ld32_nowait(ra, a0);
-            tmem_ld32_nowait(ra + 32, a1);
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&a_free[rg]);
             const bool diag = causal && kc == qc;
-            uint32_t pk[32];
+            uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; i++) {
-                const int c = grp * 64 + 2 * i;   // key index in the chunk
+                const int c = grp * 32 + 2 * i;   // key index in the chunk
                 const float w0 = w[r - c + kRC - 1], w1 = w[r - c - 1 + kRC - 1];
-                const float w2 = w[r - c - 32 + kRC - 1], w3 = w[r - c - 33 + kRC - 1];
                 pk[i] = pack_bf16x2(diag && c > r ? 0.f : __uint_as_float(a0[2 * i]) * w0,
                                     diag && c + 1 > r ? 0.f : __uint_as_float(a0[2 * i + 1]) * w1);
-                pk[16 + i] = pack_bf16x2(diag && c + 32 > r ? 0.f : __uint_as_float(a1[2 * i]) * w2,
-                                         diag && c + 33 > r ? 0.f : __uint_as_float(a1[2 * i + 1]) * w3);
             }
             const int ps = kc % PL::NP;   // the P slot of this chunk, free once the product of kc - NP has read it
             if (kc >= PL::NP) ok = ok && wait_w(&p_free[ps], ((kc / PL::NP) - 1) & 1);
             tc_fence_after();
-            tmem_st32_nowait(tmem + lane_base + (ps ? PL::T_P1 : PL::T_P) + grp * 32, pk);
+            tmem_st16_nowait(tmem + lane_base + (ps ? PL::T_P1 : PL::T_P) + grp * 16, pk);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -312,29 +307,22 @@ rpe_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         ok = ok && wait_w(num_full, 0);
         tc_fence_after();
         // the loads by the whole warp; only the stores depend on the row
-        uint32_t d[16], n0[32], n1[32];
+        uint32_t d[16], n0[32];
         tmem_ld16_nowait(tmem + lane_base + PL::T_NUM + DV, d);
-        tmem_ld32_nowait(tmem + lane_base + PL::T_NUM + grp * HALF, n0);
-        if constexpr (HALF == 64) tmem_ld32_nowait(tmem + lane_base + PL::T_NUM + grp * HALF + 32, n1);
+        if constexpr (QTR == 32)
+            tmem_ld32_nowait(tmem + lane_base + PL::T_NUM + grp * QTR, n0);
+        else
+            tmem_ld16_nowait(tmem + lane_base + PL::T_NUM + grp * QTR, *reinterpret_cast<uint32_t(*)[16]>(n0));
         tmem_ld_wait();
         if (ok && q0 + r < N) {
             const float inv = 1.f / __uint_as_float(d[0]);
-            uint4 *dst = reinterpret_cast<uint4 *>(out + ((long long)h * N + q0 + r) * DV + grp * HALF);
+            uint4 *dst = reinterpret_cast<uint4 *>(out + ((long long)h * N + q0 + r) * DV + grp * QTR);
 #pragma unroll
-            for (int j = 0; j < 4; j++)
+            for (int j = 0; j < QTR / 8; j++)
                 dst[j] = make_uint4(pack_bf16x2(__uint_as_float(n0[8 * j]) * inv, __uint_as_float(n0[8 * j + 1]) * inv),
                                     pack_bf16x2(__uint_as_float(n0[8 * j + 2]) * inv, __uint_as_float(n0[8 * j + 3]) * inv),
                                     pack_bf16x2(__uint_as_float(n0[8 * j + 4]) * inv, __uint_as_float(n0[8 * j + 5]) * inv),
                                     pack_bf16x2(__uint_as_float(n0[8 * j + 6]) * inv, __uint_as_float(n0[8 * j + 7]) * inv));
-            if constexpr (HALF == 64) {
-#pragma unroll
-                for (int j = 0; j < 4; j++)
-                    dst[4 + j] = make_uint4(
-                        pack_bf16x2(__uint_as_float(n1[8 * j]) * inv, __uint_as_float(n1[8 * j + 1]) * inv),
-                        pack_bf16x2(__uint_as_float(n1[8 * j + 2]) * inv, __uint_as_float(n1[8 * j + 3]) * inv),
-                        pack_bf16x2(__uint_as_float(n1[8 * j + 4]) * inv, __uint_as_float(n1[8 * j + 5]) * inv),
-                        pack_bf16x2(__uint_as_float(n1[8 * j + 6]) * inv, __uint_as_float(n1[8 * j + 7]) * inv));
-            }
         }
         tc_fence_before();
     }
