@@ -106,7 +106,7 @@ constexpr int kItemConsumers = kTmemWarps + kPhiWarps + 4;
 template <int JR> constexpr int kAggSplit1 = JR - 2 * (JR / 3);
 template <int JR> constexpr int kAggSplit2 = JR - JR / 3;
 
-template <int DP, int DV>
+template <int DP, int DV, bool SUMF = false>
 struct Plan {
     static constexpr int QB = kC * DP * 2;   // one Q or K chunk tile (bytes)
     static constexpr int kBudget = 227 * 1024 - 2048;
@@ -119,9 +119,11 @@ struct Plan {
     // about the same for N = 16 as for N = 144 with these operands).
     static constexpr int NQ16 = DV + 16;
     static constexpr int VB = kC * NQ16 * 2;   // one V slot: DV / 16 blocks + ONES
-    // DP = 256 (both halves of a 256-feature map at once) runs only in the
-    // segment-sum form: no Q ring and no S_prev buffer
-    static constexpr bool kSumOnly = DP > 128;
+    // The segment-sum form (SUMF; and DP = 256, both halves of a 256-feature
+    // map at once, which runs only in that form) has no Q ring and no S_prev
+    // buffer: its K and V rings take the space (three stages at D = Dv = 128
+    // instead of two)
+    static constexpr bool kSumOnly = DP > 128 || SUMF;
     // S_prev pieces along Dphi: one, or two 64-row halves when that is what
     // lets two-deep rings fit (each piece with its own z block)
     static constexpr int NSP = kSumOnly || (2 * (2 * QB + VB) + DP * NQ16 * 2 <= kBudget) ? 1 : 2;
@@ -328,7 +330,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                  __nv_bfloat16 *__restrict__ out, float *__restrict__ S_out,
                  float *__restrict__ z_out, int *err)
 {
-    using PL = Plan<DP, DV>;
+    using PL = Plan<DP, DV, AGG>;
     constexpr int NS = PL::NS, NSP = PL::NSP, PR = PL::PR;
     constexpr int HALF = DV / 2;   // state / NUM columns per TMEM warp
     constexpr bool kPhi = MODE == kModeElu;   // apply elu + 1 to the Q and K tiles in place
@@ -1818,7 +1820,8 @@ template <int DP, int DV, int MODE>
 cudaError_t set_smem()
 {
     using PL = Plan<DP, DV>;
-    cudaError_t e = set_max_smem_once<tc_causal_kernel<DP, DV, true, MODE == kModeElu ? kModeElu : kModeFeat>>(PL::SMEM);
+    cudaError_t e = set_max_smem_once<tc_causal_kernel<DP, DV, true, MODE == kModeElu ? kModeElu : kModeFeat>>(
+        Plan<DP, DV, true>::SMEM);
     if (e != cudaSuccess) return e;
     return set_max_smem_once<tc_causal_kernel<DP, DV, false, MODE>>(PL::SMEM);
 }
@@ -1844,7 +1847,7 @@ cudaError_t run_causal(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
         // pass 1: the sums of every segment but the last of each head; then the scan
         Geo ga = g;
         ga.n_items = g.BH * (g.nseg - 1);
-        tc_causal_kernel<DP, DV, true, AMODE><<<min(ga.n_items, sms), kThreads, PL::SMEM, s>>>(
+        tc_causal_kernel<DP, DV, true, AMODE><<<min(ga.n_items, sms), kThreads, Plan<DP, DV, true>::SMEM, s>>>(
             tq, tk, tv_agg, to, ga, sc, (__nv_bfloat16 *)out, nullptr, nullptr, err);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         const int sz = DP * DV + DP;
@@ -1883,7 +1886,7 @@ cudaError_t run_totals(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
     cudaError_t e;
     if ((e = set_smem<DP, DV, AMODE>()) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(scratch, 0, 16, s)) != cudaSuccess) return e;
-    tc_causal_kernel<DP, DV, true, AMODE><<<min(g.n_items, sms), kThreads, PL::SMEM, s>>>(
+    tc_causal_kernel<DP, DV, true, AMODE><<<min(g.n_items, sms), kThreads, Plan<DP, DV, true>::SMEM, s>>>(
         tq, tk, tv_agg, to, g, sc, nullptr, nullptr, nullptr, err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (!with_totals) {   // the readout adds the segment sums up itself
