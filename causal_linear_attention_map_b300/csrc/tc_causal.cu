@@ -458,8 +458,11 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (role == item_role) {
                     ok = it < 2 || wait_bar(&item_empty[slot], ((it >> 1) - 1) & 1, ctl);
                     // no new item once any CTA of this launch has given up a wait
-                    if (ok && !*abort_cta && !*ctl.glob) {
-                        item = it == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(sc.ticket, 1);
+                    // (with no more items than CTAs, no ticket and no shared abort word is
+                    // read: the header need not be cleared for such a launch)
+                    const bool dyn = g.n_items > (int)gridDim.x;
+                    if (ok && !*abort_cta && (!dyn || !*ctl.glob)) {
+                        item = it == 0 ? (int)blockIdx.x : dyn ? (int)gridDim.x + atomicAdd(sc.ticket, 1) : -1;
                         if (item >= g.n_items) item = -1;
                     }
                     item_slot[slot] = item;
@@ -1155,9 +1158,10 @@ nc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (producer) {
             const bool ok = it < 2 || wait_bar(&item_empty[slot], ((it >> 1) - 1) & 1, ctl);
             int item = -1;
-            if (ok && !*abort_cta && !*ctl.glob) {   // (not after another CTA gave up a wait)
+            const bool dyn = g.n_items > (int)gridDim.x;   // (else no ticket or shared abort word is read)
+            if (ok && !*abort_cta && (!dyn || !*ctl.glob)) {   // (not after another CTA gave up a wait)
                 // item b for CTA b first, then tickets offset by the grid size
-                item = it == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(sc.ticket, 1);
+                item = it == 0 ? (int)blockIdx.x : dyn ? (int)gridDim.x + atomicAdd(sc.ticket, 1) : -1;
                 if (item >= g.n_items) item = -1;
             }
             item_slot[slot] = item;
@@ -1842,7 +1846,8 @@ cudaError_t run_causal(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
     cudaError_t e;
     int launches = 0;
     if ((e = set_smem<DP, DV, MODE>()) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(scratch, 0, 16, s)) != cudaSuccess) return e;
+    // the header (tickets, abort word) is read only by launches with more items than CTAs
+    if (g.n_items > sms && (e = cudaMemsetAsync(scratch, 0, 16, s)) != cudaSuccess) return e;
     if (g.nseg > 1) {
         // pass 1: the sums of every segment but the last of each head; then the scan
         Geo ga = g;
@@ -1885,7 +1890,8 @@ cudaError_t run_totals(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
     Scratch sc = carve<DP, DV>(scratch, g);
     cudaError_t e;
     if ((e = set_smem<DP, DV, AMODE>()) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(scratch, 0, 16, s)) != cudaSuccess) return e;
+    // the header (tickets, abort word) is read only by launches with more items than CTAs
+    if (g.n_items > sms && (e = cudaMemsetAsync(scratch, 0, 16, s)) != cudaSuccess) return e;
     tc_causal_kernel<DP, DV, true, AMODE><<<min(g.n_items, sms), kThreads, Plan<DP, DV, true>::SMEM, s>>>(
         tq, tk, tv_agg, to, g, sc, nullptr, nullptr, nullptr, err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
