@@ -1295,6 +1295,8 @@ nc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const int c0 = s * g.L, nc = min(g.L, g.NC - c0);
             // S (bf16) and ZP for this head, once the last item's products are done
             if (ni > 0) wait_bar(s_free, (ni - 1) & 1, ctl);
+            const bool first_item = ni == 0;
+            if (first_item) phi_q();   // phi(Q) of the first chunk does not wait for the sums
             griddep_wait();   // the totals kernel (or the segment-sum pass) has completed
             // the head's totals: read (nsum = 0), or added up from its segments' sums
             const int nsl = sc.nsum > 0 ? sc.nsum : 1;
@@ -1341,7 +1343,7 @@ nc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             __syncwarp();
             if (lane == 0) mbar_arrive(s_ready);
             ni++;
-            phi_q();
+            if (!first_item) phi_q();
             for (int c = 0; c < nc; c++, k++) {
                 if (c + 1 < nc) phi_q();
                 // out = NUM / (DEN[0] + DEN[8]) for chunk k -> staging slot k % NO
