@@ -225,6 +225,9 @@ bwd_sums_kernel(const T *__restrict__ k, const T *__restrict__ v, const float *_
 //   mode 0: exclusive prefix   mode 1: exclusive suffix   mode 2: total in every slot
 __global__ void bwd_scan_kernel(float *__restrict__ st, int nseg, int elems, int mode)
 {
+    // (a dependent launch after the tensor-core passes: wait for the sums)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const long long h = blockIdx.y;
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
     if (e >= elems) return;
@@ -500,8 +503,7 @@ bool backward_supported(const Problem &p) { return (long long)p.P * p.Dv <= 1638
 cudaError_t backward_scan(float *st, long long BH, int nseg, int elems, int mode, cudaStream_t s)
 {
     const dim3 sgrid((unsigned)cdiv(elems, kBT), (unsigned)BH);
-    bwd_scan_kernel<<<sgrid, kBT, 0, s>>>(st, nseg, elems, mode);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_dependent(bwd_scan_kernel, sgrid, dim3(kBT), 0, s, st, nseg, elems, mode);
     if (e == cudaSuccess) note_launches(1);
     return e;
 }

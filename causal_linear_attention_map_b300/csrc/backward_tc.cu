@@ -333,6 +333,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         return m;
     };
 
+    // the next launch (a scan) may start; this pass reads the previous one's
+    // results only after it has completed (dependent launches)
+    griddep_launch();
+    if constexpr (PASS != 0) griddep_wait();
     // ---- the memory at the segment's start (dq: S|z prefix; dk/dv: R|r suffix) -> TMEM
     if constexpr (PASS != 0) {
         const float *src = (PASS == 1 ? stS : stR) + slot;
@@ -1008,12 +1012,14 @@ cudaError_t launch_btc(const Problem &p, const void *dout, void *dq, void *dk, v
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     note_launches(1);
     if ((e = backward_scan(stS, g.BH, g.nseg, elems, causal ? 0 : 2, s)) != cudaSuccess) return e;
-    bwd_tc_kernel<DD, 1><<<items, kBThreads, PL::SMEM, s>>>(tq, tk, tv, to, g, c, stS, stR, den, dd, bq, nullptr, err);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_dependent(bwd_tc_kernel<DD, 1>, dim3(items), dim3(kBThreads), PL::SMEM, s, tq, tk, tv, to, g, c,
+                              stS, stR, den, dd, bq, (__nv_bfloat16 *)nullptr, err)) != cudaSuccess)
+        return e;
     note_launches(1);
     if ((e = backward_scan(stR, g.BH, g.nseg, elems, causal ? 1 : 2, s)) != cudaSuccess) return e;
-    bwd_tc_kernel<DD, 2><<<items, kBThreads, PL::SMEM, s>>>(tq, tk, tv, to, g, c, stS, stR, den, dd, bk, bv, err);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_dependent(bwd_tc_kernel<DD, 2>, dim3(items), dim3(kBThreads), PL::SMEM, s, tq, tk, tv, to, g, c,
+                              stS, stR, den, dd, bk, bv, err)) != cudaSuccess)
+        return e;
     note_launches(1);
     return cudaSuccess;
 }
