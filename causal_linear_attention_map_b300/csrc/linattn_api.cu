@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "kernels.h"
+#include "prf_tc.h"
 #include "linattn.h"
 
 namespace la {
@@ -145,6 +146,16 @@ int forward_impl(const void *q, const void *k, const void *v, void *out, int B, 
     DeviceCtx *ctx = nullptr;
     if ((st = get_ctx(&ctx)) != LA_OK) return st;
 
+    if (la::prf_fused_supported(p, causal != 0)) {
+        // causal random features with the feature map formed on chip
+        const size_t fb = la::prf_fused_scratch_bytes(p);
+        void *scratch = nullptr;
+        if (fb && cudaMallocFromPoolAsync(&scratch, fb, ctx->pool, s) != cudaSuccess)
+            return cuda_status(cudaErrorMemoryAllocation);
+        cudaError_t e = la::prf_fused_forward(p, scratch, S_out, z_out, ctx->err_word, s);
+        cudaError_t e2 = scratch ? cudaFreeAsync(scratch, s) : cudaSuccess;
+        return cuda_status(e != cudaSuccess ? e : e2);
+    }
     const bool tc = la::tc_causal_supported(p) || la::tc_prf_supported(p);
     if (causal && !tc) return cuda_status(la::simt_causal(p, S_out, z_out, s));
     size_t bytes = tc ? la::tc_scratch_bytes(p, causal != 0) : la::noncausal_scratch_bytes(p);

@@ -145,19 +145,21 @@ def test_long_segment_chain_prf(la, H, N, m, Dv, causal):
 
 
 def test_prf_launch_plan(la):
-    """m = 256, few heads: the projection, then (causal: 5 kernels) one
-    segment-sum pass over all 256 features, the scan, and the output pass of
-    each 128-feature half, or (non-causal: 6 kernels) the segment-sum pass
-    and the totals per half, then one readout."""
-    W = wl.make_W(256, 64).cuda()
-    fm = la.FeatureMap("prf", W)
-    w = wl.small(B=1, H=2, N=2048, D=64, Dv=64, feature="prf", m=256, seed=9)
-    q, k, v = (t.cuda() for t in wl.make_qkv(w))
-    for causal, expect in ((True, 5), (False, 6)):
+    """Causal random features with D = Dv = 64 form phi on chip: with few
+    heads (segments) the segment-sum pass, the scan and one output pass per
+    128-feature block (m = 256: 4 kernels, m = 128: 3), with one segment per
+    head only the output passes (2, 1).  Non-causal m = 256 projects phi first,
+    then runs the segment-sum pass and the totals per half and one readout
+    (6 kernels)."""
+    for m, H, causal, expect in ((256, 2, True, 4), (128, 2, True, 3), (256, 160, True, 2),
+                                 (128, 160, True, 1), (256, 2, False, 6)):
+        fm = la.FeatureMap("prf", wl.make_W(m, 64).cuda())
+        w = wl.small(B=1, H=H, N=2048 if H < 100 else 256, D=64, Dv=64, feature="prf", m=m, seed=9)
+        q, k, v = (t.cuda() for t in wl.make_qkv(w))
         n0 = la.la_launch_count()
         la.la_forward(q, k, v, causal=causal, feature_map=fm)
         torch.cuda.synchronize()
-        assert la.la_launch_count() - n0 == expect, causal
+        assert la.la_launch_count() - n0 == expect, (m, H, causal)
 
 
 def test_noncausal_launch_plan(la):

@@ -61,6 +61,13 @@ SMALL = [
     # pass or scan, for both feature-map layouts of the causal random features
     (200, 64, 64, 2, 80, "prf", 256, "bf16", True),
     (150, 64, 128, 1, 160, "prf", 128, "bf16", True),
+    # causal random features with phi formed in the chunk kernel (D = Dv = 64):
+    # m = 128 with segments and a ragged tail, many heads with one segment
+    # each, a head shorter than one chunk, and exactly one chunk
+    (777, 64, 64, 1, 3, "prf", 128, "bf16", True),
+    (300, 64, 64, 2, 80, "prf", 128, "bf16", True),
+    (77, 64, 64, 1, 2, "prf", 256, "bf16", True),
+    (128, 64, 64, 1, 1, "prf", 128, "bf16", True),
 ]
 
 
