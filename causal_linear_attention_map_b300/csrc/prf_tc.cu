@@ -622,22 +622,30 @@ prf_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll 1
             for (int kind = AGG ? 1 : 0; kind < 2; kind++) {
                 const uint32_t t = base + (kind == 0 ? PL::Q0 : PL::K0) + sl * PL::PB;
-                wait_bar(&x_full[kind * 4 + sl], (j / NS) & 1, ctl);
-                float sq = 0.f;   // |x|^2 of row r
+                // |x|^2 of row r.  A q row's PRF factor exp(-|q|^2 / 2) multiplies
+                // every feature of that row, so it cancels between the numerator
+                // phi(q)^T S and the denominator phi(q)^T z: q tiles skip it (NPRF,
+                // whose u / |x| is not such a factor, does not)
+                const bool need_sq = kind == 1 || a.normalize;
+                float sq = 0.f;
+                if (need_sq) {
+                    wait_bar(&x_full[kind * 4 + sl], (j / NS) & 1, ctl);
 #pragma unroll
-                for (int c = 0; c < kD / 8; c++) {
-                    const uint4 x = lds128(t + sw128_off(r, c));
-                    const uint32_t u[4] = {x.x, x.y, x.z, x.w};
+                    for (int c = 0; c < kD / 8; c++) {
+                        const uint4 x = lds128(t + sw128_off(r, c));
+                        const uint32_t u[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-                    for (int i = 0; i < 4; i++) {
-                        const float lo = __uint_as_float(u[i] << 16), hi = __uint_as_float(u[i] & 0xffff0000u);
-                        sq = fmaf(lo, lo, sq);
-                        sq = fmaf(hi, hi, sq);
+                        for (int i = 0; i < 4; i++) {
+                            const float lo = __uint_as_float(u[i] << 16), hi = __uint_as_float(u[i] & 0xffff0000u);
+                            sq = fmaf(lo, lo, sq);
+                            sq = fmaf(hi, hi, sq);
+                        }
                     }
                 }
                 // PRF: exp(u - |x|^2/2 - ln(m)/2); NPRF: exp(u / |x| - 1/2 - ln(m)/2), as 2^(u a - b)
                 const float us = a.normalize ? (sq > 0.f ? rsqrtf(sq) : 0.f) : 1.f;
                 const float sh = a.normalize ? (sq > 0.f ? 0.5f : 0.f) + a.log_scale : 0.5f * sq + a.log_scale;
+                // (PRF q rows: sq = 0 here, the factor left out as above)
                 const float ua = us * kLog2e, ub = sh * kLog2e;
                 const bool zero = kind == 1 && r >= nvalid;   // k rows past the end add nothing
                 // (U complete means the projection has read x)
@@ -651,7 +659,7 @@ prf_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 __syncwarp();
                 if (lane == 0) mbar_arrive(u_free);
                 nt++;
-                quad_pair_sync(qd);   // both exp warps of this quadrant have read x: box 0 can take phi
+                if (need_sq) quad_pair_sync(qd);   // both exp warps of this quadrant have read x: box 0 can take phi
                 auto emit = [&](const uint32_t(&v)[32], int h) {
 #pragma unroll
                     for (int q4 = 0; q4 < 4; q4++) {
