@@ -144,7 +144,7 @@ struct PrfGeo {
 };
 
 struct PrfArgs {
-    const __nv_bfloat16 *q, *k;   // [BH, N, 64]: the row norms |x|^2
+    const float *sqk, *sqq;   // [BH, N]: |k|^2, |q|^2 (NPRF) of every row, from the norm pass
     const float *W;   // [m, 64] fp32
     float *preS;      // [BH, nb, nseg, 128, 64]: segment sums, then exclusive prefixes
     float *prez;      // [BH, nb, nseg, 128]
@@ -209,12 +209,6 @@ __device__ __forceinline__ float ex2_approx(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-// Sync of the two exp warps of one lane quadrant (named barrier 1 + qd).
-__device__ __forceinline__ void quad_pair_sync(int qd)
-{
-    asm volatile("bar.sync %0, 64;" ::"r"(1 + qd) : "memory");
 }
 
 // 32 fp32 state values -> bf16 at row r, columns [c0, c0 + 32) of the
@@ -619,36 +613,26 @@ prf_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         for (uint32_t j = 0; w.valid; j++, w.advance(g)) {
             const int sl = j % NS;
             const int nvalid = g.N - w.row0();   // rows of this chunk inside the sequence
+            // |x|^2 of row r of this chunk's k (and, for NPRF, q) tile, from the
+            // norm pass: loaded now, used once the tile's U is ready.  A q row's
+            // PRF factor exp(-|q|^2 / 2) multiplies every feature of that row, so
+            // it cancels between the numerator phi(q)^T S and the denominator
+            // phi(q)^T z: PRF q tiles leave it out (NPRF's u / |x| is no such factor)
+            const long long grow = (long long)w.it.bh * g.N + w.row0() + r;
+            const bool in = r < nvalid;
+            const float sq_k = in ? __ldcg(a.sqk + grow) : 0.f;
+            const float sq_q = in && a.normalize && !AGG ? __ldcg(a.sqq + grow) : 0.f;
 #pragma unroll 1
             for (int kind = AGG ? 1 : 0; kind < 2; kind++) {
                 const uint32_t t = base + (kind == 0 ? PL::Q0 : PL::K0) + sl * PL::PB;
-                // |x|^2 of row r.  A q row's PRF factor exp(-|q|^2 / 2) multiplies
-                // every feature of that row, so it cancels between the numerator
-                // phi(q)^T S and the denominator phi(q)^T z: q tiles skip it (NPRF,
-                // whose u / |x| is not such a factor, does not)
-                const bool need_sq = kind == 1 || a.normalize;
-                float sq = 0.f;
-                if (need_sq) {
-                    wait_bar(&x_full[kind * 4 + sl], (j / NS) & 1, ctl);
-#pragma unroll
-                    for (int c = 0; c < kD / 8; c++) {
-                        const uint4 x = lds128(t + sw128_off(r, c));
-                        const uint32_t u[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                        for (int i = 0; i < 4; i++) {
-                            const float lo = __uint_as_float(u[i] << 16), hi = __uint_as_float(u[i] & 0xffff0000u);
-                            sq = fmaf(lo, lo, sq);
-                            sq = fmaf(hi, hi, sq);
-                        }
-                    }
-                }
+                const float sq = kind == 1 ? sq_k : sq_q;
                 // PRF: exp(u - |x|^2/2 - ln(m)/2); NPRF: exp(u / |x| - 1/2 - ln(m)/2), as 2^(u a - b)
                 const float us = a.normalize ? (sq > 0.f ? rsqrtf(sq) : 0.f) : 1.f;
                 const float sh = a.normalize ? (sq > 0.f ? 0.5f : 0.f) + a.log_scale : 0.5f * sq + a.log_scale;
                 // (PRF q rows: sq = 0 here, the factor left out as above)
                 const float ua = us * kLog2e, ub = sh * kLog2e;
                 const bool zero = kind == 1 && r >= nvalid;   // k rows past the end add nothing
-                // (U complete means the projection has read x)
+                // (U complete means the projection has read x: the slot's first box can take phi)
                 wait_bar(u_full, nt & 1, ctl);
                 tc_fence_after();
                 uint32_t v0[32], v1[32];
@@ -659,7 +643,6 @@ prf_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 __syncwarp();
                 if (lane == 0) mbar_arrive(u_free);
                 nt++;
-                if (need_sq) quad_pair_sync(qd);   // both exp warps of this quadrant have read x: box 0 can take phi
                 auto emit = [&](const uint32_t(&v)[32], int h) {
 #pragma unroll
                     for (int q4 = 0; q4 < 4; q4++) {
@@ -897,6 +880,39 @@ prf_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
 }
 
+// |x|^2 of every row of a [rows, 64] bf16 tensor: a warp takes 32 rows (4 KB
+// in a row) as 8 coalesced 512-byte pieces, lanes 8t .. 8t + 7 of piece i
+// holding row 4i + t, and lane l writes row l's sum.
+__global__ void prf_norm_kernel(const __nv_bfloat16 *__restrict__ x, float *__restrict__ sq, long long rows)
+{
+    const int lane = threadIdx.x % 32;
+    const long long r0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / 32 * 32;
+    if (r0 >= rows) return;
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + r0 * kD);
+    const long long n = rows - r0;
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) v[i] = 4 * i + lane / 8 < n ? __ldg(src + 32 * i + lane) : make_uint4(0, 0, 0, 0);
+    float mine = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        const uint32_t u[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+        float p = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            const float lo = __uint_as_float(u[e] << 16), hi = __uint_as_float(u[e] & 0xffff0000u);
+            p = fmaf(lo, lo, p);
+            p = fmaf(hi, hi, p);
+        }
+        p += __shfl_xor_sync(0xffffffffu, p, 1);
+        p += __shfl_xor_sync(0xffffffffu, p, 2);
+        p += __shfl_xor_sync(0xffffffffu, p, 4);
+        const float t = __shfl_sync(0xffffffffu, p, 8 * (lane % 4));   // row 4i + lane % 4
+        if (i == lane / 4) mine = t;
+    }
+    if (lane < n) sq[r0 + lane] = mine;
+}
+
 // Exclusive prefix over a (head, feature block)'s segments of the segment
 // sums, in place: slot s then holds the sums over segments 0 .. s - 1 (zero
 // for s = 0).  The last segment's own sums are never computed or read.
@@ -997,7 +1013,7 @@ PrfGeo prf_plan(long long BH, int N, int nb, int sms)
 size_t up256(size_t b) { return (b + 255) & ~(size_t)255; }
 
 struct PrfLayout {
-    size_t preS, prez, num_part, den_part, total;
+    size_t preS, prez, num_part, den_part, sqk, sqq, total;
 };
 
 PrfLayout prf_layout(const Problem &p)
@@ -1010,7 +1026,10 @@ PrfLayout prf_layout(const Problem &p)
     L.num_part = L.prez + up256(slots * kFB * 4);
     const size_t rows = g.nb > 1 ? (size_t)g.BH * g.NC * kC : 0;   // whole chunks
     L.den_part = L.num_part + up256(rows * kDV * 4);
-    L.total = L.den_part + up256(rows * 4);
+    L.sqk = L.den_part + up256(rows * 4);
+    const size_t nrows = (size_t)g.BH * g.N;
+    L.sqq = L.sqk + up256(nrows * 4);
+    L.total = L.sqq + up256(p.kind == PHI_NPRF ? nrows * 4 : 0);
     return L;
 }
 
@@ -1027,8 +1046,8 @@ cudaError_t prf_run(const Problem &p, void *scratch, float *S_out, float *z_out,
         !prf_map(&tv, p.v, p.BH, p.N, true) || !prf_map(&to, p.out, p.BH, p.N, false))
         return cudaErrorInvalidValue;
     PrfArgs a;
-    a.q = (const __nv_bfloat16 *)p.q;
-    a.k = (const __nv_bfloat16 *)p.k;
+    a.sqk = (const float *)(b + L.sqk);
+    a.sqq = (const float *)(b + L.sqq);
     a.W = p.W;
     a.preS = (float *)(b + L.preS);
     a.prez = (float *)(b + L.prez);
@@ -1046,6 +1065,12 @@ cudaError_t prf_run(const Problem &p, void *scratch, float *S_out, float *z_out,
         (NB > 1 && (e = set_max_smem_once<prf_chunk_kernel<kComb, M>>(PrfPlan<kComb, M>::SMEM)) != cudaSuccess))
         return e;
     int launches = 0;
+    const long long rows = p.BH * (long long)p.N;
+    const unsigned nblk = (unsigned)((rows + 255) / 256);
+    prf_norm_kernel<<<nblk, 256, 0, s>>>((const __nv_bfloat16 *)p.k, (float *)a.sqk, rows);
+    if (p.kind == PHI_NPRF) prf_norm_kernel<<<nblk, 256, 0, s>>>((const __nv_bfloat16 *)p.q, (float *)a.sqq, rows);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    launches += p.kind == PHI_NPRF ? 2 : 1;
     const bool seg = g.nseg > 1;
     if (seg) {
         PrfGeo ga = g;

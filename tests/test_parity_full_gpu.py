@@ -145,14 +145,14 @@ def test_long_segment_chain_prf(la, H, N, m, Dv, causal):
 
 
 def test_prf_launch_plan(la):
-    """Causal random features with D = Dv = 64 form phi on chip: with few
-    heads (segments) the segment-sum pass, the scan and one output pass per
-    128-feature block (m = 256: 4 kernels, m = 128: 3), with one segment per
-    head only the output passes (2, 1).  Non-causal m = 256 projects phi first,
-    then runs the segment-sum pass and the totals per half and one readout
-    (6 kernels)."""
-    for m, H, causal, expect in ((256, 2, True, 4), (128, 2, True, 3), (256, 160, True, 2),
-                                 (128, 160, True, 1), (256, 2, False, 6)):
+    """Causal random features with D = Dv = 64 form phi on chip: the row-norm
+    pass, then with few heads (segments) the segment-sum pass, the scan and one
+    output pass per 128-feature block (m = 256: 5 kernels, m = 128: 4), with one
+    segment per head only the output passes (3, 2).  Non-causal m = 256
+    projects phi first, then runs the segment-sum pass and the totals per half
+    and one readout (6 kernels)."""
+    for m, H, causal, expect in ((256, 2, True, 5), (128, 2, True, 4), (256, 160, True, 3),
+                                 (128, 160, True, 2), (256, 2, False, 6)):
         fm = la.FeatureMap("prf", wl.make_W(m, 64).cuda())
         w = wl.small(B=1, H=H, N=2048 if H < 100 else 256, D=64, Dv=64, feature="prf", m=m, seed=9)
         q, k, v = (t.cuda() for t in wl.make_qkv(w))
