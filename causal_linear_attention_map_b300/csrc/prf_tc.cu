@@ -15,25 +15,31 @@
 // Shapes: D = 64, Dv = 64, m = 128 or 256 features, bf16 in and out.  The
 // features are taken in blocks of 128 (a pass per block).  Sums over
 // features split exactly over blocks, so with m = 256 the first pass writes
-// its un-normalised NUM, DEN to fp32 scratch and the second adds its own and
+// its un-normalised NUM, DEN to fp32 scratch (column-major per chunk, so that
+// each warp access is 128 contiguous bytes) and the second adds its own and
 // divides.
 //
-// Passes.  As in the elu+1 kernels, each head's chunks are cut into segments
-// so that every SM has a (head, segment) item: a segment-sum pass (AGG; one
-// item per head, feature block and segment but the last) sums phi(K)^T V and
+// Passes.  A row-norm pass writes |k|^2 (NPRF: and |q|^2) of every row.
+// Then, as in the elu+1 kernels, each head's chunks are cut into segments so
+// that every SM has a (head, segment) item: a segment-sum pass (AGG; one item
+// per head, feature block and segment but the last) sums phi(K)^T V and
 // colsum phi(K) over a segment, a scan turns those into exclusive prefixes
 // over segments, and the output pass starts each segment from its prefix.
 // Items are assigned statically: CTA b takes items b, b + grid, ...
+//
+// A q row's PRF factor exp(-|q|^2 / 2) multiplies every feature of the row
+// and cancels between phi(q)^T S and phi(q)^T z, so the q tiles leave it out
+// (NPRF normalises u by |x|, which is no such factor, and keeps it).
 //
 // Per tile of 128 rows of q or k (x, one 64-column box), on chip:
 //   U      = X W_blk^T       tcgen05, M = 128 rows, N = 128 features, K = 64,
 //                            W as bf16 hi + lo (W_hi = bf16(W),
 //                            W_lo = bf16(W - W_hi), both products into one
 //                            fp32 accumulator), into a 128-column TMEM buffer
-//   phi    = exp(U - s)      exp warps: U from TMEM, |x|^2 from the tile,
-//                            bf16 phi written over the tile's shared-memory
-//                            slot (x sits in the slot's first box; both warps
-//                            of a lane quadrant read x before either writes)
+//   phi    = exp(U - s)      exp warps: U from TMEM, |x|^2 from the norm
+//                            pass, bf16 phi written over the tile's
+//                            shared-memory slot (x sits in the slot's first
+//                            box and is dead once U is complete)
 // Per chunk (output pass), tcgen05.mma kind::f16, fp32 accumulation in TMEM:
 //   MMA1   A         = phiQ . phiK^T               N = 128, K = 128
 //   MMA3   NUM | DEN = phiQ . [S_prev | ZP]        N = 80,  K = 128
@@ -48,22 +54,23 @@
 // P [320, 384), U [384, 512).  A and NUM have regions of their own, so MMA1
 // of the next chunk needs only the masked P of this one, and MMA3 only the
 // epilogue of the previous one.  The segment-sum form keeps two S | z
-// regions (0 and 96) that alternate between items.
+// regions (0 and 96) that alternate between items.  Rings: two chunks deep
+// in the output passes, three in the segment-sum pass.
 //
-// Warp roles (19 warps):
+// Warp roles (20 warps, five per SM sub-partition: 96 registers):
 //   warps 0-7    exp warps: warp w owns TMEM lane quadrant w % 4 (tile rows
 //                32 (w % 4) ..) and features 64 (w / 4) .. of each U
 //   warps 8-15   TMEM warps, lane quadrant w % 4, column half (w - 8) / 4:
 //                the segment's prefix, S_prev | ZP, the masked P, the
 //                epilogue (and the state export); in the segment-sum form
 //                the segment's sums to scratch
-//   warp 16      TMA producer of the q and k tiles
+//   warp 16      TMA producer of the q and k tiles (L2 prefetch two chunks ahead)
 //   warp 17      lane 0: TMA producer of the V tiles; lane 1: TMA store of
 //                the output tiles (staged in the V slot, dead after MMA2)
-//   warp 18      MMA issuer (one thread)
-// Issue order per chunk j: U(Q(j+1)), MMA3(j), MMA4(j), U(K(j+1)), MMA2(j),
-// MMA1(j+1): the next chunk's projections and exps run while this chunk's
-// products do.
+//   warp 18      chunk MMA issuer: MMA3(j), MMA4(j), MMA2(j), MMA1(j + 1)
+//   warp 19      projection issuer: U of every tile as soon as it has landed
+//                and the exp warps have read the previous U, so that the next
+//                chunk's projections and exps run while this chunk's products do
 //
 // Every wait is bounded (clock64 budget); on expiry the kernel sets the
 // library's error word and the CTA runs to its end without waiting.
