@@ -218,6 +218,14 @@ __device__ __forceinline__ float ex2_approx(float x)
     return y;
 }
 
+// One 32-bit TMEM column of this thread's lane (no wait).
+__device__ __forceinline__ uint32_t tmem_ld1_nowait(uint32_t taddr)
+{
+    uint32_t r;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+    return r;
+}
+
 // 32 fp32 state values -> bf16 at row r, columns [c0, c0 + 32) of the
 // MN-major S_prev operand in 32-byte swizzle (16-column blocks kFB * 32 bytes apart).
 __device__ __forceinline__ void sprev_store32(uint32_t st, int r, int c0, const uint32_t (&v)[32])
@@ -615,20 +623,30 @@ prf_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
         constexpr float kLog2e = 1.4426950408889634f;
         uint32_t nt = 0;   // projections consumed
+        // |x|^2 of row r of a chunk's k (and, for NPRF, q) tile, from the norm
+        // pass, loaded a chunk ahead of its use.  A q row's PRF factor
+        // exp(-|q|^2 / 2) multiplies every feature of that row, so it cancels
+        // between the numerator phi(q)^T S and the denominator phi(q)^T z: PRF
+        // q tiles leave it out (NPRF's u / |x| is no such factor)
+        auto load_sq = [&](const Walk<AGG> &p, float &k2, float &q2) {
+            const long long grow = (long long)p.it.bh * g.N + p.row0() + r;
+            const bool in = r < g.N - p.row0();
+            k2 = in ? __ldcg(a.sqk + grow) : 0.f;
+            q2 = in && a.normalize && !AGG ? __ldcg(a.sqq + grow) : 0.f;
+        };
         Walk<AGG> w;
         w.start(g);
+        float nsq_k = 0.f, nsq_q = 0.f;
+        if (w.valid) load_sq(w, nsq_k, nsq_q);
         for (uint32_t j = 0; w.valid; j++, w.advance(g)) {
             const int sl = j % NS;
             const int nvalid = g.N - w.row0();   // rows of this chunk inside the sequence
-            // |x|^2 of row r of this chunk's k (and, for NPRF, q) tile, from the
-            // norm pass: loaded now, used once the tile's U is ready.  A q row's
-            // PRF factor exp(-|q|^2 / 2) multiplies every feature of that row, so
-            // it cancels between the numerator phi(q)^T S and the denominator
-            // phi(q)^T z: PRF q tiles leave it out (NPRF's u / |x| is no such factor)
-            const long long grow = (long long)w.it.bh * g.N + w.row0() + r;
-            const bool in = r < nvalid;
-            const float sq_k = in ? __ldcg(a.sqk + grow) : 0.f;
-            const float sq_q = in && a.normalize && !AGG ? __ldcg(a.sqq + grow) : 0.f;
+            const float sq_k = nsq_k, sq_q = nsq_q;
+            {
+                Walk<AGG> nx = w;
+                nx.advance(g);
+                if (nx.valid) load_sq(nx, nsq_k, nsq_q);
+            }
 #pragma unroll 1
             for (int kind = AGG ? 1 : 0; kind < 2; kind++) {
                 const uint32_t t = base + (kind == 0 ? PL::Q0 : PL::K0) + sl * PL::PB;
@@ -729,8 +747,9 @@ prf_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             auto epilogue = [&](uint32_t jj, int bh, int row0) {
                 wait_bar(num_full, jj & 1, ctl);
                 tc_fence_after();
-                uint32_t d[16], n[32];
-                tmem_ld16_nowait(tmem + lane_base + T_N + kDV, d);
+                uint32_t n[32];
+                const uint32_t d0 = tmem_ld1_nowait(tmem + lane_base + T_N + kDV);       // phiQ z_prev hi + rowsum P
+                const uint32_t d8 = tmem_ld1_nowait(tmem + lane_base + T_N + kDV + 8);   // phiQ z_prev lo
                 tmem_ld32_nowait(tmem + lane_base + T_N + grp * 32, n);
                 tmem_ld_wait();
                 tc_fence_before();
@@ -740,7 +759,7 @@ prf_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 // fp32, so that a warp's access to one column is 128 contiguous bytes
                 const long long cid = (long long)bh * g.NC + row0 / kC;
                 float *part = a.num_part + cid * (kDV * kC) + (long long)(grp * 32) * kC + r;
-                float den = __uint_as_float(d[0]) + __uint_as_float(d[8]);
+                float den = __uint_as_float(d0) + __uint_as_float(d8);
                 float o[32];
 #pragma unroll
                 for (int i = 0; i < 32; i++) o[i] = __uint_as_float(n[i]);
@@ -827,27 +846,26 @@ prf_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 // the epilogue waited for MMA2(j - 1))
                 wait_bar(a_full, j & 1, ctl);
                 tc_fence_after();
-                uint32_t a0[32], a1[32];
-                tmem_ld32_nowait(tmem + lane_base + T_A + grp * 64, a0);
-                tmem_ld32_nowait(tmem + lane_base + T_A + grp * 64 + 32, a1);
-                tmem_ld_wait();
+                // (in two halves of 32 keys, which keeps the P step within the registers)
+                uint32_t pk[32];
+                const int cb = grp * 64;
+#pragma unroll
+                for (int hh = 0; hh < 2; hh++) {
+                    uint32_t av[32];
+                    tmem_ld32_nowait(tmem + lane_base + T_A + cb + 32 * hh, av);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; i++) {
+                        const int col = cb + 32 * hh + 2 * i;
+                        pk[16 * hh + i] = pack_bf16x2(col <= r ? __uint_as_float(av[2 * i]) : 0.f,
+                                                      col + 1 <= r ? __uint_as_float(av[2 * i + 1]) : 0.f);
+                    }
+                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(a_free);
-                {
-                    uint32_t pk[32];
-                    const int cb = grp * 64;
-#pragma unroll
-                    for (int i = 0; i < 16; i++) {
-                        const int col = cb + 2 * i;
-                        pk[i] = pack_bf16x2(col <= r ? __uint_as_float(a0[2 * i]) : 0.f,
-                                            col + 1 <= r ? __uint_as_float(a0[2 * i + 1]) : 0.f);
-                        pk[16 + i] = pack_bf16x2(col + 32 <= r ? __uint_as_float(a1[2 * i]) : 0.f,
-                                                 col + 33 <= r ? __uint_as_float(a1[2 * i + 1]) : 0.f);
-                    }
-                    tmem_st32_nowait(tmem + lane_base + T_P + grp * 32, pk);
-                    tmem_st_wait();
-                }
+                tmem_st32_nowait(tmem + lane_base + T_P + grp * 32, pk);
+                tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(p_ready);
