@@ -2,16 +2,17 @@
 cannot allocate device memory (allocator hooks, memory-budgeted embedders,
 real-time paths).  Its scratch is a fixed device array shared by all calls.
 
-Checked through the C ABI against la_forward (causal = 0) on the same
-inputs, on two calls in a row with different inputs, so that a stale
-accumulator left by the first call would show up in the second.  This file
-is named to be collected last.
+Checked through the C ABI against the fp64 oracle (and la_forward,
+causal = 0) on the same inputs, on two calls in a row with different
+inputs, so that a stale accumulator left by the first call would show up in
+the second.  This file is named to be collected last.
 """
 import ctypes
 
 import pytest
 import torch
 
+import oracle
 import workloads as wl
 from parity_util import assert_close, np64
 
@@ -34,7 +35,7 @@ def _noalloc(la, q, k, v, out, fm_struct, dtype_code):
     ((1, 3, 300, 32, 16), "f32", "elu1", 0),
     ((1, 2, 513, 64, 64), "bf16", "prf", 128),
 ])
-def test_noalloc_matches_la_forward_twice(la, shape, dtype, feature, m):
+def test_noalloc_matches_the_oracle_twice(la, shape, dtype, feature, m):
     B, H, N, D, Dv = shape
     W = wl.make_W(m, D).cuda() if feature == "prf" else None
     fm = la.FeatureMap("prf", W) if W is not None else la.FeatureMap()
@@ -48,13 +49,16 @@ def test_noalloc_matches_la_forward_twice(la, shape, dtype, feature, m):
         st = _noalloc(la, q, k, v, out, fm.c_struct(), code)
         assert st == la.LA_OK, la.la_status_string(st)
         torch.cuda.synchronize()
-        assert_close(np64(out), np64(ref), dtype, what=f"call {call}")
+        exact = oracle.forward(np64(q), np64(k), np64(v), causal=False, feature=feature,
+                               W=W.double().cpu().numpy() if W is not None else None)
+        assert_close(np64(out), exact, dtype, what=f"call {call} against the oracle")
+        assert_close(np64(out), np64(ref), dtype, what=f"call {call} against la_forward")
 
 
 def test_noalloc_accepts_the_largest_problem_that_fits(la):
     """B*H*Dphi*(Dv+1)*4 bytes: 63 heads x 128 x 129 x 4 = 4,161,024 B, the
     largest elu+1 D = Dv = 128 problem under the 4 MiB limit (64 heads is
-    over it: the next test); results checked against la_forward."""
+    over it: the next test); results checked against the oracle and la_forward."""
     w = wl.small(B=1, H=63, N=300, D=128, Dv=128, causal=False, seed=77)
     q, k, v = (t.cuda() for t in wl.make_qkv(w))
     assert 63 * 128 * 129 * 4 <= la.LA_NOALLOC_SCRATCH_BYTES < 64 * 128 * 129 * 4
@@ -63,7 +67,9 @@ def test_noalloc_accepts_the_largest_problem_that_fits(la):
     st = _noalloc(la, q, k, v, out, la.FeatureMap().c_struct(), la.LA_BF16)
     assert st == la.LA_OK, la.la_status_string(st)
     torch.cuda.synchronize()
-    assert_close(np64(out), np64(ref), "bf16", what="63 heads")
+    assert_close(np64(out), oracle.forward(np64(q), np64(k), np64(v), causal=False), "bf16",
+                 what="63 heads against the oracle")
+    assert_close(np64(out), np64(ref), "bf16", what="63 heads against la_forward")
 
 
 def test_noalloc_steady_state_calls_allocate_nothing(la):
