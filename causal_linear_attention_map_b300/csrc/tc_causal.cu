@@ -1081,7 +1081,10 @@ struct NcPlan {
     static constexpr int SB = DP * NQ16 * 2;
     static constexpr int ZB = 0;
     static constexpr int NO = 2;
-    static constexpr int kBudget = 227 * 1024 - 2048;
+    // D = Dv = 64: two CTAs per SM (half the shared memory and TMEM each), so
+    // that one CTA's per-chunk chain overlaps the other's; else one per SM
+    static constexpr bool kTwo = DP == 64 && DV == 64;
+    static constexpr int kBudget = kTwo ? 113 * 1024 - 2048 : 227 * 1024 - 2048;
     static constexpr int NQ0 = (kBudget - NO * OB - SB - ZB) / QB;
     static constexpr int NQ = NQ0 > 6 ? 6 : NQ0;   // Q ring depth: what fits, at most 6
     static_assert(NQ >= 2, "Q ring too shallow");
@@ -1094,13 +1097,14 @@ struct NcPlan {
     // TMEM: region r at column RS r holds NUM | DEN (DV + 16 columns)
     static constexpr int RS = NQ16 > kC ? NQ16 : kC;
     static constexpr bool ALN32 = RS % 32 == 0;
-    static constexpr int TMEM_COLS = 512;
+    static constexpr int TMEM_COLS = kTwo ? 256 : 512;
     static_assert(SMEM <= 227 * 1024, "shared memory plan too large");
-    static_assert(SMEM > 114 * 1024, "one CTA per SM: the kernel holds all 512 TMEM columns");
+    static_assert(kTwo ? SMEM <= 113 * 1024 && 2 * RS <= TMEM_COLS
+                       : SMEM > 114 * 1024, "CTAs per SM: shared memory and TMEM shares disagree");
 };
 
 template <int DP, int DV, bool PHI>
-__global__ void __launch_bounds__(kNcThreads, 1)
+__global__ void __launch_bounds__(kNcThreads, NcPlan<DP, DV>::kTwo ? 2 : 1)
 nc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o, Geo g,
               Scratch sc, int *err)
 {
@@ -1926,11 +1930,21 @@ cudaError_t run_readout(const CUtensorMap &tq, const CUtensorMap &to, Geo g, voi
         sc.exz = z_out;
     }
     sc.ticket = (int *)((unsigned char *)scratch + 8);   // cleared with the header by run_totals
+    // Items of the readout: its own segments (it needs only the per-head
+    // totals); with two CTAs per SM, enough of them to give every CTA slot one
+    int slots = num_sms();
+    if constexpr (NP::kTwo) {
+        slots *= 2;
+        const int want = g.BH >= slots ? 1 : slots / g.BH;
+        g.L = cdiv(g.NC, max(1, min(want, g.NC)));
+        g.nseg = cdiv(g.NC, g.L);
+        g.n_items = g.BH * g.nseg;
+    }
     cudaError_t e;
     if ((e = set_max_smem_once<nc_out_kernel<DP, DV, PHI>>(NP::SMEM)) != cudaSuccess)
         return e;
     // (after the totals kernel: a dependent launch that waits for it before reading S, z)
-    if ((e = launch_dependent(nc_out_kernel<DP, DV, PHI>, dim3(min(g.n_items, num_sms())), dim3(kNcThreads),
+    if ((e = launch_dependent(nc_out_kernel<DP, DV, PHI>, dim3(min(g.n_items, slots)), dim3(kNcThreads),
                               NP::SMEM, s, tq, to, g, sc, err)) != cudaSuccess)
         return e;
     note_launches(1);
