@@ -124,6 +124,11 @@ struct Plan {
     // buffer: its K and V rings take the space (three stages at D = Dv = 128
     // instead of two)
     static constexpr bool kSumOnly = DP > 128 || SUMF;
+    // The segment-sum form at D = Dv = 64 takes V in 32-byte swizzle like the
+    // output form, so that one N = Dv + 16 product per K step with the ONES
+    // block gives S and z (else one N = Dv and one N = 16 product): its chunks
+    // are bound by the issue of their products
+    static constexpr bool kV32Agg = SUMF && DP == 64 && DV == 64;
     // S_prev pieces along Dphi: one, or two 64-row halves when that is what
     // lets two-deep rings fit (each piece with its own z block)
     static constexpr int NSP = kSumOnly || (2 * (2 * QB + VB) + DP * NQ16 * 2 <= kBudget) ? 1 : 2;
@@ -419,7 +424,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // boxes per tile, their width and stride: V of the output form in 16-column
             // boxes (32-byte swizzle); Q, K and the segment-sum form's V in 64-column
             // boxes (128-byte swizzle: fewer, longer rows per TMA request)
-            constexpr bool kV32 = !AGG;
+            constexpr bool kV32 = !AGG || PL::kV32Agg;
             const int nb = role == 2 ? (kV32 ? DV / 16 : DV / 64) : DP / 64;
             const int bw = role == 2 && kV32 ? 16 : 64;
             const int bs = role == 2 && kV32 ? kC * 32 : kC * 128;
@@ -579,7 +584,15 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         tc_fence_after();
                         const uint32_t ka = base + PL::K0 + st * PL::QB;
                         const uint32_t va = base + PL::V0 + st * PL::VB;
-                        if (!*abort_cta) {
+                        if (!*abort_cta && PL::kV32Agg) {
+                            // S | z += phiK^T [V | ONES]: V in 32-byte swizzle, ONES its last block
+                            constexpr uint32_t id_kv = idesc_bf16(128, PL::NQ16, 1, 1);
+#pragma unroll
+                            for (int k = 0; k < kC; k += 16)
+                                mma_bf16_ss(dS, sw128_desc(ka + (k / 8) * 1024, lbo_kT, 1024),
+                                            sw32_desc(va + (k / 8) * 256, kC * 32, 256), id_kv,
+                                            (c > 0 || k > 0) ? 1u : 0u);
+                        } else if (!*abort_cta) {
                             // (V in 128-byte swizzle here; z from the slot's ONES block)
                             constexpr uint32_t id_s = idesc_bf16(128, DV, 1, 1);
                             constexpr uint32_t id_z = idesc_bf16(128, 16, 1, 1);
@@ -1859,7 +1872,8 @@ cudaError_t run_causal(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
         Geo ga = g;
         ga.n_items = g.BH * (g.nseg - 1);
         tc_causal_kernel<DP, DV, true, AMODE><<<min(ga.n_items, sms), kThreads, Plan<DP, DV, true>::SMEM, s>>>(
-            tq, tk, tv_agg, to, ga, sc, (__nv_bfloat16 *)out, nullptr, nullptr, err);
+            tq, tk, Plan<DP, DV, true>::kV32Agg ? tv : tv_agg, to, ga, sc, (__nv_bfloat16 *)out, nullptr, nullptr,
+            err);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         const int sz = DP * DV + DP;
         if ((e = launch_dependent(seg_scan_kernel, dim3(cdiv(sz, 256), (unsigned)g.BH), dim3(256), 0, s, sc.preS,
@@ -1987,11 +2001,13 @@ cudaError_t run_elu(const Problem &p, void *scratch, float *S_out, float *z_out,
     float *totz = totS + (size_t)g.BH * DP * DV;
     if (g.nseg <= kNcFoldSegs) {
         // few segments per head: the readout adds them up (no totals kernel)
-        cudaError_t e = run_totals<DP, DV, kModeElu>(tq, tk, tva, to, g, scratch, totS, totz, DP, 0, err, s, false);
+        cudaError_t e = run_totals<DP, DV, kModeElu>(tq, tk, Plan<DP, DV, true>::kV32Agg ? tv : tva, to, g, scratch,
+                                                     totS, totz, DP, 0, err, s, false);
         if (e == cudaSuccess) e = run_readout<DP, DV, true>(tq, to, g, scratch, nullptr, nullptr, err, s, S_out, z_out);
         return e;
     }
-    cudaError_t e = run_totals<DP, DV, kModeElu>(tq, tk, tva, to, g, scratch, totS, totz, DP, 0, err, s);
+    cudaError_t e = run_totals<DP, DV, kModeElu>(tq, tk, Plan<DP, DV, true>::kV32Agg ? tv : tva, to, g, scratch,
+                                                 totS, totz, DP, 0, err, s);
     if (e == cudaSuccess) e = run_readout<DP, DV, true>(tq, to, g, scratch, totS, totz, err, s);
     if (e == cudaSuccess) e = export_totals(S_out, z_out, totS, totz, g.BH, DP, DV, s);
     return e;
