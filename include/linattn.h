@@ -47,13 +47,16 @@
  *    m <= 128 (else LA_ERR_FEATURE); Dphi * Dv <= 32768.
  *  - Execution: bf16 inputs with elu+1 and D, Dv in {64, 128}, or with PRF or
  *    NPRF, D = 64 and (m = 128, Dv in {64, 128}) or (m = 256, Dv = 64), run on
- *    the tensor cores (tcgen05); every other supported case (fp32, TRF, other
- *    sizes) runs on the CUDA cores.  Both compute the same sums; rounding
- *    differs.
+ *    the tensor cores (tcgen05); causal PRF / NPRF with D = Dv = 64 form
+ *    phi(q), phi(k) inside the chunk kernels, the other random-feature cases
+ *    write them to scratch first; every other supported case (fp32, TRF,
+ *    other sizes) runs on the CUDA cores.  All compute the same sums;
+ *    rounding differs.
  *  - Scratch: la_forward may take stream-ordered scratch memory from a
  *    library-owned CUDA memory pool on the current device (per-segment
- *    states of the causal scan, partial sums of the non-causal pass, the
- *    phi(q), phi(k) tiles of random features); it is returned to the pool,
+ *    states of the causal scan, partial sums of the non-causal pass, row
+ *    norms and block partial sums of random features formed on chip, the
+ *    phi(q), phi(k) tiles of the other random-feature cases); it is returned to the pool,
  *    in stream order, before the call returns.  la_shutdown() releases the
  *    pools.
  */
