@@ -66,9 +66,11 @@ __host__ __device__ inline BwdSmem bwd_layout(const BwdGeo &g, bool dq_pass)
 
 // phi of rows [t0, t0 + n) of a head's [N, D] block into f [C, P]; rows
 // n..C-1 are zero.  PRF: |x|^2 into sq, and the raw rows into X (if given).
+// Wt is W transposed ([D, m]): the threads of a warp take consecutive
+// features, so their reads of it are consecutive.
 template <typename T>
 __device__ void phi_rows(const T *__restrict__ x, int t0, int n, const BwdGeo &g,
-                         const float *__restrict__ W, float *f, float *sq, float *X)
+                         const float *__restrict__ Wt, float *f, float *sq, float *X)
 {
     const int C = g.C, D = g.D, P = g.P;
     if (g.kind == PHI_ELU1) {
@@ -94,9 +96,9 @@ __device__ void phi_rows(const T *__restrict__ x, int t0, int n, const BwdGeo &g
         const int i = idx / P, r = idx % P;
         float val = 0.f;
         if (i < n) {
-            const float *wr = W + (long long)rf_proj(g.kind, r, m) * D;
+            const float *wc = Wt + rf_proj(g.kind, r, m);
             float u = 0.f;
-            for (int d = 0; d < D; d++) u = fmaf(wr[d], X[i * D + d], u);
+            for (int d = 0; d < D; d++) u = fmaf(wc[(long long)d * m], X[i * D + d], u);
             val = rf_value(g.kind, r, m, u, sq[i]);
         }
         f[idx] = val;
@@ -196,7 +198,7 @@ __device__ void accum_outer(float *acc, float *acc1, const float *X, const float
 // ---- pass 1: per-segment sums of S = phi(K)^T V and z = colsum phi(K)
 template <typename T>
 __global__ void __launch_bounds__(kBT)
-bwd_sums_kernel(const T *__restrict__ k, const T *__restrict__ v, const float *__restrict__ W, BwdGeo g,
+bwd_sums_kernel(const T *__restrict__ k, const T *__restrict__ v, const float *__restrict__ Wt, BwdGeo g,
                 float *__restrict__ stS)
 {
     extern __shared__ float sm[];
@@ -211,7 +213,7 @@ bwd_sums_kernel(const T *__restrict__ k, const T *__restrict__ v, const float *_
     for (int c = c0; c < c1; c++) {
         const int t0 = c * C, n = min(C, g.N - t0);
         __syncthreads();
-        phi_rows(kh, t0, n, g, W, F, sq, X);
+        phi_rows(kh, t0, n, g, Wt, F, sq, X);
         load_rows(vh, t0, n, C, Dv, V);
         __syncthreads();
         accum_outer(acc, acc1, F, V, nullptr, n, P, Dv, Dv);
@@ -261,7 +263,7 @@ __global__ void bwd_scan_kernel(float *__restrict__ st, int nseg, int elems, int
 template <typename T>
 __global__ void __launch_bounds__(kBT)
 bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
-              const T *__restrict__ dout, const float *__restrict__ W, BwdGeo g,
+              const T *__restrict__ dout, const float *__restrict__ W, const float *__restrict__ Wt, BwdGeo g,
               const float *__restrict__ stS, float *__restrict__ stR, float *__restrict__ den_out,
               float *__restrict__ dd_out, T *__restrict__ dq)
 {
@@ -290,11 +292,11 @@ bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     for (int c = c0; c < c1; c++) {
         const int t0 = c * C, n = min(C, g.N - t0);
         __syncthreads();
-        if (g.causal) phi_rows(kh, t0, n, g, W, F, sq, X);
+        if (g.causal) phi_rows(kh, t0, n, g, Wt, F, sq, X);
         load_rows(vh, t0, n, C, Dv, V);
         load_rows(oh, t0, n, C, Dv, O);
         __syncthreads();
-        phi_rows(qh, t0, n, g, W, G, sq, X);   // (X keeps the raw q rows for the chain rule)
+        phi_rows(qh, t0, n, g, Wt, G, sq, X);   // (X keeps the raw q rows for the chain rule)
         __syncthreads();
         if (g.causal)
             for (int idx = threadIdx.x; idx < C * C; idx += blockDim.x) {
@@ -371,7 +373,7 @@ bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
 template <typename T>
 __global__ void __launch_bounds__(kBT)
 bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
-                const T *__restrict__ dout, const float *__restrict__ W, BwdGeo g,
+                const T *__restrict__ dout, const float *__restrict__ W, const float *__restrict__ Wt, BwdGeo g,
                 const float *__restrict__ stR, const float *__restrict__ den_in,
                 const float *__restrict__ dd_in, T *__restrict__ dk, T *__restrict__ dv)
 {
@@ -394,7 +396,7 @@ bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__res
     for (int c = c1 - 1; c >= c0; c--) {
         const int t0 = c * C, n = min(C, g.N - t0);
         __syncthreads();
-        phi_rows(qh, t0, n, g, W, G, sq, X);
+        phi_rows(qh, t0, n, g, Wt, G, sq, X);
         load_rows(vh, t0, n, C, Dv, V);
         load_rows(oh, t0, n, C, Dv, Mn);
         for (int i = threadIdx.x; i < C; i += blockDim.x) {
@@ -402,7 +404,7 @@ bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__res
             dd[i] = i < n ? dd_in[(long long)h * g.N + t0 + i] : 0.f;
         }
         __syncthreads();
-        phi_rows(kh, t0, n, g, W, F, sq, X);   // (X keeps the raw k rows for the chain rule)
+        phi_rows(kh, t0, n, g, Wt, F, sq, X);   // (X keeps the raw k rows for the chain rule)
         for (int idx = threadIdx.x; idx < C * Dv; idx += blockDim.x) Mn[idx] /= den[idx / Dv];
         __syncthreads();
         if (g.causal)
@@ -442,6 +444,13 @@ bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__res
     }
 }
 
+// W [m, D] -> Wt [D, m]
+__global__ void bwd_wt_kernel(const float *__restrict__ W, float *__restrict__ Wt, int m, int D)
+{
+    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx < m * D) Wt[(long long)(idx % D) * m + idx / D] = W[idx];
+}
+
 BwdGeo bwd_plan(const Problem &p, bool causal, int sms)
 {
     BwdGeo g;
@@ -476,6 +485,7 @@ cudaError_t launch_backward(const Problem &p, const void *dout, void *dq, void *
     float *stR = stS + (size_t)g.BH * g.nseg * elems;
     float *den = stR + (size_t)g.BH * g.nseg * elems;
     float *dd = den + (size_t)g.BH * g.N;
+    float *Wt = dd + (size_t)g.BH * g.N;   // random features: W transposed
     const size_t sm_sum = ((size_t)elems + (size_t)g.C * (g.P + g.Dv + 1 + g.D)) * sizeof(float);
     const size_t sm_dq = bwd_layout(g, true).total, sm_dkdv = bwd_layout(g, false).total;
     if (sm_dq > 227 * 1024 || sm_sum > 227 * 1024) return cudaErrorInvalidValue;
@@ -486,13 +496,15 @@ cudaError_t launch_backward(const Problem &p, const void *dout, void *dq, void *
     const unsigned items = (unsigned)(g.BH * g.nseg);
     const dim3 sgrid((unsigned)cdiv(elems, kBT), (unsigned)g.BH);
     const T *q = (const T *)p.q, *k = (const T *)p.k, *v = (const T *)p.v, *o = (const T *)dout;
-    bwd_sums_kernel<T><<<items, kBT, sm_sum, st>>>(k, v, p.W, g, stS);
+    const int m = p.kind == PHI_ELU1 ? 0 : rf_m(p.kind, p.P);
+    if (m > 0) bwd_wt_kernel<<<cdiv(m * g.D, kBT), kBT, 0, st>>>(p.W, Wt, m, g.D);
+    bwd_sums_kernel<T><<<items, kBT, sm_sum, st>>>(k, v, Wt, g, stS);
     bwd_scan_kernel<<<sgrid, kBT, 0, st>>>(stS, g.nseg, elems, causal ? 0 : 2);
-    bwd_dq_kernel<T><<<items, kBT, sm_dq, st>>>(q, k, v, o, p.W, g, stS, stR, den, dd, (T *)dq);
+    bwd_dq_kernel<T><<<items, kBT, sm_dq, st>>>(q, k, v, o, p.W, Wt, g, stS, stR, den, dd, (T *)dq);
     bwd_scan_kernel<<<sgrid, kBT, 0, st>>>(stR, g.nseg, elems, causal ? 1 : 2);
-    bwd_dkdv_kernel<T><<<items, kBT, sm_dkdv, st>>>(q, k, v, o, p.W, g, stR, den, dd, (T *)dk, (T *)dv);
+    bwd_dkdv_kernel<T><<<items, kBT, sm_dkdv, st>>>(q, k, v, o, p.W, Wt, g, stR, den, dd, (T *)dk, (T *)dv);
     e = cudaGetLastError();
-    if (e == cudaSuccess) note_launches(5);
+    if (e == cudaSuccess) note_launches(m > 0 ? 6 : 5);
     return e;
 }
 
@@ -516,7 +528,8 @@ size_t backward_scratch_bytes(const Problem &p, bool causal)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const BwdGeo g = bwd_plan(p, causal, sms);
     const size_t elems = (size_t)g.P * g.Dv + g.P;
-    return (2 * (size_t)g.BH * g.nseg * elems + 2 * (size_t)g.BH * g.N) * sizeof(float);
+    const size_t wt = p.kind == PHI_ELU1 ? 0 : (size_t)rf_m(p.kind, p.P) * p.D;   // W transposed
+    return (2 * (size_t)g.BH * g.nseg * elems + 2 * (size_t)g.BH * g.N + wt) * sizeof(float);
 }
 
 cudaError_t backward(const Problem &p, const void *dout, void *dq, void *dk, void *dv, bool causal,
