@@ -464,8 +464,9 @@ BwdGeo bwd_plan(const Problem &p, bool causal, int sms)
     g.causal = causal ? 1 : 0;
     g.C = p.P * p.Dv > 4096 || p.P > 128 ? 16 : 32;
     g.NC = cdiv(p.N, g.C);
-    // about two items per SM; fewer, longer segments when the heads alone fill the GPU
-    const long long want = (2LL * sms + p.BH - 1) / p.BH;
+    // at most two items per SM (one CTA fits an SM at a time: two waves, no
+    // third one); fewer, longer segments when the heads alone fill the GPU
+    const long long want = (2LL * sms) / p.BH;
     const int nseg = (int)(want < 1 ? 1 : want > g.NC ? g.NC : want);
     g.L = cdiv(g.NC, nseg);
     g.nseg = cdiv(g.NC, g.L);
