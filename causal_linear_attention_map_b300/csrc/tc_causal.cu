@@ -124,17 +124,20 @@ struct Plan {
     // buffer: its K and V rings take the space (three stages at D = Dv = 128
     // instead of two)
     static constexpr bool kSumOnly = DP > 128 || SUMF;
-    // The segment-sum form at D = Dv = 64 takes V in 32-byte swizzle like the
-    // output form, so that one N = Dv + 16 product per K step with the ONES
-    // block gives S and z (else one N = Dv and one N = 16 product): its chunks
-    // are bound by the issue of their products
-    static constexpr bool kV32Agg = SUMF && DP == 64 && DV == 64;
+    // The segment-sum form at D = Dv = 64 issues one N = Dv + 16 product per K
+    // step (else one N = Dv and one N = 16 product; its chunks are bound by
+    // the issue of their products): V stays one 128-byte-swizzled 64-column
+    // box (one TMA request per tile) and a shared ONES block in the same
+    // layout is the operand's second 64-column block (its first 16 columns
+    // read), reached through the descriptor's block stride
+    static constexpr bool kOnesAgg = SUMF && DP == 64 && DV == 64;
+    static constexpr int OB128 = kOnesAgg ? kC * 128 : 0;   // the shared ONES block
     // S_prev pieces along Dphi: one, or two 64-row halves when that is what
     // lets two-deep rings fit (each piece with its own z block)
     static constexpr int NSP = kSumOnly || (2 * (2 * QB + VB) + DP * NQ16 * 2 <= kBudget) ? 1 : 2;
     static constexpr int PR = DP / NSP;      // S_prev rows per piece
     static constexpr int SB = kSumOnly ? 0 : PR * NQ16 * 2;
-    static constexpr int kFixed = SB;
+    static constexpr int kFixed = SB + OB128;
     static constexpr int STAGE = (kSumOnly ? 1 : 2) * QB + VB;   // ring bytes per stage
     static constexpr int NS = (kFixed + 4 * STAGE <= kBudget)   ? 4
                               : (kFixed + 3 * STAGE <= kBudget) ? 3
@@ -143,7 +146,8 @@ struct Plan {
     static constexpr int Q0 = 0;
     static constexpr int K0 = Q0 + (kSumOnly ? 0 : NS * QB);
     static constexpr int V0 = K0 + NS * QB;
-    static constexpr int S0 = V0 + NS * VB;   // S_prev (and its z block)
+    static constexpr int ONES0 = V0 + NS * VB;   // segment-sum form at D = Dv = 64: the shared ONES block
+    static constexpr int S0 = ONES0 + OB128;      // S_prev (and its z block)
     static constexpr int TILES = S0 + SB;
     static constexpr int SMEM = TILES + 1024 /* alignment */ + 1024 /* barriers */;
     // TMEM columns: state S | z; the regions R0, R1 (A, then NUM | DEN of
@@ -396,7 +400,14 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         *abort_cta = 0;
         fence_mbar_init();
     }
-    if (warp < kTmemWarps) {   // the ONES block after every V slot's DV / 16 blocks (never loaded over)
+    if (warp < kTmemWarps && PL::kOnesAgg) {   // the shared ONES block: columns 0-7 one, the rest zero
+        const uint32_t one = pack_bf16x2(1.f, 1.f);
+        for (int i = threadIdx.x; i < kC * 8; i += kTmemWarps * 32) {
+            const int r = i / 8, c = i % 8;
+            sts128(base + PL::ONES0 + sw128_off(r, c), c == 0 ? make_uint4(one, one, one, one) : make_uint4(0, 0, 0, 0));
+        }
+        fence_proxy_async_smem();
+    } else if (warp < kTmemWarps) {   // the ONES block after every V slot's DV / 16 blocks (never loaded over)
         const uint32_t one = pack_bf16x2(1.f, 1.f);
         for (int i = threadIdx.x; i < NS * kC; i += kTmemWarps * 32) {
             const int st = i / kC, r = i % kC;
@@ -424,7 +435,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // boxes per tile, their width and stride: V of the output form in 16-column
             // boxes (32-byte swizzle); Q, K and the segment-sum form's V in 64-column
             // boxes (128-byte swizzle: fewer, longer rows per TMA request)
-            constexpr bool kV32 = !AGG || PL::kV32Agg;
+            constexpr bool kV32 = !AGG;
             const int nb = role == 2 ? (kV32 ? DV / 16 : DV / 64) : DP / 64;
             const int bw = role == 2 && kV32 ? 16 : 64;
             const int bs = role == 2 && kV32 ? kC * 32 : kC * 128;
@@ -584,13 +595,15 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         tc_fence_after();
                         const uint32_t ka = base + PL::K0 + st * PL::QB;
                         const uint32_t va = base + PL::V0 + st * PL::VB;
-                        if (!*abort_cta && PL::kV32Agg) {
-                            // S | z += phiK^T [V | ONES]: V in 32-byte swizzle, ONES its last block
+                        if (!*abort_cta && PL::kOnesAgg) {
+                            // S | z += phiK^T [V | ONES]: the shared ONES block is the second
+                            // 64-column block of the operand, lbo bytes after this V slot
                             constexpr uint32_t id_kv = idesc_bf16(128, PL::NQ16, 1, 1);
+                            const uint32_t lbo_ones = base + PL::ONES0 - va;
 #pragma unroll
                             for (int k = 0; k < kC; k += 16)
                                 mma_bf16_ss(dS, sw128_desc(ka + (k / 8) * 1024, lbo_kT, 1024),
-                                            sw32_desc(va + (k / 8) * 256, kC * 32, 256), id_kv,
+                                            sw128_desc(va + (k / 8) * 1024, lbo_ones, 1024), id_kv,
                                             (c > 0 || k > 0) ? 1u : 0u);
                         } else if (!*abort_cta) {
                             // (V in 128-byte swizzle here; z from the slot's ONES block)
@@ -1872,8 +1885,7 @@ cudaError_t run_causal(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
         Geo ga = g;
         ga.n_items = g.BH * (g.nseg - 1);
         tc_causal_kernel<DP, DV, true, AMODE><<<min(ga.n_items, sms), kThreads, Plan<DP, DV, true>::SMEM, s>>>(
-            tq, tk, Plan<DP, DV, true>::kV32Agg ? tv : tv_agg, to, ga, sc, (__nv_bfloat16 *)out, nullptr, nullptr,
-            err);
+            tq, tk, tv_agg, to, ga, sc, (__nv_bfloat16 *)out, nullptr, nullptr, err);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         const int sz = DP * DV + DP;
         if ((e = launch_dependent(seg_scan_kernel, dim3(cdiv(sz, 256), (unsigned)g.BH), dim3(256), 0, s, sc.preS,
@@ -2001,13 +2013,11 @@ cudaError_t run_elu(const Problem &p, void *scratch, float *S_out, float *z_out,
     float *totz = totS + (size_t)g.BH * DP * DV;
     if (g.nseg <= kNcFoldSegs) {
         // few segments per head: the readout adds them up (no totals kernel)
-        cudaError_t e = run_totals<DP, DV, kModeElu>(tq, tk, Plan<DP, DV, true>::kV32Agg ? tv : tva, to, g, scratch,
-                                                     totS, totz, DP, 0, err, s, false);
+        cudaError_t e = run_totals<DP, DV, kModeElu>(tq, tk, tva, to, g, scratch, totS, totz, DP, 0, err, s, false);
         if (e == cudaSuccess) e = run_readout<DP, DV, true>(tq, to, g, scratch, nullptr, nullptr, err, s, S_out, z_out);
         return e;
     }
-    cudaError_t e = run_totals<DP, DV, kModeElu>(tq, tk, Plan<DP, DV, true>::kV32Agg ? tv : tva, to, g, scratch,
-                                                 totS, totz, DP, 0, err, s);
+    cudaError_t e = run_totals<DP, DV, kModeElu>(tq, tk, tva, to, g, scratch, totS, totz, DP, 0, err, s);
     if (e == cudaSuccess) e = run_readout<DP, DV, true>(tq, to, g, scratch, totS, totz, err, s);
     if (e == cudaSuccess) e = export_totals(S_out, z_out, totS, totz, g.BH, DP, DV, s);
     return e;
